@@ -1,0 +1,453 @@
+"""Benchmark of the KVpop hot path on GB300.
+
+Default workload: the Qwen3-4B-like layer prefill (b=1, 8 KV heads, 32 query
+heads, D=128, S=16384, budget s=16 w=512 k=1520).  One step = the whole hot
+path over the batch: kvpop_mask, sparse attention forward, dense teacher LSE
+and the future-attention target.  The fixed-budget decode workload (64
+sequences, B=2048, 8192-token prefix, one token per step) is timed in the same
+run and reported in the "decode" object.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kvpop|reference]
+
+Under torchrun every rank runs its own replica (weak scaling, no data-path
+collective); the step time is the max over ranks.  `--impl reference` times the
+fp64 CPU oracle on a bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "prefill tokens/s (sparse attn + future target) & decode tokens/s; % of roofline"
+LAUNCHES_MASK = 4 * 3 + 1 + 1 + 1 + 2   # radix passes, wavelet, tau, evict_at, lists
+LAUNCHES_STEP = LAUNCHES_MASK + 1 + 1 + 2  # + sparse attention, dense LSE, target (prep + kernel)
+LAUNCHES_DECODE_STEP = 3
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="kvpop", choices=["kvpop", "reference"])
+    ap.add_argument("--workload", default="qwen3-4b-layer-prefill")
+    ap.add_argument("--decode-steps", type=int, default=4096)
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+
+REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+           0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+           0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+
+
+class ClockSampler:
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 3:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = max(mx, float(parts[1]))
+                bits = int(parts[2], 16)
+            except ValueError:
+                continue
+            for bit, name in REASONS.items():
+                if bits & bit and name != "gpu_idle":
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": mx or None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+
+def prefill_flops(wl, masks_ev=None):
+    """Useful work per step (algorithmic): sparse fwd 4*D per retained (q, t, head);
+    dense LSE-only 2*D per causal pair; target 2*D per pair with d >= t + w."""
+    S, D, Hq, B, w = wl.S, wl.D, wl.Hq, wl.B, wl.w
+    q = np.arange(S, dtype=np.float64)
+    sparse = 4.0 * D * Hq * wl.b * np.minimum(q + 1, B).sum()
+    dense = 2.0 * D * Hq * wl.b * S * (S + 1) / 2
+    target = 2.0 * D * Hq * wl.b * np.maximum(0, S - q - w).sum()
+    return {"sparse_attn": sparse, "dense_lse": dense, "future_target": target}
+
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    from fixed_budget_kv_gb300 import kvpop, synth
+
+    import __graft_entry__
+    __graft_entry__.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    wl = synth.PREFILL_WORKLOADS[args.workload]
+    q, k, v, prio = synth.make_prefill_device(wl, dev)
+    b, S, H, D = wl.b, wl.S, wl.H, wl.D
+    bud = (wl.s, wl.w, wl.k)
+    ws_mask = torch.empty(kvpop.mask_workspace_size(b, H, S, *bud), dtype=torch.uint8, device=dev)
+    ws_tgt = torch.empty(kvpop.target_workspace_size(b, S, wl.Hq, H), dtype=torch.uint8, device=dev)
+    rank_t = torch.empty((b, H, S), dtype=torch.int32, device=dev)
+    tau_t, ev_t = torch.empty_like(rank_t), torch.empty_like(rank_t)
+    lists = torch.empty((b, H, (S + 63) // 64, wl.k), dtype=torch.int32, device=dev)
+    O = torch.empty_like(q)
+    lse_s = torch.empty((b, wl.Hq, S), dtype=torch.float32, device=dev)
+    lse_d = torch.empty_like(lse_s)
+    target = torch.empty((b, H, S), dtype=torch.float32, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    def step(ev=None):
+        if ev:
+            ev[0].record()
+        kvpop.mask(prio, *bud, workspace=ws_mask, out=(rank_t, tau_t, ev_t, lists))
+        if ev:
+            ev[1].record()
+        kvpop.attn_fwd(q, k, v, 0.0, ev_t, lists, bud, out=(O, lse_s))
+        if ev:
+            ev[2].record()
+        kvpop.attn_fwd(q, k, None, 0.0, want_o=False, out=(None, lse_d))
+        if ev:
+            ev[3].record()
+        kvpop.future_target(q, k, lse_d, wl.w, workspace=ws_tgt, out=target)
+        if ev:
+            ev[4].record()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st, words = kvpop.device_status(reset=True)
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {words}")
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        for i in range(args.steps):
+            flush.zero_()             # L2 flush between timed steps (outside the step's events)
+            step(evs[i])
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    per_pass = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(4)] for i in range(args.steps)])
+    step_ms = float(per_pass.sum(axis=1).mean())
+    pass_ms = per_pass.mean(axis=0)
+    st, words = kvpop.device_status(reset=True)
+    if st != 0:
+        raise RuntimeError(f"device status after timing: {words}")
+
+    t = torch.tensor([step_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    step_ms_max = float(t.item())
+    tokens = b * S
+    value = world * tokens / (step_ms_max / 1e3)
+
+    flops = prefill_flops(wl)
+    pk = peaks()
+    names = ["mask", "sparse_attn", "dense_lse", "future_target"]
+    times = dict(zip(names, pass_ms.tolist()))
+    dom = max(["sparse_attn", "dense_lse", "future_target"], key=lambda n: times[n])
+    achieved = flops[dom] / (times[dom] / 1e3) / 1e12
+    passes = {n: {"ms": round(times[n], 4)} for n in names}
+    for n in ("sparse_attn", "dense_lse", "future_target"):
+        passes[n]["tflops"] = round(flops[n] / (times[n] / 1e3) / 1e12, 1)
+        passes[n]["frac_of_sustained_bf16"] = round(flops[n] / (times[n] / 1e3) / 1e12 / pk["bf16_tflops_sustained"], 3)
+
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms_max, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded counter-based generator; shapes of the Qwen3-4B-like layer)",
+        "config": {"workload": wl.name, "batch": b, "seq_len": S, "kv_heads": H, "q_heads": wl.Hq,
+                   "head_dim": D, "budget": {"s": wl.s, "w": wl.w, "k": wl.k},
+                   "l2": "flushed between timed steps (512 MB write)",
+                   "parallelism": f"replicas x{world}"},
+        "passes_ms": passes,
+        "roofline": {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1),
+                     "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                     "frac": round(achieved / pk["bf16_tflops_sustained"], 4), "traffic": None,
+                     "peak_kind": f"bf16 sustained, {pk['source']}",
+                     "algorithmic_flops_per_launch": flops[dom]},
+        "gpu_launches": LAUNCHES_STEP * args.steps,
+        "clocks": clk.summary(),
+    }
+
+    if not args.no_e2e:
+        result["e2e"] = e2e(args, wl, q, k, v, prio, ws_mask, ws_tgt, dev, world)
+    if not args.no_decode:
+        result["decode"] = run_decode(args, dev, pk)
+        result["gpu_launches"] += LAUNCHES_DECODE_STEP * result["decode"]["steps"]
+    del q, k, v, O
+    return result
+
+
+def e2e(args, wl, q, k, v, prio, ws_mask, ws_tgt, dev, world):
+    """Same step through the C ABI with host buffers: pinned H2D of q/k/v/prio,
+    the pipeline, D2H of O and the targets, all inside the timed region."""
+    import torch
+    from fixed_budget_kv_gb300 import kvpop
+    hq, hk, hv, hp = (t.cpu().pin_memory() for t in (q, k, v, prio))
+    b, S, H = wl.b, wl.S, wl.H
+    bud = (wl.s, wl.w, wl.k)
+    dq, dk, dv, dp = (torch.empty_like(t) for t in (q, k, v, prio))
+    hO = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    ht = torch.empty((b, H, S), dtype=torch.float32).pin_memory()
+
+    def step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        dp.copy_(hp, non_blocking=True)
+        _, _, ev, lists = kvpop.mask(dp, *bud, workspace=ws_mask)
+        O, _ = kvpop.attn_fwd(dq, dk, dv, 0.0, ev, lists, bud)
+        _, lse = kvpop.attn_fwd(dq, dk, None, 0.0, want_o=False)
+        tg = kvpop.future_target(dq, dk, lse, wl.w, workspace=ws_tgt)
+        hO.copy_(O, non_blocking=True)
+        ht.copy_(tg, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = max(3, args.steps // 2)
+    e0.record()
+    for _ in range(n):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    ms = float(t.item())
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hp))
+    d2h = hO.numel() * hO.element_size() + ht.numel() * ht.element_size()
+    return {"value": round(world * b * S / (ms / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": n}
+
+
+def run_decode(args, dev, pk):
+    import torch
+    from fixed_budget_kv_gb300 import kvpop, synth
+    wl = synth.DECODE
+    steps = args.decode_steps
+    n, H, G, D, P = wl.n, wl.H, wl.G, wl.D, wl.P
+    kp = synth.normal_bf16_torch(wl.seed, synth.K, (n, P, H, D), dev)
+    vp = synth.normal_bf16_torch(wl.seed, synth.V, (n, P, H, D), dev)
+    pp = torch.from_numpy(synth.priorities("uniform", wl.seed, (n, H, P))).to(dev)
+    qn = synth.normal_bf16_torch(wl.seed, synth.QN, (steps, n, wl.Hq, D), dev)
+    kn = synth.normal_bf16_torch(wl.seed, synth.KN, (steps, n, H, D), dev)
+    vn = synth.normal_bf16_torch(wl.seed, synth.VN, (steps, n, H, D), dev)
+    pn = torch.from_numpy(synth.priorities("uniform", wl.seed, (steps, n, H), stream=synth.PRION)).to(dev)
+    _, _, ev, _ = kvpop.mask(pp, wl.s, wl.w, wl.k, lists=False)
+    O = torch.empty((n, wl.Hq, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((n, wl.Hq), dtype=torch.float32, device=dev)
+    evd = torch.empty((n, H), dtype=torch.int32, device=dev)
+    cache = kvpop.Cache(n, H, G, D, wl.s, wl.w, wl.k)
+    # warm-up on a throw-away cache state, then reload the prefix
+    cache.prefill(kp, vp, pp, ev)
+    for i in range(min(8, steps)):
+        cache.step(qn[i], kn[i], vn[i], pn[i], out=(O, lse, evd))
+    cache.prefill(kp, vp, pp, ev)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(steps):
+        cache.step(qn[i], kn[i], vn[i], pn[i], out=(O, lse, evd))
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    cache.close()
+    bytes_step = n * H * wl.B * D * 2 * 2
+    gbs = bytes_step / (ms / 1e3) / 1e9
+    return {"workload": wl.name, "sequences": n, "budget": {"s": wl.s, "w": wl.w, "k": wl.k}, "prefix": P,
+            "steps": steps, "us_per_step": round(ms * 1e3, 2), "value": round(n / (ms / 1e3), 1),
+            "unit": "tokens/s",
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(gbs / pk["hbm_gbs"], 4), "traffic": None,
+                         "algorithmic_bytes_per_step": bytes_step,
+                         "note": "whole step (update + split attention + combine) timed with CUDA events"}}
+
+
+# ----------------------------------------------------------------------------
+# CPU baseline: the fp64 oracle on a bounded sample of the same workload
+# ----------------------------------------------------------------------------
+
+_CPU_DATA = {}
+
+
+def _cpu_data(wl):
+    """Host inputs for the oracle sample (generated once per process)."""
+    if wl.name not in _CPU_DATA:
+        from fixed_budget_kv_gb300 import synth
+        S, H, Hq, D = wl.S, wl.H, wl.Hq, wl.D
+        prio = synth.priorities(wl.prio, wl.seed, (wl.b, wl.H, wl.S))
+        kf = synth.bf16_bits_to_f32(synth.bf16_block(wl.seed, synth.K, (1, S, H, D), 0, wl.k_scale))
+        vf = synth.bf16_bits_to_f32(synth.bf16_block(wl.seed, synth.V, (1, S, H, D), 0))
+        qf = synth.bf16_bits_to_f32(synth.bf16_block(wl.seed, synth.Q, (1, S, Hq, D), 0))
+        _CPU_DATA[wl.name] = (prio, qf, kf, vf)
+    return _CPU_DATA[wl.name]
+
+
+def cpu_sample(wl, seed=0, nrows=1024, nkeys=96):
+    """Times the oracle on sampled units of the workload and scales to tokens/s.
+
+    Units per token (one query position of one batch row): Hq sparse-attention
+    rows, Hq dense-LSE rows, H target keys and H mask positions."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    S, H, G, Hq, D = wl.S, wl.H, wl.G, wl.Hq, wl.D
+    prio, qf, kf, vf = _cpu_data(wl)
+    scale = 1 / math.sqrt(D)
+    t0 = time.perf_counter()
+    r, tau, _ = oracle.mask(prio, wl.s, wl.w, wl.k)
+    t_mask = (time.perf_counter() - t0) / (wl.b * H * S)          # per (position, head)
+    qp = rng.integers(0, S, nrows)
+    j = rng.integers(0, Hq, nrows)
+    rows = np.stack([np.zeros(nrows, int), j, qp], axis=1).astype(np.int32)
+    qv = qf[0, qp, j]
+    t0 = time.perf_counter()
+    oracle.attn_rows(qv, kf, vf, G, scale, rows, r[:1], tau[:1], wl.s, wl.w)
+    t_sparse = (time.perf_counter() - t0) / nrows
+    t0 = time.perf_counter()
+    oracle.attn_rows(qv, kf, vf, G, scale, rows, want_o=False)
+    t_dense = (time.perf_counter() - t0) / nrows
+    # target keys: the cost is (S - t - w) query rows x G heads whatever the LSE values
+    lse0 = np.zeros((1, Hq, S))
+    keys = np.stack([np.zeros(nkeys, int), rng.integers(0, H, nkeys), rng.integers(0, S, nkeys)], axis=1)
+    t0 = time.perf_counter()
+    oracle.target_lse(qf, kf, lse0, wl.w, scale, keys.astype(np.int32))
+    t_tgt_sample = time.perf_counter() - t0
+    mean_work = np.maximum(0, S - keys[:, 2] - wl.w).mean()
+    avg_work = np.maximum(0, S - np.arange(S) - wl.w).mean()
+    t_target = t_tgt_sample / nkeys * (avg_work / max(mean_work, 1.0))
+    per_token = Hq * (t_sparse + t_dense) + H * (t_target + t_mask)
+    sample = (f"{wl.name}: mask of all {wl.b * H} heads; {nrows} sparse and {nrows} dense attention rows; "
+              f"{nkeys} target keys (scaled by their share of the causal work); per token = "
+              f"{Hq} x (sparse + dense row) + {H} x (target key + mask position)")
+    return 1.0 / per_token, sample
+
+
+def run_reference(args):
+    """The reference arm: the fp64 oracle on the host cores, one bounded sample per step."""
+    from fixed_budget_kv_gb300 import synth
+    import oracle
+    oracle.build()
+    wl = synth.PREFILL_WORKLOADS[args.workload]
+    vals = []
+    sample = ""
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        v, sample = cpu_sample(wl, seed=i, nrows=512, nkeys=48)
+        if i >= args.warmup:
+            vals.append((v, time.perf_counter() - t0))
+    value = float(np.median([v for v, _ in vals]))
+    cores = oracle.num_threads()
+    ms = 1e3 * wl.b * wl.S / value
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "batch": wl.b, "seq_len": wl.S, "kv_heads": wl.H, "q_heads": wl.Hq,
+                       "head_dim": wl.D, "budget": {"s": wl.s, "w": wl.w, "k": wl.k}},
+            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    # the CPU baseline runs before the first CUDA call (the oracle uses OpenMP threads)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        import oracle
+        from fixed_budget_kv_gb300 import synth
+        oracle.build()
+        v, sample = cpu_sample(synth.PREFILL_WORKLOADS[args.workload])
+        cpu = {"value": round(v, 3), "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+               "sample": sample}
+    if world > 1:
+        import torch
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    res = run_gpu(args, rank, world, local_rank)
+    if cpu is not None:
+        res["cpu_baseline"] = cpu
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,647 @@
+// kvpop_attn_fwd: causal GQA attention over the fixed-budget retained set
+// (sparse) or over all past tokens (dense teacher), returning O and the
+// log-sum-exp ("KVpop ... 精读笔记", sections 2.1 and 2.3).
+//
+// One CTA owns two 128-row query tiles of one (batch, KV head).  A row is one
+// (position, query head) pair: the G query heads of a KV head share every K/V
+// tile, so a tile covers 128/G positions.  Warp roles (384 threads):
+//   warp 0      TMA producer (Q; K/V in dense mode) and, in sparse mode, the
+//               key metadata (position, eviction row) of each KV tile
+//   warp 1      TMEM allocation and the single-thread tcgen05.mma issuer
+//   warps 2-3   sparse mode: gather of the retained K/V rows with cp.async
+//               into the 128-byte-swizzled operand layout
+//   warps 4-7   softmax for query tile 0 (one thread per row / TMEM lane)
+//   warps 8-11  softmax for query tile 1
+// S = Q K^T lands in TMEM (fp32); the softmax warps turn it into bf16 P in
+// place and the MMA warp accumulates O += P V with A read from TMEM.  The two
+// query tiles ping-pong so that the tensor core works on one tile while the
+// softmax warps work on the other.  Running max updates are lazy: O and the
+// row sum are rescaled only when the max grows by more than 2^8.
+#include "common.cuh"
+
+namespace kvpop {
+namespace {
+
+constexpr int kThreads = 384;
+constexpr int kKeys = 128;
+constexpr int kMetaStages = 4;
+constexpr int kBlockBytes = 128 * 128;  // 128 rows x 128 bytes
+constexpr float kRescaleLog2 = 8.0f;
+
+struct AttnParams {
+  CUtensorMap tq, tk, tv;
+  const __nv_bfloat16* k;
+  const __nv_bfloat16* v;
+  const int32_t* evict_at;
+  const int32_t* lists;
+  __nv_bfloat16* O;
+  float* lse;
+  int* status;
+  int S, Hq, H, G, P, nqb;
+  int s, w, kk, nL;
+  float scale_log2;
+};
+
+template <int D, bool WITH_O, bool SPARSE>
+struct Layout {
+  static constexpr int DH = D / 64;
+  static constexpr int NS = WITH_O ? (D == 128 ? 2 : 4) : (D == 128 ? 4 : 8);
+  static constexpr int q_off = 0;
+  static constexpr int k_off = q_off + 2 * DH * kBlockBytes;
+  static constexpr int v_off = k_off + NS * DH * kBlockBytes;
+  static constexpr int meta_off = v_off + (WITH_O ? NS * DH * kBlockBytes : 0);
+  static constexpr int bar_off = meta_off + (SPARSE ? kMetaStages * kKeys * 8 : 0);
+  // barrier block
+  static constexpr int nbar = 1 + 4 * NS + 4 + 4 + 2 + 1 + 2 * kMetaStages + 1;
+  static constexpr int misc_off = bar_off + nbar * 8;
+  static constexpr int total = misc_off + 64 + 1024;  // + alignment slack
+};
+
+template <int NS>
+struct Bars {
+  uint64_t q_full;
+  uint64_t k_full[NS], k_empty[NS], v_full[NS], v_empty[NS];
+  uint64_t s_full[2][2], s_empty[2][2];
+  uint64_t p_full[2];
+  uint64_t o_final;
+  uint64_t meta_full[kMetaStages], meta_empty[kMetaStages];
+  uint64_t drain;
+};
+
+__device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
+
+template <int D, bool WITH_O, bool SPARSE>
+__global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant__ AttnParams p) {
+  using L = Layout<D, WITH_O, SPARSE>;
+  constexpr int DH = L::DH;
+  constexpr int NS = L::NS;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  Bars<NS>* bars = reinterpret_cast<Bars<NS>*>(smem + L::bar_off);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::misc_off);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::misc_off + 4);
+  int2* meta = reinterpret_cast<int2*>(smem + L::meta_off);
+  const uint32_t sbase = smem_u32(smem);
+
+  const int warp = warp_id(), lane = lane_id();
+  const int b = blockIdx.z, h = blockIdx.y;
+  const int S = p.S, G = p.G, P = p.P;
+  const int qblock = SPARSE ? (int)blockIdx.x : (p.nqb - 1 - (int)blockIdx.x);
+  const int qb0 = qblock * 2 * P;
+  const int qb1 = min(qb0 + 2 * P, S) - 1;
+
+  // keys of this CTA: [sinks][long-range list][contiguous span] or [0, qb1]
+  int n_sink = 0, n_list = 0, sp0 = 0, NK;
+  const int32_t* list = nullptr;
+  if (SPARSE) {
+    const int jl = qb0 / KVPOP_LIST_QBLOCK;
+    const int q0l = jl * KVPOP_LIST_QBLOCK;
+    n_sink = min(p.s, qb1 + 1);
+    n_list = p.kk > 0 ? min(p.kk, max(0, q0l - p.w - p.s + 1)) : 0;
+    list = p.lists + ((size_t)(b * p.H + h) * p.nL + jl) * (size_t)max(p.kk, 1);
+    sp0 = max(p.s, q0l - p.w + 1);
+    NK = n_sink + n_list + max(0, qb1 - sp0 + 1);
+  } else {
+    NK = qb1 + 1;
+  }
+  const int NT = (NK + kKeys - 1) / kKeys;
+  auto key_pos = [&](int i) -> int {
+    int pos = -1;
+    if (i < n_sink) pos = i;
+    else if (i < n_sink + n_list) pos = __ldg(list + (i - n_sink));
+    else if (i < NK) pos = sp0 + (i - n_sink - n_list);
+    if (pos >= S || pos < -1) {  // a corrupt list entry: never read outside [0, S)
+      report_error(p.status, KVPOP_ERR_INTERNAL, SITE_INTERNAL_CHECK, 10);
+      pos = -1;
+    }
+    return pos;
+  };
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&bars->k_full[i], SPARSE ? 64 : 1);
+      mbar_init(&bars->v_full[i], SPARSE ? 64 : 1);
+      mbar_init(&bars->k_empty[i], 1);
+      mbar_init(&bars->v_empty[i], 1);
+    }
+    for (int a = 0; a < 2; ++a)
+      for (int c = 0; c < 2; ++c) {
+        mbar_init(&bars->s_full[a][c], 1);
+        mbar_init(&bars->s_empty[a][c], 4);
+      }
+    mbar_init(&bars->p_full[0], 4);
+    mbar_init(&bars->p_full[1], 4);
+    mbar_init(&bars->o_final, 1);
+    for (int i = 0; i < kMetaStages; ++i) {
+      mbar_init(&bars->meta_full[i], 1);
+      mbar_init(&bars->meta_empty[i], 8);
+    }
+    mbar_init(&bars->drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  auto fail = [&](int site, int detail) {
+    report_error(p.status, KVPOP_ERR_TIMEOUT, site, detail);
+    *abort_flag = 1;
+  };
+
+  const uint32_t q_addr = sbase + L::q_off;
+  const uint32_t k_addr = sbase + L::k_off;
+  const uint32_t v_addr = sbase + L::v_off;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&p.tq);
+      mbar_arrive_expect_tx(&bars->q_full, 2 * DH * kBlockBytes);
+      for (int qt = 0; qt < 2; ++qt)
+        for (int dh = 0; dh < DH; ++dh)
+          tma_load_4d(smem + L::q_off + (qt * DH + dh) * kBlockBytes, &p.tq, &bars->q_full, dh * 64,
+                      h * G, qb0 + qt * P, b);
+    }
+    if (!SPARSE) {
+      if (lane == 0) {
+        for (int j = 0; j < NT; ++j) {
+          const int st = j % NS;
+          const uint32_t ph = (j / NS) & 1;
+          if (!mbar_wait(&bars->k_empty[st], ph ^ 1, abort_flag)) {
+            fail(SITE_ATTN_PRODUCER, 1);
+            break;
+          }
+          mbar_arrive_expect_tx(&bars->k_full[st], DH * kBlockBytes);
+          for (int dh = 0; dh < DH; ++dh)
+            tma_load_4d(smem + L::k_off + (st * DH + dh) * kBlockBytes, &p.tk, &bars->k_full[st],
+                        dh * 64, h, j * kKeys, b);
+          if (WITH_O) {
+            if (!mbar_wait(&bars->v_empty[st], ph ^ 1, abort_flag)) {
+              fail(SITE_ATTN_PRODUCER, 2);
+              break;
+            }
+            mbar_arrive_expect_tx(&bars->v_full[st], DH * kBlockBytes);
+            for (int dh = 0; dh < DH; ++dh)
+              tma_load_4d(smem + L::v_off + (st * DH + dh) * kBlockBytes, &p.tv, &bars->v_full[st],
+                          dh * 64, h, j * kKeys, b);
+          }
+        }
+      }
+    } else {
+      const int32_t* ev = p.evict_at + (size_t)(b * p.H + h) * S;
+      for (int j = 0; j < NT; ++j) {
+        const int ms = j % kMetaStages;
+        if (!warp_wait(&bars->meta_empty[ms], ((j / kMetaStages) & 1) ^ 1, abort_flag)) {
+          if (lane == 0) fail(SITE_ATTN_PRODUCER, 3);
+          break;
+        }
+        for (int e = lane; e < kKeys; e += 32) {
+          const int pos = key_pos(j * kKeys + e);
+          meta[ms * kKeys + e] = pos >= 0 ? make_int2(pos, __ldg(ev + pos)) : make_int2(0x7fffffff, 0);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->meta_full[ms]);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      bool ok = mbar_wait(&bars->q_full, 0, abort_flag);
+      if (!ok) fail(SITE_ATTN_MMA, 1);
+      tc_fence_after();
+      constexpr uint32_t idesc_qk = idesc_bf16(128, 128, 0);
+      constexpr uint32_t idesc_pv = idesc_bf16(128, D, 1);
+      auto issue_s = [&](int qt, int st, uint32_t d_tmem) {
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const int dh = ks >> 2;
+          const uint32_t w32 = (uint32_t)(ks & 3) * 32;
+          const uint64_t a = smem_desc_sw128(q_addr + (qt * DH + dh) * kBlockBytes + w32, 16, 1024);
+          const uint64_t bd = smem_desc_sw128(k_addr + (st * DH + dh) * kBlockBytes + w32, 16, 1024);
+          mma_ss(d_tmem, a, bd, idesc_qk, ks > 0 ? 1u : 0u);
+        }
+      };
+      auto wait_kv = [&](uint64_t* bar, uint32_t ph, int detail) -> bool {
+        if (!mbar_wait(bar, ph, abort_flag)) {
+          fail(SITE_ATTN_MMA, detail);
+          return false;
+        }
+        if (SPARSE) fence_proxy_async_smem();
+        tc_fence_after();
+        return true;
+      };
+      if (ok && WITH_O) {
+        // S tiles at columns 0 / 128, O tiles at 256 / 384
+        if (NT > 0) {
+          ok = wait_kv(&bars->k_full[0], 0, 2);
+          if (ok) {
+            issue_s(0, 0, tbase + 0);
+            mma_commit(&bars->s_full[0][0]);
+            issue_s(1, 0, tbase + 128);
+            mma_commit(&bars->s_full[1][0]);
+            mma_commit(&bars->k_empty[0]);
+          }
+        }
+        for (int j = 0; ok && j < NT; ++j) {
+          const int st = j % NS;
+          const uint32_t ph = (j / NS) & 1;
+          for (int qt = 0; qt < 2 && ok; ++qt) {
+            if (!mbar_wait(&bars->p_full[qt], j & 1, abort_flag)) {
+              fail(SITE_ATTN_MMA, 3);
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            if (qt == 0 && !(ok = wait_kv(&bars->v_full[st], ph, 4))) break;
+#pragma unroll
+            for (int ks = 0; ks < kKeys / 16; ++ks) {
+              const uint64_t bd = smem_desc_sw128(v_addr + st * DH * kBlockBytes + ks * 2048,
+                                                  DH > 1 ? kBlockBytes : 16, 1024);
+              mma_ts(tbase + 256 + 128 * qt, tbase + 128 * qt + ks * 8, bd, idesc_pv,
+                     (j > 0 || ks > 0) ? 1u : 0u);
+            }
+            if (qt == 1) mma_commit(&bars->v_empty[st]);
+            if (j + 1 < NT) {
+              const int st1 = (j + 1) % NS;
+              if (qt == 0 && !(ok = wait_kv(&bars->k_full[st1], ((j + 1) / NS) & 1, 5))) break;
+              issue_s(qt, st1, tbase + 128 * qt);
+              mma_commit(&bars->s_full[qt][0]);
+              if (qt == 1) mma_commit(&bars->k_empty[st1]);
+            }
+          }
+        }
+        mma_commit(&bars->o_final);
+      } else if (ok) {
+        for (int j = 0; j < NT; ++j) {
+          const int st = j % NS;
+          if (!wait_kv(&bars->k_full[st], (j / NS) & 1, 6)) break;
+          const int buf = j & 1;
+          bool ok2 = true;
+          for (int qt = 0; qt < 2; ++qt) {
+            if (!mbar_wait(&bars->s_empty[qt][buf], ((j >> 1) & 1) ^ 1, abort_flag)) {
+              fail(SITE_ATTN_MMA, 7);
+              ok2 = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(qt, st, tbase + 128 * (2 * qt + buf));
+            mma_commit(&bars->s_full[qt][buf]);
+          }
+          if (!ok2) break;
+          mma_commit(&bars->k_empty[st]);
+        }
+      }
+      // drain every issued MMA before teardown
+      mma_commit(&bars->drain);
+      mbar_wait(&bars->drain, 0, nullptr);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax
+    const int qt = (warp - 4) >> 2;
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const int p_row = row / G, g = row - p_row * G;
+    const int q = qb0 + qt * P + p_row;
+    const int jh = h * G + g;
+    const uint32_t tl = tbase + ((uint32_t)(quarter * 32) << 16);
+    const float sl2 = p.scale_log2;
+    float m_ref = neg_inf(), l = 0.0f;
+    bool ok = true;
+    if (WITH_O) {
+      const uint32_t s_col = 128 * qt, o_col = 256 + 128 * qt;
+      for (int j = 0; j < NT; ++j) {
+        if (!warp_wait(&bars->s_full[qt][0], j & 1, abort_flag)) {
+          if (lane == 0) fail(SITE_ATTN_SOFTMAX, 1);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int2* km = nullptr;
+        const int ms = j % kMetaStages;
+        if (SPARSE) {
+          if (!warp_wait(&bars->meta_full[ms], (j / kMetaStages) & 1, abort_flag)) {
+            if (lane == 0) fail(SITE_ATTN_SOFTMAX, 2);
+            ok = false;
+            break;
+          }
+          km = meta + ms * kKeys;
+        }
+        // pass 1: visibility bits and the tile max
+        uint32_t vis[4];
+        float mt = neg_inf();
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t r[32];
+          tmem_ld32(tl + s_col + ch * 32, r);
+          tmem_wait_ld();
+          uint32_t bits = 0;
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int col = ch * 32 + c;
+            bool visible;
+            if (SPARSE) {
+              const int2 m = km[col];
+              visible = (m.x <= q) && (q < m.y);
+            } else {
+              visible = (j * kKeys + col) <= q;
+            }
+            if (visible) {
+              bits |= 1u << c;
+              mt = fmaxf(mt, __uint_as_float(r[c]));
+            }
+          }
+          vis[ch] = bits;
+        }
+        // lazy rescale of the running max
+        const float m_new = fmaxf(m_ref, mt);
+        const bool need = (m_new - m_ref) * sl2 > kRescaleLog2;  // true when m_ref == -inf and mt finite
+        float alpha = 1.0f;
+        if (need) {
+          alpha = ex2_approx((m_ref - m_new) * sl2);
+          l *= alpha;
+          m_ref = m_new;
+        }
+        if (__any_sync(0xffffffffu, need) && j > 0) {
+#pragma unroll
+          for (int cd = 0; cd < D / 32; ++cd) {
+            uint32_t r[32];
+            tmem_ld32(tl + o_col + cd * 32, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * alpha);
+            tmem_st32(tl + o_col + cd * 32, r);
+          }
+          tmem_wait_st();
+        }
+        // pass 2: P = exp2(s * scale_log2 - m) as bf16, written over S
+        const float neg = (m_ref == neg_inf()) ? 0.0f : -m_ref * sl2;
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t r[32];
+          tmem_ld32(tl + s_col + ch * 32, r);
+          tmem_wait_ld();
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            float p0 = ((vis[ch] >> c) & 1u) ? ex2_approx(fmaf(__uint_as_float(r[c]), sl2, neg)) : 0.0f;
+            float p1 = ((vis[ch] >> (c + 1)) & 1u) ? ex2_approx(fmaf(__uint_as_float(r[c + 1]), sl2, neg))
+                                                   : 0.0f;
+            l += p0 + p1;
+            pk[c >> 1] = pack_bf16x2(p0, p1);
+          }
+          tmem_st16(tl + s_col + ch * 16, pk);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&bars->p_full[qt]);
+          if (SPARSE) mbar_arrive(&bars->meta_empty[ms]);
+        }
+      }
+      // epilogue: O / l and the LSE
+      if (ok) {
+        if (!warp_wait(&bars->o_final, 0, abort_flag)) {
+          if (lane == 0) fail(SITE_ATTN_EPILOGUE, 1);
+          ok = false;
+        }
+      }
+      if (ok) {
+        tc_fence_after();
+        const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+        __nv_bfloat16* orow = p.O + (((size_t)b * S + q) * p.Hq + jh) * D;
+#pragma unroll
+        for (int cd = 0; cd < D / 32; ++cd) {
+          uint32_t r[32];
+          tmem_ld32(tl + o_col + cd * 32, r);
+          tmem_wait_ld();
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 32; c += 2)
+            pk[c >> 1] = pack_bf16x2(__uint_as_float(r[c]) * inv, __uint_as_float(r[c + 1]) * inv);
+          if (q <= qb1) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + cd * 32);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              dst[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+          }
+        }
+        if (q <= qb1)
+          p.lse[((size_t)b * p.Hq + jh) * S + q] =
+              l > 0.0f ? (m_ref * sl2 + __log2f(l)) * 0.69314718055994531f : neg_inf();
+      }
+    } else {
+      for (int j = 0; j < NT; ++j) {
+        const int buf = j & 1;
+        if (!warp_wait(&bars->s_full[qt][buf], (j >> 1) & 1, abort_flag)) {
+          if (lane == 0) fail(SITE_ATTN_SOFTMAX, 3);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t s_col = 128 * (2 * qt + buf);
+        const bool diag = (j * kKeys + kKeys - 1) > qb0;
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t r[32];
+          tmem_ld32(tl + s_col + ch * 32, r);
+          tmem_wait_ld();
+          float x[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            x[c] = __uint_as_float(r[c]);
+            if (diag && (j * kKeys + ch * 32 + c) > q) x[c] = neg_inf();
+          }
+          float cm = x[0];
+#pragma unroll
+          for (int c = 1; c < 32; ++c) cm = fmaxf(cm, x[c]);
+          if ((cm - m_ref) * sl2 > kRescaleLog2) {
+            l *= ex2_approx((m_ref - cm) * sl2);
+            m_ref = cm;
+          }
+          if (m_ref != neg_inf()) {
+            const float neg = -m_ref * sl2;
+            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+            for (int c = 0; c < 32; c += 4) {
+              a0 += ex2_approx(fmaf(x[c], sl2, neg));
+              a1 += ex2_approx(fmaf(x[c + 1], sl2, neg));
+              a2 += ex2_approx(fmaf(x[c + 2], sl2, neg));
+              a3 += ex2_approx(fmaf(x[c + 3], sl2, neg));
+            }
+            l += (a0 + a1) + (a2 + a3);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->s_empty[qt][buf]);
+      }
+      if (ok && q <= qb1)
+        p.lse[((size_t)b * p.Hq + jh) * S + q] =
+            l > 0.0f ? (m_ref * sl2 + __log2f(l)) * 0.69314718055994531f : neg_inf();
+    }
+  } else if (SPARSE) {
+    // ------------------------------------------------------------ gather warps 2-3
+    constexpr int CH = D / 8;  // 16-byte chunks per row
+    constexpr int RSTEP = 64 / CH;
+    const int gt = (warp - 2) * 32 + lane;
+    const int c = gt % CH, rg = gt / CH;
+    const int dh = c >> 3, cc = c & 7;
+    const size_t kv_stride = (size_t)p.H * D;
+    const __nv_bfloat16* kb = p.k + ((size_t)b * S * p.H + h) * D + c * 8;
+    const __nv_bfloat16* vb = p.v + ((size_t)b * S * p.H + h) * D + c * 8;
+    for (int j = 0; j < NT; ++j) {
+      const int st = j % NS;
+      const uint32_t ph = (j / NS) & 1;
+      int pos[kKeys / RSTEP];
+#pragma unroll
+      for (int i = 0; i < kKeys / RSTEP; ++i) pos[i] = key_pos(j * kKeys + rg + i * RSTEP);
+      if (!mbar_wait(&bars->k_empty[st], ph ^ 1, abort_flag)) {
+        fail(SITE_ATTN_PRODUCER, 4);
+        break;
+      }
+      uint8_t* kdst = smem + L::k_off + (st * DH + dh) * kBlockBytes;
+#pragma unroll
+      for (int i = 0; i < kKeys / RSTEP; ++i) {
+        const int r = rg + i * RSTEP;
+        const bool valid = pos[i] >= 0;
+        cp_async_16(kdst + sw128_offset(r, cc), valid ? (const void*)(kb + (size_t)pos[i] * kv_stride)
+                                                       : (const void*)p.k,
+                    valid ? 16u : 0u);
+      }
+      cp_async_arrive_noinc(&bars->k_full[st]);
+      if (!mbar_wait(&bars->v_empty[st], ph ^ 1, abort_flag)) {
+        fail(SITE_ATTN_PRODUCER, 5);
+        break;
+      }
+      uint8_t* vdst = smem + L::v_off + (st * DH + dh) * kBlockBytes;
+#pragma unroll
+      for (int i = 0; i < kKeys / RSTEP; ++i) {
+        const int r = rg + i * RSTEP;
+        const bool valid = pos[i] >= 0;
+        cp_async_16(vdst + sw128_offset(r, cc), valid ? (const void*)(vb + (size_t)pos[i] * kv_stride)
+                                                       : (const void*)p.v,
+                    valid ? 16u : 0u);
+      }
+      cp_async_arrive_noinc(&bars->v_full[st]);
+    }
+    cp_async_wait_all();
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+template <int D, bool WITH_O, bool SPARSE>
+kvpop_status launch(const AttnParams& prm, int b, int H, cudaStream_t stream) {
+  using L = Layout<D, WITH_O, SPARSE>;
+  auto kern = attn_kernel<D, WITH_O, SPARSE>;
+  kvpop_status st = cuda_check(
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::total),
+      "kvpop_attn_fwd: smem attribute");
+  if (st != KVPOP_OK) return st;
+  dim3 grid(prm.nqb, H, b);
+  kern<<<grid, kThreads, L::total, stream>>>(prm);
+  return cuda_check(cudaGetLastError(), "kvpop_attn_fwd: launch");
+}
+
+}  // namespace
+}  // namespace kvpop
+
+using namespace kvpop;
+
+extern "C" kvpop_status kvpop_attn_fwd(const void* q, const void* k, const void* v, int b, int S,
+                                       int Hq, int H, int D, float scale, const int32_t* evict_at,
+                                       const int32_t* lists, kvpop_budget bud, void* O, float* lse,
+                                       kvpop_stream stream) {
+  if (!q || !k || !lse || (O && !v)) {
+    set_last_error("kvpop_attn_fwd: q, k, lse (and v when O is requested) must be non-NULL");
+    return KVPOP_ERR_INVALID_ARG;
+  }
+  if (b <= 0 || S <= 0 || H <= 0 || Hq <= 0 || Hq % H != 0) {
+    set_last_error("kvpop_attn_fwd: bad shape b=%d S=%d Hq=%d H=%d", b, S, Hq, H);
+    return KVPOP_ERR_INVALID_ARG;
+  }
+  const int G = Hq / H;
+  if (D != 64 && D != 128) {
+    set_last_error("kvpop_attn_fwd: D=%d unsupported (64 or 128)", D);
+    return KVPOP_ERR_UNSUPPORTED;
+  }
+  if (128 % G != 0) {
+    set_last_error("kvpop_attn_fwd: G=%d must divide 128", G);
+    return KVPOP_ERR_UNSUPPORTED;
+  }
+  if (b > 65535 || H > 65535) {
+    set_last_error("kvpop_attn_fwd: b and H must be <= 65535");
+    return KVPOP_ERR_UNSUPPORTED;
+  }
+  const bool sparse = evict_at != nullptr || lists != nullptr;
+  if (sparse) {
+    if (!evict_at || (!lists && bud.k > 0) || !O || !v) {
+      set_last_error("kvpop_attn_fwd: sparse mode needs evict_at, lists (k > 0), v and O");
+      return KVPOP_ERR_INVALID_ARG;
+    }
+    if (bud.s < 0 || bud.w < 0 || bud.k < 0 || (long long)bud.s + bud.w + bud.k < 1) {
+      set_last_error("kvpop_attn_fwd: invalid budget");
+      return KVPOP_ERR_INVALID_ARG;
+    }
+  }
+  const uintptr_t am = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                       reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(O);
+  if (am & 15) {
+    set_last_error("kvpop_attn_fwd: q, k, v, O must be 16-byte aligned");
+    return KVPOP_ERR_UNSUPPORTED;
+  }
+  AttnParams prm;
+  memset(&prm, 0, sizeof(prm));
+  const int P = 128 / G;
+  {
+    uint64_t dq[4] = {(uint64_t)D, (uint64_t)Hq, (uint64_t)S, (uint64_t)b};
+    uint64_t sq[3] = {(uint64_t)D * 2, (uint64_t)Hq * D * 2, (uint64_t)S * Hq * D * 2};
+    uint32_t bq[4] = {64, (uint32_t)G, (uint32_t)P, 1};
+    uint64_t dk[4] = {(uint64_t)D, (uint64_t)H, (uint64_t)S, (uint64_t)b};
+    uint64_t sk[3] = {(uint64_t)D * 2, (uint64_t)H * D * 2, (uint64_t)S * H * D * 2};
+    uint32_t bk[4] = {64, 1, 128, 1};
+    if (!make_tmap_4d(&prm.tq, q, dq, sq, bq) || !make_tmap_4d(&prm.tk, k, dk, sk, bk) ||
+        (v && !make_tmap_4d(&prm.tv, v, dk, sk, bk)))
+      return KVPOP_ERR_CUDA;
+  }
+  prm.k = static_cast<const __nv_bfloat16*>(k);
+  prm.v = static_cast<const __nv_bfloat16*>(v);
+  prm.evict_at = evict_at;
+  prm.lists = lists;
+  prm.O = static_cast<__nv_bfloat16*>(O);
+  prm.lse = lse;
+  prm.status = device_status_ptr();
+  prm.S = S;
+  prm.Hq = Hq;
+  prm.H = H;
+  prm.G = G;
+  prm.P = P;
+  prm.nqb = (S + 2 * P - 1) / (2 * P);
+  prm.s = bud.s;
+  prm.w = bud.w;
+  prm.kk = bud.k;
+  prm.nL = (S + KVPOP_LIST_QBLOCK - 1) / KVPOP_LIST_QBLOCK;
+  const float sc = scale > 0.0f ? scale : 1.0f / sqrtf((float)D);
+  prm.scale_log2 = sc * 1.4426950408889634f;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (sparse) {
+    return D == 128 ? launch<128, true, true>(prm, b, H, cs) : launch<64, true, true>(prm, b, H, cs);
+  }
+  if (O) return D == 128 ? launch<128, true, false>(prm, b, H, cs) : launch<64, true, false>(prm, b, H, cs);
+  return D == 128 ? launch<128, false, false>(prm, b, H, cs) : launch<64, false, false>(prm, b, H, cs);
+}

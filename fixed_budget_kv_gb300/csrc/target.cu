@@ -1,0 +1,377 @@
+// kvpop_future_target: the transposed-attention pass of "KVpop ... 精读笔记",
+// sections 2.2-2.3 (Eq. 8, Figure 2).  The future-attention mass of key t is a
+// column sum of the dense attention map; with keys as rows and queries as
+// columns it becomes a row sum that an attention-shaped kernel computes
+// without materialising the map:
+//   target[b,h,t] = log sum_{g<G} sum_{d>=t+w} exp(scale q_{d,hG+g}.k_t - LSE_{d,hG+g}).
+// Every term is a probability (<= 1), so a plain fp32 sum needs no running max.
+//
+// One CTA owns two 128-key row tiles of one (batch, KV head); it streams the
+// query tiles (128/G positions x G heads = 128 columns) that can see them.
+// Warp roles (384 threads): warp 0 TMA producer (K once, Q tiles, the LSE of
+// each query tile pre-scaled to log2 units), warp 1 TMEM allocation and MMA
+// issuer, warps 4-7 / 8-11 the exp-and-sum for row tile 0 / 1.  S' = K Q^T is
+// double-buffered in TMEM per row tile (4 x 128 columns).
+#include "common.cuh"
+
+namespace kvpop {
+namespace {
+
+constexpr int kThreads = 384;
+constexpr int kBlockBytes = 128 * 128;
+constexpr int kLseStages = 4;
+
+struct TargetParams {
+  CUtensorMap tq, tk;
+  const float* lse2;  // [b, H, Spad, G] = LSE * log2(e), +inf past S
+  float* target;
+  int* status;
+  int S, Spad, H, G, logG, P, nct, w;
+  float scale_log2;
+};
+
+template <int D>
+struct TLayout {
+  static constexpr int DH = D / 64;
+  static constexpr int NS = D == 128 ? 4 : 8;
+  static constexpr int k_off = 0;
+  static constexpr int q_off = k_off + 2 * DH * kBlockBytes;
+  static constexpr int lse_off = q_off + NS * DH * kBlockBytes;
+  static constexpr int bar_off = lse_off + kLseStages * 512;
+  static constexpr int nbar = 1 + 2 * NS + 8 + 2 * kLseStages + 1;
+  static constexpr int misc_off = bar_off + nbar * 8;
+  static constexpr int total = misc_off + 64 + 1024;
+};
+
+template <int NS>
+struct TBars {
+  uint64_t k_full;
+  uint64_t q_full[NS], q_empty[NS];
+  uint64_t s_full[2][2], s_empty[2][2];
+  uint64_t l_full[kLseStages], l_empty[kLseStages];
+  uint64_t drain;
+};
+
+__global__ void lse_prep(const float* __restrict__ lse, int b, int H, int G, int S, int Spad,
+                         float* __restrict__ lse2) {
+  const long long n = (long long)b * H * Spad * G;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int g = (int)(i % G);
+    long long r = i / G;
+    const int d = (int)(r % Spad);
+    r /= Spad;
+    const int h = (int)(r % H);
+    const int bi = (int)(r / H);
+    lse2[i] = d < S ? lse[((size_t)bi * H * G + (size_t)h * G + g) * S + d] * 1.4426950408889634f
+                    : __int_as_float(0x7f800000);
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) target_kernel(const __grid_constant__ TargetParams p) {
+  using L = TLayout<D>;
+  constexpr int DH = L::DH;
+  constexpr int NS = L::NS;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  TBars<NS>* bars = reinterpret_cast<TBars<NS>*>(smem + L::bar_off);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::misc_off);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::misc_off + 4);
+  const float* lse_s = reinterpret_cast<const float*>(smem + L::lse_off);
+  const uint32_t sbase = smem_u32(smem);
+
+  const int warp = warp_id(), lane = lane_id();
+  const int b = blockIdx.z, h = blockIdx.y;
+  const int t0 = blockIdx.x * 256;
+  const int S = p.S, P = p.P, G = p.G;
+  int c_start[2];
+  for (int rt = 0; rt < 2; ++rt) {
+    const long long first = (long long)t0 + 128 * rt + p.w;  // first visible query position
+    c_start[rt] = first > S - 1 ? p.nct : (int)(first / P);
+  }
+  const int c_begin = c_start[0];
+  const int NTc = p.nct - c_begin;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->k_full, 1);
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&bars->q_full[i], 1);
+      mbar_init(&bars->q_empty[i], 1);
+    }
+    for (int a = 0; a < 2; ++a)
+      for (int c = 0; c < 2; ++c) {
+        mbar_init(&bars->s_full[a][c], 1);
+        mbar_init(&bars->s_empty[a][c], 4);
+      }
+    for (int i = 0; i < kLseStages; ++i) {
+      mbar_init(&bars->l_full[i], 1);
+      mbar_init(&bars->l_empty[i], 8);
+    }
+    mbar_init(&bars->drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  auto fail = [&](int site, int detail) {
+    report_error(p.status, KVPOP_ERR_TIMEOUT, site, detail);
+    *abort_flag = 1;
+  };
+
+  if (warp == 0) {
+    if (lane == 0 && NTc > 0) {
+      tma_prefetch_desc(&p.tq);
+      mbar_arrive_expect_tx(&bars->k_full, 2 * DH * kBlockBytes);
+      for (int rt = 0; rt < 2; ++rt)
+        for (int dh = 0; dh < DH; ++dh)
+          tma_load_4d(smem + L::k_off + (rt * DH + dh) * kBlockBytes, &p.tk, &bars->k_full, dh * 64, h,
+                      t0 + 128 * rt, b);
+      const float* lsrc = p.lse2 + ((size_t)b * p.H + h) * (size_t)p.Spad * G;
+      for (int jc = 0; jc < NTc; ++jc) {
+        const int c = c_begin + jc;
+        const int st = jc % NS;
+        if (!mbar_wait(&bars->q_empty[st], ((jc / NS) & 1) ^ 1, abort_flag)) {
+          fail(SITE_TARGET_PRODUCER, 1);
+          break;
+        }
+        mbar_arrive_expect_tx(&bars->q_full[st], DH * kBlockBytes);
+        for (int dh = 0; dh < DH; ++dh)
+          tma_load_4d(smem + L::q_off + (st * DH + dh) * kBlockBytes, &p.tq, &bars->q_full[st], dh * 64,
+                      h * G, c * P, b);
+        const int ls = jc % kLseStages;
+        if (!mbar_wait(&bars->l_empty[ls], ((jc / kLseStages) & 1) ^ 1, abort_flag)) {
+          fail(SITE_TARGET_PRODUCER, 2);
+          break;
+        }
+        mbar_arrive_expect_tx(&bars->l_full[ls], 512);
+        bulk_load(smem + L::lse_off + ls * 512, lsrc + (size_t)c * P * G, 512, &bars->l_full[ls]);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && NTc > 0) {
+      bool ok = mbar_wait(&bars->k_full, 0, abort_flag);
+      if (!ok) fail(SITE_TARGET_MMA, 1);
+      tc_fence_after();
+      constexpr uint32_t idesc = idesc_bf16(128, 128, 0);
+      const uint32_t k_addr = sbase + L::k_off, q_addr = sbase + L::q_off;
+      int n_rt[2] = {0, 0};
+      for (int jc = 0; ok && jc < NTc; ++jc) {
+        const int c = c_begin + jc;
+        const int st = jc % NS;
+        if (!mbar_wait(&bars->q_full[st], (jc / NS) & 1, abort_flag)) {
+          fail(SITE_TARGET_MMA, 2);
+          break;
+        }
+        tc_fence_after();
+        for (int rt = 0; rt < 2; ++rt) {
+          if (c < c_start[rt]) continue;
+          const int n = n_rt[rt]++;
+          const int buf = n & 1;
+          if (!mbar_wait(&bars->s_empty[rt][buf], ((n >> 1) & 1) ^ 1, abort_flag)) {
+            fail(SITE_TARGET_MMA, 3);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tbase + 128 * (2 * rt + buf);
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const int dh = ks >> 2;
+            const uint32_t w32 = (uint32_t)(ks & 3) * 32;
+            const uint64_t a = smem_desc_sw128(k_addr + (rt * DH + dh) * kBlockBytes + w32, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(q_addr + (st * DH + dh) * kBlockBytes + w32, 16, 1024);
+            mma_ss(d_tmem, a, bd, idesc, ks > 0 ? 1u : 0u);
+          }
+          mma_commit(&bars->s_full[rt][buf]);
+        }
+        mma_commit(&bars->q_empty[st]);
+      }
+      mma_commit(&bars->drain);
+      mbar_wait(&bars->drain, 0, nullptr);
+    }
+  } else if (warp >= 4) {
+    const int rt = (warp - 4) >> 2;
+    const int quarter = warp & 3;
+    const int t = t0 + 128 * rt + quarter * 32 + lane;  // this thread's key
+    const uint32_t tl = tbase + ((uint32_t)(quarter * 32) << 16);
+    const float sl2 = p.scale_log2;
+    const int row_first = t0 + 128 * rt;
+    float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+    bool ok = true;
+    int n = 0;
+    for (int jc = 0; jc < NTc; ++jc) {
+      const int c = c_begin + jc;
+      const int ls = jc % kLseStages;
+      if (!warp_wait(&bars->l_full[ls], (jc / kLseStages) & 1, abort_flag)) {
+        if (lane == 0) fail(SITE_TARGET_SOFTMAX, 1);
+        ok = false;
+        break;
+      }
+      if (c >= c_start[rt]) {
+        const int buf = n & 1;
+        if (!warp_wait(&bars->s_full[rt][buf], (n >> 1) & 1, abort_flag)) {
+          if (lane == 0) fail(SITE_TARGET_SOFTMAX, 2);
+          ok = false;
+          break;
+        }
+        ++n;
+        tc_fence_after();
+        const float* l2 = lse_s + ls * 128;
+        const uint32_t s_col = 128 * (2 * rt + buf);
+        const bool masked = (long long)c * P < (long long)row_first + 127 + p.w;
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t r[32];
+          tmem_ld32(tl + s_col + ch * 32, r);
+          tmem_wait_ld();
+          if (!masked) {
+#pragma unroll
+            for (int cc = 0; cc < 32; cc += 4) {
+              const float4 lv = *reinterpret_cast<const float4*>(l2 + ch * 32 + cc);
+              acc0 += ex2_approx(fmaf(__uint_as_float(r[cc]), sl2, -lv.x));
+              acc1 += ex2_approx(fmaf(__uint_as_float(r[cc + 1]), sl2, -lv.y));
+              acc2 += ex2_approx(fmaf(__uint_as_float(r[cc + 2]), sl2, -lv.z));
+              acc3 += ex2_approx(fmaf(__uint_as_float(r[cc + 3]), sl2, -lv.w));
+            }
+          } else {
+#pragma unroll
+            for (int cc = 0; cc < 32; ++cc) {
+              const int col = ch * 32 + cc;
+              const int d = c * P + (col >> p.logG);
+              if (d >= t + p.w) acc0 += ex2_approx(fmaf(__uint_as_float(r[cc]), sl2, -l2[col]));
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->s_empty[rt][buf]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->l_empty[ls]);
+    }
+    if (ok && t < S) {
+      const float sum = (acc0 + acc1) + (acc2 + acc3);
+      p.target[((size_t)b * p.H + h) * S + t] =
+          sum > 0.0f ? __log2f(sum) * 0.69314718055994531f : __int_as_float(0xff800000);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+template <int D>
+kvpop_status launch_target(const TargetParams& prm, int b, int H, cudaStream_t cs) {
+  using L = TLayout<D>;
+  auto kern = target_kernel<D>;
+  kvpop_status st = cuda_check(
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::total),
+      "kvpop_future_target: smem attribute");
+  if (st != KVPOP_OK) return st;
+  dim3 grid((prm.S + 255) / 256, H, b);
+  kern<<<grid, kThreads, L::total, cs>>>(prm);
+  return cuda_check(cudaGetLastError(), "kvpop_future_target: launch");
+}
+
+}  // namespace
+}  // namespace kvpop
+
+using namespace kvpop;
+
+extern "C" kvpop_status kvpop_future_target_workspace_size(int b, int S, int Hq, int H,
+                                                           size_t* bytes) {
+  if (!bytes || b <= 0 || S <= 0 || H <= 0 || Hq <= 0 || Hq % H != 0) {
+    set_last_error("kvpop_future_target_workspace_size: bad arguments");
+    return KVPOP_ERR_INVALID_ARG;
+  }
+  const int G = Hq / H;
+  if (128 % G != 0) {
+    set_last_error("kvpop_future_target_workspace_size: G=%d must divide 128", G);
+    return KVPOP_ERR_UNSUPPORTED;
+  }
+  const int P = 128 / G;
+  const size_t spad = (size_t)((S + P - 1) / P) * P;
+  *bytes = (size_t)b * H * spad * G * sizeof(float);
+  return KVPOP_OK;
+}
+
+extern "C" kvpop_status kvpop_future_target(const void* q, const void* k, const float* lse, int b,
+                                            int S, int Hq, int H, int D, float scale, int w,
+                                            float* target, void* workspace, size_t ws_bytes,
+                                            kvpop_stream stream) {
+  if (!q || !k || !lse || !target || !workspace) {
+    set_last_error("kvpop_future_target: q, k, lse, target and workspace must be non-NULL");
+    return KVPOP_ERR_INVALID_ARG;
+  }
+  if (w < 0) {
+    set_last_error("kvpop_future_target: w must be >= 0");
+    return KVPOP_ERR_INVALID_ARG;
+  }
+  size_t need = 0;
+  kvpop_status st = kvpop_future_target_workspace_size(b, S, Hq, H, &need);
+  if (st != KVPOP_OK) return st;
+  if (ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 15)) {
+    set_last_error("kvpop_future_target: workspace needs %zu bytes, 16-byte aligned", need);
+    return KVPOP_ERR_INVALID_ARG;
+  }
+  if (D != 64 && D != 128) {
+    set_last_error("kvpop_future_target: D=%d unsupported (64 or 128)", D);
+    return KVPOP_ERR_UNSUPPORTED;
+  }
+  if (((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k)) & 15) != 0) {
+    set_last_error("kvpop_future_target: q and k must be 16-byte aligned");
+    return KVPOP_ERR_UNSUPPORTED;
+  }
+  if (b > 65535 || H > 65535) {
+    set_last_error("kvpop_future_target: b and H must be <= 65535");
+    return KVPOP_ERR_UNSUPPORTED;
+  }
+  const int G = Hq / H;
+  const int P = 128 / G;
+  TargetParams prm;
+  memset(&prm, 0, sizeof(prm));
+  {
+    uint64_t dq[4] = {(uint64_t)D, (uint64_t)Hq, (uint64_t)S, (uint64_t)b};
+    uint64_t sq[3] = {(uint64_t)D * 2, (uint64_t)Hq * D * 2, (uint64_t)S * Hq * D * 2};
+    uint32_t bq[4] = {64, (uint32_t)G, (uint32_t)P, 1};
+    uint64_t dk[4] = {(uint64_t)D, (uint64_t)H, (uint64_t)S, (uint64_t)b};
+    uint64_t sk[3] = {(uint64_t)D * 2, (uint64_t)H * D * 2, (uint64_t)S * H * D * 2};
+    uint32_t bk[4] = {64, 1, 128, 1};
+    if (!make_tmap_4d(&prm.tq, q, dq, sq, bq) || !make_tmap_4d(&prm.tk, k, dk, sk, bk))
+      return KVPOP_ERR_CUDA;
+  }
+  prm.S = S;
+  prm.nct = (S + P - 1) / P;
+  prm.Spad = prm.nct * P;
+  prm.H = H;
+  prm.G = G;
+  int lg = 0;
+  while ((1 << lg) < G) ++lg;
+  prm.logG = lg;
+  prm.P = P;
+  prm.w = w;
+  const float sc = scale > 0.0f ? scale : 1.0f / sqrtf((float)D);
+  prm.scale_log2 = sc * 1.4426950408889634f;
+  prm.lse2 = static_cast<const float*>(workspace);
+  prm.target = target;
+  prm.status = device_status_ptr();
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const long long n = (long long)b * H * prm.Spad * G;
+  const int blocks = (int)std::min<long long>((n + 255) / 256, 4096);
+  lse_prep<<<blocks, 256, 0, cs>>>(lse, b, H, G, S, prm.Spad, static_cast<float*>(workspace));
+  st = cuda_check(cudaGetLastError(), "kvpop_future_target: lse prep");
+  if (st != KVPOP_OK) return st;
+  return D == 128 ? launch_target<128>(prm, b, H, cs) : launch_target<64>(prm, b, H, cs);
+}

@@ -22,14 +22,17 @@ row-major layout, so a sub-block can be regenerated without the rest.
 """
 from __future__ import annotations
 
+import concurrent.futures
 import dataclasses
+import os
+
 import numpy as np
 
 _GOLDEN = np.uint64(0x9E3779B97F4A7C15)
 _STREAM_MUL = np.uint64(0xD1B54A32D192ED03)
 _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
-_CHUNK = 1 << 22
+_CHUNK = 1 << 21
 
 # stream ids
 Q, K, V, PRIO, SPIKE = 1, 2, 3, 4, 5
@@ -58,24 +61,35 @@ def raw_draws(seed: int, stream: int, start: int, count: int) -> np.ndarray:
         return _mix64(key + idx * _GOLDEN)
 
 
-def uniform24(seed: int, stream: int, n: int, start: int = 0) -> np.ndarray:
+def _chunked(n: int, fill) -> np.ndarray:
+    """Fill an fp32 array chunk by chunk; chunks are independent (counter-based
+    draws), so they run on a thread pool (numpy releases the GIL)."""
     out = np.empty(n, dtype=np.float32)
-    for c0 in range(0, n, _CHUNK):
-        c1 = min(n, c0 + _CHUNK)
-        z = raw_draws(seed, stream, start + c0, c1 - c0)
-        out[c0:c1] = (z >> np.uint64(40)).astype(np.float32) * np.float32(2.0 ** -24)
+    starts = list(range(0, n, _CHUNK))
+    if len(starts) <= 1:
+        for c0 in starts:
+            fill(out, c0, min(n, c0 + _CHUNK))
+        return out
+    workers = min(len(starts), os.cpu_count() or 1, 32)
+    with concurrent.futures.ThreadPoolExecutor(max_workers=workers) as ex:
+        list(ex.map(lambda c0: fill(out, c0, min(n, c0 + _CHUNK)), starts))
     return out
 
 
+def uniform24(seed: int, stream: int, n: int, start: int = 0) -> np.ndarray:
+    def fill(out, c0, c1):
+        z = raw_draws(seed, stream, start + c0, c1 - c0)
+        out[c0:c1] = (z >> np.uint64(40)).astype(np.float32) * np.float32(2.0 ** -24)
+    return _chunked(n, fill)
+
+
 def normal(seed: int, stream: int, n: int, start: int = 0) -> np.ndarray:
-    out = np.empty(n, dtype=np.float32)
-    for c0 in range(0, n, _CHUNK):
-        c1 = min(n, c0 + _CHUNK)
+    def fill(out, c0, c1):
         z = raw_draws(seed, stream, 2 * (start + c0), 2 * (c1 - c0))
         u1 = ((z[0::2] >> np.uint64(11)).astype(np.float64) + 1.0) * 2.0 ** -53
         u2 = (z[1::2] >> np.uint64(11)).astype(np.float64) * 2.0 ** -53
         out[c0:c1] = (np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * np.pi * u2)).astype(np.float32)
-    return out
+    return _chunked(n, fill)
 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
@@ -229,3 +243,75 @@ def make_decode(wl: DecodeWorkload, steps: int | None = None) -> DecodeInputs:
     vn = _bf16_tensor(s, VN, (T, wl.n, wl.H, wl.D))
     pn = priorities("uniform", s, (T, wl.n, wl.H), stream=PRION)
     return DecodeInputs(wl, kp, vp, pp, qn, kn, vn, pn)
+
+
+# --------------------------------------------------------------------------
+# the same generator on a torch device (for multi-GB workloads)
+# --------------------------------------------------------------------------
+# uint64 arithmetic is emulated on int64 tensors: + and * wrap modulo 2**64 in
+# two's complement, and a logical right shift is an arithmetic shift masked to
+# the low 64 - k bits.  uniform24 is exact integer arithmetic, so it matches the
+# numpy path bit for bit; normals go through the device's fp64 log/sqrt/cos and
+# then fp32 -> bf16 rounding, so an element can differ from the numpy value only
+# when the fp64 result sits within an ulp of an fp32 rounding boundary.
+
+def _s64(x: int) -> int:
+    x &= (1 << 64) - 1
+    return x - (1 << 64) if x >= (1 << 63) else x
+
+
+def _lsr(z, k: int):
+    import torch
+    return (z >> k) & ((1 << (64 - k)) - 1)
+
+
+def _mix64_t(z):
+    z = z ^ _lsr(z, 30)
+    z = z * _s64(0xBF58476D1CE4E5B9)
+    z = z ^ _lsr(z, 27)
+    z = z * _s64(0x94D049BB133111EB)
+    return z ^ _lsr(z, 31)
+
+
+def _raw_draws_t(seed, stream, start, count, device):
+    import torch
+    key = _s64(int(stream_key(seed, stream)))
+    idx = torch.arange(start + 1, start + count + 1, dtype=torch.int64, device=device)
+    return _mix64_t(idx * _s64(0x9E3779B97F4A7C15) + key)
+
+
+def normal_bf16_torch(seed: int, stream: int, shape, device, scale: float = 1.0, chunk: int = 1 << 26):
+    """bf16 tensor of the stated normal draws (times `scale`, in fp32), generated on `device`."""
+    import torch
+    n = int(np.prod(shape))
+    out = torch.empty(n, dtype=torch.bfloat16, device=device)
+    for c0 in range(0, n, chunk):
+        c1 = min(n, c0 + chunk)
+        z = _raw_draws_t(seed, stream, 2 * c0, 2 * (c1 - c0), device)
+        u1 = (_lsr(z[0::2], 11).to(torch.float64) + 1.0) * 2.0 ** -53
+        u2 = _lsr(z[1::2], 11).to(torch.float64) * 2.0 ** -53
+        x = (torch.sqrt(-2.0 * torch.log(u1)) * torch.cos(2.0 * np.pi * u2)).to(torch.float32)
+        if scale != 1.0:
+            x = x * scale
+        out[c0:c1] = x.to(torch.bfloat16)
+        del z, u1, u2, x
+    return out.view(*shape)
+
+
+def make_prefill_device(wl: Workload, device):
+    """(q, k, v, prio) on `device`: q/k/v generated there, prio copied from the numpy path."""
+    import torch
+    q = normal_bf16_torch(wl.seed, Q, (wl.b, wl.S, wl.Hq, wl.D), device)
+    k = normal_bf16_torch(wl.seed, K, (wl.b, wl.S, wl.H, wl.D), device, wl.k_scale)
+    v = normal_bf16_torch(wl.seed, V, (wl.b, wl.S, wl.H, wl.D), device)
+    prio = torch.from_numpy(priorities(wl.prio, wl.seed, (wl.b, wl.H, wl.S))).to(device)
+    return q, k, v, prio
+
+
+def bf16_block(seed: int, stream: int, shape, start_elem: int, scale: float = 1.0) -> np.ndarray:
+    """numpy bf16 bits of elements start_elem .. start_elem + prod(shape) of a stream."""
+    n = int(np.prod(shape))
+    x = normal(seed, stream, n, start=start_elem)
+    if scale != 1.0:
+        x = x * np.float32(scale)
+    return f32_to_bf16_bits(x).reshape(shape)

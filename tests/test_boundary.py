@@ -1,0 +1,75 @@
+"""The C ABI without a GPU: the library loads, exports every declared symbol,
+and rejects bad arguments on the host before anything is launched."""
+import ctypes
+
+import pytest
+
+from fixed_budget_kv_gb300 import kvpop
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    return kvpop.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = kvpop.header_functions()
+    assert len(names) >= 15
+    for name in names:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for st in range(6):
+        assert lib.kvpop_status_string(st)
+    assert lib.kvpop_version() >= 1
+
+
+def test_sizes(lib):
+    # mask workspace and lists grow with the problem; lists are [b,H,ceil(S/64),k] int32
+    assert kvpop.mask_lists_size(1, 8, 16384, 16, 512, 1520) == 8 * 256 * 1520 * 4
+    assert kvpop.mask_lists_size(2, 1, 100, 0, 0, 3) == 2 * 2 * 3 * 4
+    assert kvpop.mask_workspace_size(1, 1, 256, 4, 32, 32) > 0
+    assert kvpop.target_workspace_size(1, 16384, 32, 8) == 16384 * 32 * 4
+
+
+@pytest.mark.parametrize("args,code", [
+    ((1, 1, 0, kvpop.Budget(1, 1, 1)), 1),           # S = 0
+    ((1, 1, 10, kvpop.Budget(0, 0, 0)), 1),          # B = 0
+    ((1, 1, 10, kvpop.Budget(-1, 2, 2)), 1),         # negative budget
+    ((1, 1, 131073, kvpop.Budget(1, 1, 1)), 2),      # S above the supported maximum
+])
+def test_mask_validation(lib, args, code):
+    n = ctypes.c_size_t()
+    assert lib.kvpop_mask_workspace_size(*args, ctypes.byref(n)) == code
+    assert lib.kvpop_last_error()
+
+
+def test_attn_validation(lib):
+    P = ctypes.c_void_p(16)
+    bud = kvpop.Budget(0, 0, 0)
+    # D = 96 unsupported
+    assert lib.kvpop_attn_fwd(P, P, P, 1, 64, 4, 1, 96, 0.0, None, None, bud, None, P, None) == 2
+    # Hq not a multiple of H
+    assert lib.kvpop_attn_fwd(P, P, P, 1, 64, 5, 2, 64, 0.0, None, None, bud, None, P, None) == 1
+    # G = 3 does not divide 128
+    assert lib.kvpop_attn_fwd(P, P, P, 1, 64, 3, 1, 64, 0.0, None, None, bud, None, P, None) == 2
+    # misaligned pointer
+    assert lib.kvpop_attn_fwd(ctypes.c_void_p(18), P, P, 1, 64, 4, 1, 64, 0.0, None, None, bud, None, P,
+                              None) == 2
+    # sparse mode without lists and O
+    assert lib.kvpop_attn_fwd(P, P, P, 1, 64, 4, 1, 64, 0.0, P, None, kvpop.Budget(1, 1, 1), None, P,
+                              None) == 1
+
+
+def test_target_and_cache_validation(lib):
+    P = ctypes.c_void_p(16)
+    n = ctypes.c_size_t()
+    assert lib.kvpop_future_target_workspace_size(1, 64, 3, 1, ctypes.byref(n)) == 2
+    assert lib.kvpop_future_target(P, P, P, 1, 64, 4, 1, 64, 0.0, -1, P, P, 1 << 20, None) == 1
+    h = ctypes.c_void_p()
+    assert lib.kvpop_cache_create(1, 1, 3, 64, kvpop.Budget(1, 1, 1), ctypes.byref(h)) == 2
+    assert lib.kvpop_cache_create(1, 1, 4, 64, kvpop.Budget(0, 0, 0), ctypes.byref(h)) == 1
+    assert lib.kvpop_decode_step(None, P, P, P, P, P, P, None, None) == 1
