@@ -25,29 +25,53 @@ def _built():
     assert st == 0, f"device status {words}"
 
 
+def _decode_inputs(wl, steps):
+    """Step tokens and priorities on the host; the prefix K/V on the device.  Large
+    prefixes are generated on the device and the oracle regenerates only the
+    sequences whose floats it checks (element i of a tensor is draw i)."""
+    n, P, H, D, Hq = wl.n, wl.P, wl.H, wl.D, wl.Hq
+    shp = (n, P, H, D)
+    pp = synth.priorities("uniform", wl.seed, (n, H, P))
+    qs = synth.bf16_block(wl.seed, synth.QN, (steps, n, Hq, D), 0)
+    ks = synth.bf16_block(wl.seed, synth.KN, (steps, n, H, D), 0)
+    vs = synth.bf16_block(wl.seed, synth.VN, (steps, n, H, D), 0)
+    ps = synth.priorities("uniform", wl.seed, (steps, n, H), stream=synth.PRION)
+    if n * P * H * D > (1 << 26):
+        kp = synth.normal_bf16_torch(wl.seed, synth.K, shp, "cuda")
+        vp = synth.normal_bf16_torch(wl.seed, synth.V, shp, "cuda")
+    else:
+        kp = dev_bf16(synth.bf16_block(wl.seed, synth.K, shp, 0))
+        vp = dev_bf16(synth.bf16_block(wl.seed, synth.V, shp, 0))
+
+    def prefix_f32(seqs, stream):
+        blocks = [synth.bf16_block(wl.seed, stream, (P, H, D), i * P * H * D) for i in seqs]
+        return synth.bf16_bits_to_f32(np.stack(blocks)) if blocks else np.zeros((0, P, H, D), np.float32)
+
+    return kp, vp, pp, qs, ks, vs, ps, prefix_f32
+
+
 def run_decode(wl, steps, check_seqs, float_seqs, check_every=1):
-    inp = synth.make_decode(wl, steps=steps)
+    kp, vp, prio_prefix, q_steps, k_steps, v_steps, prio_steps, prefix_f32 = _decode_inputs(wl, steps)
     f = synth.bf16_bits_to_f32
     cache = kvpop.Cache(wl.n, wl.H, wl.G, wl.D, wl.s, wl.w, wl.k)
-    kp, vp = dev_bf16(inp.k_prefix), dev_bf16(inp.v_prefix)
-    pp = dev(inp.prio_prefix)
+    pp = dev(prio_prefix)
     _, _, ev, _ = kvpop.mask(pp, wl.s, wl.w, wl.k, lists=False)
     cache.prefill(kp, vp, pp, ev)
     assert cache.position() == wl.P
     scale = 1 / math.sqrt(wl.D)
-    # slot sets need only the priorities; floats are simulated for a subset of sequences
-    ref = oracle.decode_sim(inp.k_prefix, inp.v_prefix, inp.prio_prefix, inp.q_steps, inp.k_steps,
-                            inp.v_steps, inp.prio_steps, wl.s, wl.w, wl.k, scale, seqs=list(check_seqs),
-                            want_floats=False)
+    # slot sets need only the priorities and shapes; floats are simulated for a subset
+    shape_only = np.empty((wl.n, wl.P, wl.H, wl.D), np.uint16)
+    ref = oracle.decode_sim(shape_only, shape_only, prio_prefix, q_steps, k_steps, v_steps, prio_steps,
+                            wl.s, wl.w, wl.k, scale, seqs=list(check_seqs), want_floats=False)
     fs = list(float_seqs)
     if fs:
-        reff = oracle.decode_sim(f(inp.k_prefix[fs]), f(inp.v_prefix[fs]), inp.prio_prefix[fs],
-                                 f(inp.q_steps[:, fs]), f(inp.k_steps[:, fs]), f(inp.v_steps[:, fs]),
-                                 inp.prio_steps[:, fs], wl.s, wl.w, wl.k, scale, seqs=range(len(fs)))
+        reff = oracle.decode_sim(prefix_f32(fs, synth.K), prefix_f32(fs, synth.V), prio_prefix[fs],
+                                 f(q_steps[:, fs]), f(k_steps[:, fs]), f(v_steps[:, fs]),
+                                 prio_steps[:, fs], wl.s, wl.w, wl.k, scale, seqs=range(len(fs)))
         for i, n in enumerate(fs):
             ref.setdefault(n, {}).update(O=reff[i]["O"], lse=reff[i]["lse"])
-    qs, ks, vs = dev_bf16(inp.q_steps), dev_bf16(inp.k_steps), dev_bf16(inp.v_steps)
-    ps = dev(inp.prio_steps)
+    qs, ks, vs = dev_bf16(q_steps), dev_bf16(k_steps), dev_bf16(v_steps)
+    ps = dev(prio_steps)
     worst_o = worst_l = 0.0
     for i in range(steps):
         O, lse, evicted = cache.step(qs[i], ks[i], vs[i], ps[i])
