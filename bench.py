@@ -352,7 +352,7 @@ def _cpu_data(wl):
     return _CPU_DATA[wl.name]
 
 
-def cpu_sample(wl, seed=0, nrows=1024, nkeys=96):
+def cpu_sample(wl, seed=0, nrows=8192, nkeys=512):
     """Times the oracle on sampled units of the workload and scales to tokens/s.
 
     Units per token (one query position of one batch row): Hq sparse-attention
@@ -401,7 +401,7 @@ def run_reference(args):
     sample = ""
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
-        v, sample = cpu_sample(wl, seed=i, nrows=512, nkeys=48)
+        v, sample = cpu_sample(wl, seed=i, nrows=2048, nkeys=128)
         if i >= args.warmup:
             vals.append((v, time.perf_counter() - t0))
     value = float(np.median([v for v, _ in vals]))
