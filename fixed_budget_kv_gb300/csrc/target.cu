@@ -12,6 +12,8 @@
 // each query tile pre-scaled to log2 units), warp 1 TMEM allocation and MMA
 // issuer, warps 4-7 / 8-11 the exp-and-sum for row tile 0 / 1.  S' = K Q^T is
 // double-buffered in TMEM per row tile (4 x 128 columns).
+#include <mutex>
+
 #include "common.cuh"
 
 namespace kvpop {
@@ -374,4 +376,68 @@ extern "C" kvpop_status kvpop_future_target(const void* q, const void* k, const 
   st = cuda_check(cudaGetLastError(), "kvpop_future_target: lse prep");
   if (st != KVPOP_OK) return st;
   return D == 128 ? launch_target<128>(prm, b, H, cs) : launch_target<64>(prm, b, H, cs);
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of kvpop_future_target.
+//
+// Some callers cannot call cudaMalloc: a serving engine whose allocator has
+// reserved all device memory up front for its KV pool, or a caller on a path
+// where cudaMalloc's implicit device synchronisation is not allowed.  This
+// entry point keeps the pass's scratch (the LSE rescaled to log2 units in
+// query-tile order) in a file-scope device array instead of caller workspace.
+// The array is part of the module image: every GPU that loads the library
+// holds these 16 MiB until the process exits.
+// ---------------------------------------------------------------------------
+namespace kvpop {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB = 4,194,304 floats
+static __device__ __align__(256) unsigned char g_target_scratch[kNoAllocScratchBytes];
+
+// Device address of g_target_scratch, looked up once per device with that
+// device current (the host-side symbol is only a stand-in, never a device address).
+void* target_scratch_ptr(kvpop_status* st) {
+  static void* cache[64] = {nullptr};
+  static std::mutex mu;
+  const int d = current_device();
+  if (d < 0 || d >= 64) {
+    set_last_error("kvpop_future_target_noalloc: device index %d out of range", d);
+    *st = KVPOP_ERR_UNSUPPORTED;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[d] == nullptr) {
+    void* p = nullptr;
+    *st = cuda_check(cudaGetSymbolAddress(&p, g_target_scratch),
+                     "kvpop_future_target_noalloc: cudaGetSymbolAddress");
+    if (*st != KVPOP_OK) return nullptr;
+    cache[d] = p;
+  }
+  *st = KVPOP_OK;
+  return cache[d];
+}
+
+}  // namespace
+}  // namespace kvpop
+
+extern "C" kvpop_status kvpop_future_target_noalloc(const void* q, const void* k, const float* lse,
+                                                    int b, int S, int Hq, int H, int D, float scale,
+                                                    int w, float* target, kvpop_stream stream) {
+  size_t need = 0;
+  kvpop_status st = kvpop_future_target_workspace_size(b, S, Hq, H, &need);
+  if (st != KVPOP_OK) return st;
+  if (need > kvpop::kNoAllocScratchBytes) {
+    kvpop::set_last_error(
+        "kvpop_future_target_noalloc: needs %zu bytes of scratch (b*H*ceil(S/P)*P*G floats), "
+        "above the built-in %zu; use kvpop_future_target with caller workspace",
+        need, kvpop::kNoAllocScratchBytes);
+    return KVPOP_ERR_UNSUPPORTED;
+  }
+  void* scratch = kvpop::target_scratch_ptr(&st);
+  if (st != KVPOP_OK) return st;
+  // Every element of the scratch that the pass reads is written by it first
+  // (the LSE re-layout covers all b*H*Spad*G entries), so nothing is cleared.
+  return kvpop_future_target(q, k, lse, b, S, Hq, H, D, scale, w, target, scratch,
+                             kvpop::kNoAllocScratchBytes, stream);
 }

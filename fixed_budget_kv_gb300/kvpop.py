@@ -72,6 +72,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "kvpop_future_target_workspace_size": ([c_int, c_int, c_int, c_int, P], c_int),
         "kvpop_future_target": ([P, P, P, c_int, c_int, c_int, c_int, c_int, c_float, c_int, P, P, c_size,
                                  P], c_int),
+        "kvpop_future_target_noalloc": ([P, P, P, c_int, c_int, c_int, c_int, c_int, c_float, c_int, P, P],
+                                        c_int),
         "kvpop_cache_create": ([c_int, c_int, c_int, c_int, Budget, P], c_int),
         "kvpop_cache_destroy": ([P], c_int),
         "kvpop_cache_prefill": ([P, P, P, P, c_int, P, P], c_int),
@@ -209,6 +211,22 @@ def future_target(q, k, lse, w: int, scale: float = 0.0, workspace=None, out=Non
     _check(load().kvpop_future_target(_p(q), _p(k), _p(lse), b, S, Hq, H, D, float(scale), int(w),
                                       _p(target), _p(workspace), workspace.numel(), _stream(stream)),
            "kvpop_future_target")
+    return target
+
+
+def future_target_noalloc(q, k, lse, w: int, scale: float = 0.0, out=None, stream=None):
+    """Same result as future_target, for callers that cannot allocate device
+    memory: the pass's scratch lives in a fixed 16 MiB array inside the library
+    (problems needing more raise KvpopError).  Only the output is allocated here,
+    and only when `out` is not given."""
+    _need(q, torch.bfloat16, "q")
+    _need(k, torch.bfloat16, "k")
+    _need(lse, torch.float32, "lse")
+    b, S, Hq, D = q.shape
+    H = k.shape[2]
+    target = torch.empty((b, H, S), dtype=torch.float32, device=q.device) if out is None else out
+    _check(load().kvpop_future_target_noalloc(_p(q), _p(k), _p(lse), b, S, Hq, H, D, float(scale), int(w),
+                                              _p(target), _stream(stream)), "kvpop_future_target_noalloc")
     return target
 
 

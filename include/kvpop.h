@@ -149,6 +149,29 @@ kvpop_status kvpop_future_target(const void* q, const void* k, const float* lse,
                                  void* workspace, size_t workspace_bytes, kvpop_stream stream);
 
 /* ------------------------------------------------------------------------
+ * kvpop_future_target_noalloc -- kvpop_future_target without caller scratch.
+ *
+ * The paper has no counterpart: this exists for callers that cannot call
+ * cudaMalloc -- e.g. an engine whose allocator has reserved all device memory
+ * for its own pools, or a path where cudaMalloc's implicit device
+ * synchronisation is not allowed.  Same arguments and result as
+ * kvpop_future_target minus the workspace; it allocates nothing.
+ *   - Scratch is a 16 MiB file-scope device array (every GPU that loads the
+ *     library holds it until exit).  Calls needing more than that
+ *     (b*H*ceil(S/P)*P*G floats, P = 128/G, above 4,194,304) return
+ *     KVPOP_ERR_UNSUPPORTED with a message; nothing is launched.
+ *   - The first call on a device looks the array's device address up
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - All calls share the one array: calls that overlap on the GPU (different
+ *     streams, no ordering between them) race.  Every scratch element a call
+ *     reads is written by that call first, so no clearing is needed.
+ * ---------------------------------------------------------------------- */
+kvpop_status kvpop_future_target_noalloc(const void* q, const void* k, const float* lse, int b,
+                                         int S, int Hq, int H, int D, float scale, int w,
+                                         float* target, kvpop_stream stream);
+
+/* ------------------------------------------------------------------------
  * Fixed-budget decode cache ([notes] section 2.4 and section 3.3: B slots
  * per KV head, the token u = q - w leaving the window is kept or evicted by
  * comparing its priority with the worst held long-range token; [summary]
