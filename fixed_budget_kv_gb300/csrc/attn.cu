@@ -438,6 +438,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
               l > 0.0f ? (m_ref * sl2 + __log2f(l)) * 0.69314718055994531f : neg_inf();
       }
     } else {
+      // LSE only: per row l = sum 2^(s*sl2 - m_ref*sl2) against a lazily moved
+      // reference m_ref; a 32-column chunk that would overflow moves it.
+      const int q_first = qb0 + qt * P;
       for (int j = 0; j < NT; ++j) {
         const int buf = j & 1;
         if (!warp_wait(&bars->s_full[qt][buf], (j >> 1) & 1, abort_flag)) {
@@ -447,37 +450,35 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         }
         tc_fence_after();
         const uint32_t s_col = 128 * (2 * qt + buf);
-        const bool diag = (j * kKeys + kKeys - 1) > qb0;
+        const bool diag = (j * kKeys + kKeys - 1) > q_first;  // some key may lie after some row
+        uint32_t ra[32], rb[32];
+        tmem_ld32(tl + s_col, ra);
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
-          uint32_t r[32];
-          tmem_ld32(tl + s_col + ch * 32, r);
-          tmem_wait_ld();
-          float x[32];
+          uint32_t(&cur)[32] = (ch & 1) ? rb : ra;
+          uint32_t(&nxt)[32] = (ch & 1) ? ra : rb;
+          tmem_wait_ld_dep(cur);
+          if (ch < 3) tmem_ld32(tl + s_col + (ch + 1) * 32, nxt);
+          if (diag) {
+            const int t0 = j * kKeys + ch * 32;
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            x[c] = __uint_as_float(r[c]);
-            if (diag && (j * kKeys + ch * 32 + c) > q) x[c] = neg_inf();
+            for (int c = 0; c < 32; ++c)
+              if (t0 + c > q) cur[c] = 0xff800000u;
           }
-          float cm = x[0];
-#pragma unroll
-          for (int c = 1; c < 32; ++c) cm = fmaxf(cm, x[c]);
-          if ((cm - m_ref) * sl2 > kRescaleLog2) {
-            l *= ex2_approx((m_ref - cm) * sl2);
+          if (m_ref == neg_inf()) {
+            const float cm = max32(cur);
+            if (cm == neg_inf()) continue;
             m_ref = cm;
           }
-          if (m_ref != neg_inf()) {
-            const float neg = -m_ref * sl2;
-            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-            for (int c = 0; c < 32; c += 4) {
-              a0 += ex2_approx(fmaf(x[c], sl2, neg));
-              a1 += ex2_approx(fmaf(x[c + 1], sl2, neg));
-              a2 += ex2_approx(fmaf(x[c + 2], sl2, neg));
-              a3 += ex2_approx(fmaf(x[c + 3], sl2, neg));
-            }
-            l += (a0 + a1) + (a2 + a3);
+          const uint64_t s2 = pack2(sl2, sl2);
+          float sum = exp2_sum32(cur, s2, pack2(-m_ref * sl2, -m_ref * sl2));
+          if (!(sum <= 0x1p64f)) {  // a score far above the reference: move it
+            const float cm = max32(cur);
+            l *= ex2_approx((m_ref - cm) * sl2);
+            m_ref = cm;
+            sum = exp2_sum32(cur, s2, pack2(-m_ref * sl2, -m_ref * sl2));
           }
+          l += sum;
         }
         tc_fence_before();
         __syncwarp();
@@ -643,5 +644,5 @@ extern "C" kvpop_status kvpop_attn_fwd(const void* q, const void* k, const void*
     return D == 128 ? launch<128, true, true>(prm, b, H, cs) : launch<64, true, true>(prm, b, H, cs);
   }
   if (O) return D == 128 ? launch<128, true, false>(prm, b, H, cs) : launch<64, true, false>(prm, b, H, cs);
-  return D == 128 ? launch<128, false, false>(prm, b, H, cs) : launch<64, false, false>(prm, b, H, cs);
+  return launch_dense_lse(q, k, b, S, Hq, H, D, prm.scale_log2, lse, cs);
 }

@@ -309,10 +309,76 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int c) {
   return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
 }
 
+// Wait for this thread's tcgen05.ld results; the "+r" operands make every later
+// use of `r` depend on the wait, so the compiler cannot read them early.
+__device__ __forceinline__ void tmem_wait_ld_dep(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                 "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]),
+                 "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]),
+                 "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]),
+                 "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]),
+                 "+r"(r[31])
+               :
+               : "memory");
+}
+
+// Packed fp32 pairs (two lanes of one 64-bit register) for the f32x2 FMA/ADD pipes.
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Maximum of 32 fp32 values held as raw bits.
+__device__ __forceinline__ float max32(const uint32_t (&r)[32]) {
+  float m = __uint_as_float(r[0]);
+#pragma unroll
+  for (int c = 1; c < 31; c += 2) m = max3(m, __uint_as_float(r[c]), __uint_as_float(r[c + 1]));
+  return fmaxf(m, __uint_as_float(r[31]));
+}
+
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// sum over 32 raw-bit fp32 values x of 2^(x * s + n), with s2 = (s, s), n2 = (n, n)
+// as packed pairs: one f32x2 FMA and one f32x2 ADD per two exponentials.
+__device__ __forceinline__ float exp2_sum32(const uint32_t (&r)[32], uint64_t s2, uint64_t n2) {
+  uint64_t a0 = 0, a1 = 0;
+#pragma unroll
+  for (int c = 0; c < 32; c += 4) {
+    const uint64_t t0 = fma2(pack2(__uint_as_float(r[c]), __uint_as_float(r[c + 1])), s2, n2);
+    const uint64_t t1 = fma2(pack2(__uint_as_float(r[c + 2]), __uint_as_float(r[c + 3])), s2, n2);
+    float e0, e1, e2, e3;
+    unpack2(t0, e0, e1);
+    unpack2(t1, e2, e3);
+    a0 = add2(a0, pack2(ex2_approx(e0), ex2_approx(e1)));
+    a1 = add2(a1, pack2(ex2_approx(e2), ex2_approx(e3)));
+  }
+  float x, y;
+  unpack2(add2(a0, a1), x, y);
+  return x + y;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -333,5 +399,9 @@ bool make_tmap_4d(CUtensorMap* map, const void* base, const uint64_t dims[4],
 
 int current_device();
 int num_sms();
+
+// Dense causal LSE-only pass (csrc/dense_lse.cu); arguments already validated.
+kvpop_status launch_dense_lse(const void* q, const void* k, int b, int S, int Hq, int H, int D,
+                              float scale_log2, float* lse, cudaStream_t cs);
 
 }  // namespace kvpop

@@ -6,12 +6,16 @@
 //   target[b,h,t] = log sum_{g<G} sum_{d>=t+w} exp(scale q_{d,hG+g}.k_t - LSE_{d,hG+g}).
 // Every term is a probability (<= 1), so a plain fp32 sum needs no running max.
 //
-// One CTA owns two 128-key row tiles of one (batch, KV head); it streams the
-// query tiles (128/G positions x G heads = 128 columns) that can see them.
-// Warp roles (384 threads): warp 0 TMA producer (K once, Q tiles, the LSE of
-// each query tile pre-scaled to log2 units), warp 1 TMEM allocation and MMA
-// issuer, warps 4-7 / 8-11 the exp-and-sum for row tile 0 / 1.  S' = K Q^T is
-// double-buffered in TMEM per row tile (4 x 128 columns).
+// One CTA owns four 128-key row tiles (512 keys) of one (batch, KV head) and a
+// chunk of at most 64 query tiles (128/G positions x G heads = 128 columns
+// each) among those the keys can see; each query tile fetched feeds four MMAs.
+// 576 threads: warp 0 TMA producer (K once, Q tiles, and the LSE of each query
+// tile, negated and in log2 units, by a 1-D bulk copy), warp 1 TMEM allocator
+// and single-thread MMA issuer, warps 2-17 four warpgroups summing
+// exponentials, one per row tile (one thread per key = TMEM lane).  A row
+// tile's 128 TMEM columns are handed back as soon as they are read.  Chunks of
+// the same keys add their partial sums into the output with one atomicAdd per
+// key; a last pass takes the log.
 #include <mutex>
 
 #include "common.cuh"
@@ -19,28 +23,30 @@
 namespace kvpop {
 namespace {
 
-constexpr int kThreads = 384;
+constexpr int kNR = 4;  // row tiles per CTA
+constexpr int kThreads = (2 + 4 * kNR) * 32;
 constexpr int kBlockBytes = 128 * 128;
 constexpr int kLseStages = 4;
+constexpr int kChunkTiles = 64;  // query tiles per CTA
 
 struct TargetParams {
   CUtensorMap tq, tk;
-  const float* lse2;  // [b, H, Spad, G] = LSE * log2(e), +inf past S
-  float* target;
+  const float* lse2;  // [b, H, Spad, G] = -LSE * log2(e), -inf past S
+  float* acc;         // [b, H, S] partial sums (the output buffer, zeroed first)
   int* status;
-  int S, Spad, H, G, logG, P, nct, w;
+  int S, Spad, H, G, logG, P, nct, w, nchunk;
   float scale_log2;
 };
 
 template <int D>
 struct TLayout {
   static constexpr int DH = D / 64;
-  static constexpr int NS = D == 128 ? 4 : 8;
+  static constexpr int NS = D == 128 ? 2 : 4;
   static constexpr int k_off = 0;
-  static constexpr int q_off = k_off + 2 * DH * kBlockBytes;
+  static constexpr int q_off = k_off + kNR * DH * kBlockBytes;
   static constexpr int lse_off = q_off + NS * DH * kBlockBytes;
   static constexpr int bar_off = lse_off + kLseStages * 512;
-  static constexpr int nbar = 1 + 2 * NS + 8 + 2 * kLseStages + 1;
+  static constexpr int nbar = 1 + 2 * NS + 2 * kNR + 2 * kLseStages + 1;
   static constexpr int misc_off = bar_off + nbar * 8;
   static constexpr int total = misc_off + 64 + 1024;
 };
@@ -49,7 +55,7 @@ template <int NS>
 struct TBars {
   uint64_t k_full;
   uint64_t q_full[NS], q_empty[NS];
-  uint64_t s_full[2][2], s_empty[2][2];
+  uint64_t s_full[kNR], s_empty[kNR];
   uint64_t l_full[kLseStages], l_empty[kLseStages];
   uint64_t drain;
 };
@@ -65,8 +71,16 @@ __global__ void lse_prep(const float* __restrict__ lse, int b, int H, int G, int
     r /= Spad;
     const int h = (int)(r % H);
     const int bi = (int)(r / H);
-    lse2[i] = d < S ? lse[((size_t)bi * H * G + (size_t)h * G + g) * S + d] * 1.4426950408889634f
-                    : __int_as_float(0x7f800000);
+    lse2[i] = d < S ? -lse[((size_t)bi * H * G + (size_t)h * G + g) * S + d] * 1.4426950408889634f
+                    : __int_as_float(0xff800000);
+  }
+}
+
+__global__ void target_finalize(float* __restrict__ t, long long n) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const float s = t[i];
+    t[i] = s > 0.0f ? __log2f(s) * 0.69314718055994531f : __int_as_float(0xff800000);
   }
 }
 
@@ -75,6 +89,21 @@ __global__ void __launch_bounds__(kThreads, 1) target_kernel(const __grid_consta
   using L = TLayout<D>;
   constexpr int DH = L::DH;
   constexpr int NS = L::NS;
+  const int chunk = blockIdx.x, rb = blockIdx.y;
+  const int b = blockIdx.z / p.H, h = blockIdx.z % p.H;
+  const int S = p.S, P = p.P, G = p.G;
+  const int t0 = rb * 128 * kNR;
+  int c_start[kNR];
+#pragma unroll
+  for (int rt = 0; rt < kNR; ++rt) {
+    const long long first = (long long)t0 + 128 * rt + p.w;  // first query position any key here sees
+    c_start[rt] = first > S - 1 ? p.nct : (int)(first / P);
+  }
+  const int c_lo = c_start[0] + chunk * kChunkTiles;
+  const int c_hi = min(p.nct, c_lo + kChunkTiles);
+  if (c_lo >= c_hi) return;  // nothing left for this chunk (uniform over the CTA)
+  const int NTc = c_hi - c_lo;
+
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   TBars<NS>* bars = reinterpret_cast<TBars<NS>*>(smem + L::bar_off);
@@ -82,18 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1) target_kernel(const __grid_consta
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::misc_off + 4);
   const float* lse_s = reinterpret_cast<const float*>(smem + L::lse_off);
   const uint32_t sbase = smem_u32(smem);
-
   const int warp = warp_id(), lane = lane_id();
-  const int b = blockIdx.z, h = blockIdx.y;
-  const int t0 = blockIdx.x * 256;
-  const int S = p.S, P = p.P, G = p.G;
-  int c_start[2];
-  for (int rt = 0; rt < 2; ++rt) {
-    const long long first = (long long)t0 + 128 * rt + p.w;  // first visible query position
-    c_start[rt] = first > S - 1 ? p.nct : (int)(first / P);
-  }
-  const int c_begin = c_start[0];
-  const int NTc = p.nct - c_begin;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->k_full, 1);
@@ -101,14 +119,13 @@ __global__ void __launch_bounds__(kThreads, 1) target_kernel(const __grid_consta
       mbar_init(&bars->q_full[i], 1);
       mbar_init(&bars->q_empty[i], 1);
     }
-    for (int a = 0; a < 2; ++a)
-      for (int c = 0; c < 2; ++c) {
-        mbar_init(&bars->s_full[a][c], 1);
-        mbar_init(&bars->s_empty[a][c], 4);
-      }
+    for (int i = 0; i < kNR; ++i) {
+      mbar_init(&bars->s_full[i], 1);
+      mbar_init(&bars->s_empty[i], 4);
+    }
     for (int i = 0; i < kLseStages; ++i) {
       mbar_init(&bars->l_full[i], 1);
-      mbar_init(&bars->l_empty[i], 8);
+      mbar_init(&bars->l_empty[i], 4 * kNR);
     }
     mbar_init(&bars->drain, 1);
     *abort_flag = 0;
@@ -128,16 +145,17 @@ __global__ void __launch_bounds__(kThreads, 1) target_kernel(const __grid_consta
   };
 
   if (warp == 0) {
-    if (lane == 0 && NTc > 0) {
+    if (lane == 0) {
       tma_prefetch_desc(&p.tq);
-      mbar_arrive_expect_tx(&bars->k_full, 2 * DH * kBlockBytes);
-      for (int rt = 0; rt < 2; ++rt)
+      tma_prefetch_desc(&p.tk);
+      mbar_arrive_expect_tx(&bars->k_full, kNR * DH * kBlockBytes);
+      for (int rt = 0; rt < kNR; ++rt)
         for (int dh = 0; dh < DH; ++dh)
           tma_load_4d(smem + L::k_off + (rt * DH + dh) * kBlockBytes, &p.tk, &bars->k_full, dh * 64, h,
                       t0 + 128 * rt, b);
       const float* lsrc = p.lse2 + ((size_t)b * p.H + h) * (size_t)p.Spad * G;
       for (int jc = 0; jc < NTc; ++jc) {
-        const int c = c_begin + jc;
+        const int c = c_lo + jc;
         const int st = jc % NS;
         if (!mbar_wait(&bars->q_empty[st], ((jc / NS) & 1) ^ 1, abort_flag)) {
           fail(SITE_TARGET_PRODUCER, 1);
@@ -157,68 +175,69 @@ __global__ void __launch_bounds__(kThreads, 1) target_kernel(const __grid_consta
       }
     }
   } else if (warp == 1) {
-    if (lane == 0 && NTc > 0) {
+    if (lane == 0) {
       bool ok = mbar_wait(&bars->k_full, 0, abort_flag);
       if (!ok) fail(SITE_TARGET_MMA, 1);
       tc_fence_after();
       constexpr uint32_t idesc = idesc_bf16(128, 128, 0);
       const uint32_t k_addr = sbase + L::k_off, q_addr = sbase + L::q_off;
-      int n_rt[2] = {0, 0};
+      int n_rt[kNR] = {0, 0, 0, 0};
       for (int jc = 0; ok && jc < NTc; ++jc) {
-        const int c = c_begin + jc;
+        const int c = c_lo + jc;
         const int st = jc % NS;
         if (!mbar_wait(&bars->q_full[st], (jc / NS) & 1, abort_flag)) {
           fail(SITE_TARGET_MMA, 2);
           break;
         }
         tc_fence_after();
-        for (int rt = 0; rt < 2; ++rt) {
+#pragma unroll
+        for (int rt = 0; rt < kNR; ++rt) {
           if (c < c_start[rt]) continue;
           const int n = n_rt[rt]++;
-          const int buf = n & 1;
-          if (!mbar_wait(&bars->s_empty[rt][buf], ((n >> 1) & 1) ^ 1, abort_flag)) {
+          if (!mbar_wait(&bars->s_empty[rt], (n & 1) ^ 1, abort_flag)) {
             fail(SITE_TARGET_MMA, 3);
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t d_tmem = tbase + 128 * (2 * rt + buf);
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
             const int dh = ks >> 2;
             const uint32_t w32 = (uint32_t)(ks & 3) * 32;
             const uint64_t a = smem_desc_sw128(k_addr + (rt * DH + dh) * kBlockBytes + w32, 16, 1024);
             const uint64_t bd = smem_desc_sw128(q_addr + (st * DH + dh) * kBlockBytes + w32, 16, 1024);
-            mma_ss(d_tmem, a, bd, idesc, ks > 0 ? 1u : 0u);
+            mma_ss(tbase + 128 * rt, a, bd, idesc, ks > 0 ? 1u : 0u);
           }
-          mma_commit(&bars->s_full[rt][buf]);
+          mma_commit(&bars->s_full[rt]);
         }
         mma_commit(&bars->q_empty[st]);
       }
       mma_commit(&bars->drain);
       mbar_wait(&bars->drain, 0, nullptr);
     }
-  } else if (warp >= 4) {
-    const int rt = (warp - 4) >> 2;
+  } else {
+    // warpgroups: warps 2-5 -> row tile 0, 6-9 -> 1, 10-13 -> 2, 14-17 -> 3
+    const int rt = (warp - 2) >> 2;
     const int quarter = warp & 3;
     const int t = t0 + 128 * rt + quarter * 32 + lane;  // this thread's key
-    const uint32_t tl = tbase + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t tl = tbase + ((uint32_t)(quarter * 32) << 16) + 128 * rt;
     const float sl2 = p.scale_log2;
     const int row_first = t0 + 128 * rt;
-    float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+    const int crt = c_start[rt];
+    uint64_t acc0 = 0, acc1 = 0;  // packed fp32 pairs
+    const uint64_t s2 = pack2(sl2, sl2);
     bool ok = true;
     int n = 0;
     for (int jc = 0; jc < NTc; ++jc) {
-      const int c = c_begin + jc;
+      const int c = c_lo + jc;
       const int ls = jc % kLseStages;
       if (!warp_wait(&bars->l_full[ls], (jc / kLseStages) & 1, abort_flag)) {
         if (lane == 0) fail(SITE_TARGET_SOFTMAX, 1);
         ok = false;
         break;
       }
-      if (c >= c_start[rt]) {
-        const int buf = n & 1;
-        if (!warp_wait(&bars->s_full[rt][buf], (n >> 1) & 1, abort_flag)) {
+      if (c >= crt) {
+        if (!warp_wait(&bars->s_full[rt], n & 1, abort_flag)) {
           if (lane == 0) fail(SITE_TARGET_SOFTMAX, 2);
           ok = false;
           break;
@@ -226,42 +245,51 @@ __global__ void __launch_bounds__(kThreads, 1) target_kernel(const __grid_consta
         ++n;
         tc_fence_after();
         const float* l2 = lse_s + ls * 128;
-        const uint32_t s_col = 128 * (2 * rt + buf);
         const bool masked = (long long)c * P < (long long)row_first + 127 + p.w;
+        uint32_t ra[32], rb[32];
+        tmem_ld32(tl, ra);
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
-          uint32_t r[32];
-          tmem_ld32(tl + s_col + ch * 32, r);
-          tmem_wait_ld();
-          if (!masked) {
-#pragma unroll
-            for (int cc = 0; cc < 32; cc += 4) {
-              const float4 lv = *reinterpret_cast<const float4*>(l2 + ch * 32 + cc);
-              acc0 += ex2_approx(fmaf(__uint_as_float(r[cc]), sl2, -lv.x));
-              acc1 += ex2_approx(fmaf(__uint_as_float(r[cc + 1]), sl2, -lv.y));
-              acc2 += ex2_approx(fmaf(__uint_as_float(r[cc + 2]), sl2, -lv.z));
-              acc3 += ex2_approx(fmaf(__uint_as_float(r[cc + 3]), sl2, -lv.w));
-            }
-          } else {
+          uint32_t(&cur)[32] = (ch & 1) ? rb : ra;
+          uint32_t(&nxt)[32] = (ch & 1) ? ra : rb;
+          tmem_wait_ld_dep(cur);
+          if (ch < 3) {
+            tmem_ld32(tl + (ch + 1) * 32, nxt);
+          } else {  // the whole S' row tile is in registers: hand TMEM back
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->s_empty[rt]);
+          }
+          if (masked) {  // only the query tiles that straddle d = t + w
 #pragma unroll
             for (int cc = 0; cc < 32; ++cc) {
-              const int col = ch * 32 + cc;
-              const int d = c * P + (col >> p.logG);
-              if (d >= t + p.w) acc0 += ex2_approx(fmaf(__uint_as_float(r[cc]), sl2, -l2[col]));
+              const int d = c * P + ((ch * 32 + cc) >> p.logG);
+              if (d < t + p.w) cur[cc] = 0xff800000u;
             }
           }
+#pragma unroll
+          for (int cc = 0; cc < 32; cc += 4) {
+            const float4 lv = *reinterpret_cast<const float4*>(l2 + ch * 32 + cc);
+            const uint64_t x0 = fma2(pack2(__uint_as_float(cur[cc]), __uint_as_float(cur[cc + 1])), s2,
+                                     pack2(lv.x, lv.y));
+            const uint64_t x1 = fma2(pack2(__uint_as_float(cur[cc + 2]), __uint_as_float(cur[cc + 3])), s2,
+                                     pack2(lv.z, lv.w));
+            float e0, e1, e2, e3;
+            unpack2(x0, e0, e1);
+            unpack2(x1, e2, e3);
+            acc0 = add2(acc0, pack2(ex2_approx(e0), ex2_approx(e1)));
+            acc1 = add2(acc1, pack2(ex2_approx(e2), ex2_approx(e3)));
+          }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->s_empty[rt][buf]);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->l_empty[ls]);
     }
     if (ok && t < S) {
-      const float sum = (acc0 + acc1) + (acc2 + acc3);
-      p.target[((size_t)b * p.H + h) * S + t] =
-          sum > 0.0f ? __log2f(sum) * 0.69314718055994531f : __int_as_float(0xff800000);
+      float y0, y1;
+      unpack2(add2(acc0, acc1), y0, y1);
+      const float sum = y0 + y1;
+      if (sum > 0.0f) atomicAdd(p.acc + ((size_t)b * p.H + h) * S + t, sum);
     }
   }
 
@@ -282,7 +310,8 @@ kvpop_status launch_target(const TargetParams& prm, int b, int H, cudaStream_t c
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::total),
       "kvpop_future_target: smem attribute");
   if (st != KVPOP_OK) return st;
-  dim3 grid((prm.S + 255) / 256, H, b);
+  const int nrb = (prm.S + 128 * kNR - 1) / (128 * kNR);
+  dim3 grid(prm.nchunk, nrb, b * H);
   kern<<<grid, kThreads, L::total, cs>>>(prm);
   return cuda_check(cudaGetLastError(), "kvpop_future_target: launch");
 }
@@ -336,8 +365,8 @@ extern "C" kvpop_status kvpop_future_target(const void* q, const void* k, const 
     set_last_error("kvpop_future_target: q and k must be 16-byte aligned");
     return KVPOP_ERR_UNSUPPORTED;
   }
-  if (b > 65535 || H > 65535) {
-    set_last_error("kvpop_future_target: b and H must be <= 65535");
+  if ((long long)b * H > 65535) {
+    set_last_error("kvpop_future_target: b*H must be <= 65535");
     return KVPOP_ERR_UNSUPPORTED;
   }
   const int G = Hq / H;
@@ -364,18 +393,25 @@ extern "C" kvpop_status kvpop_future_target(const void* q, const void* k, const 
   prm.logG = lg;
   prm.P = P;
   prm.w = w;
+  prm.nchunk = (prm.nct + kChunkTiles - 1) / kChunkTiles;
   const float sc = scale > 0.0f ? scale : 1.0f / sqrtf((float)D);
   prm.scale_log2 = sc * 1.4426950408889634f;
   prm.lse2 = static_cast<const float*>(workspace);
-  prm.target = target;
+  prm.acc = target;
   prm.status = device_status_ptr();
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const long long nout = (long long)b * H * S;
+  st = cuda_check(cudaMemsetAsync(target, 0, (size_t)nout * sizeof(float), cs), "kvpop_future_target: zero");
+  if (st != KVPOP_OK) return st;
   const long long n = (long long)b * H * prm.Spad * G;
   const int blocks = (int)std::min<long long>((n + 255) / 256, 4096);
   lse_prep<<<blocks, 256, 0, cs>>>(lse, b, H, G, S, prm.Spad, static_cast<float*>(workspace));
   st = cuda_check(cudaGetLastError(), "kvpop_future_target: lse prep");
   if (st != KVPOP_OK) return st;
-  return D == 128 ? launch_target<128>(prm, b, H, cs) : launch_target<64>(prm, b, H, cs);
+  st = D == 128 ? launch_target<128>(prm, b, H, cs) : launch_target<64>(prm, b, H, cs);
+  if (st != KVPOP_OK) return st;
+  target_finalize<<<(int)std::min<long long>((nout + 255) / 256, 4096), 256, 0, cs>>>(target, nout);
+  return cuda_check(cudaGetLastError(), "kvpop_future_target: finalize");
 }
 
 // ---------------------------------------------------------------------------
