@@ -149,7 +149,7 @@ def run_gpu(args, rank, world, local_rank):
     ws_tgt = torch.empty(kvpop.target_workspace_size(b, S, wl.Hq, H), dtype=torch.uint8, device=dev)
     rank_t = torch.empty((b, H, S), dtype=torch.int32, device=dev)
     tau_t, ev_t = torch.empty_like(rank_t), torch.empty_like(rank_t)
-    lists = torch.empty((b, H, (S + 63) // 64, wl.k), dtype=torch.int32, device=dev)
+    lists = torch.empty((b, H, (S + 63) // 64, wl.k, 2), dtype=torch.int32, device=dev)
     O = torch.empty_like(q)
     lse_s = torch.empty((b, wl.Hq, S), dtype=torch.float32, device=dev)
     lse_d = torch.empty_like(lse_s)

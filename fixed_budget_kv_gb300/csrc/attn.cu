@@ -1,22 +1,33 @@
 // kvpop_attn_fwd: causal GQA attention over the fixed-budget retained set
-// (sparse) or over all past tokens (dense teacher), returning O and the
-// log-sum-exp ("KVpop ... 精读笔记", sections 2.1 and 2.3).
+// (sparse) or over all past tokens (dense), returning O and the log-sum-exp
+// ("KVpop ... 精读笔记", sections 2.1 and 2.3).  The dense LSE-only teacher pass
+// lives in dense_lse.cu.
 //
 // One CTA owns two 128-row query tiles of one (batch, KV head).  A row is one
 // (position, query head) pair: the G query heads of a KV head share every K/V
 // tile, so a tile covers 128/G positions.  Warp roles (384 threads):
 //   warp 0      TMA producer (Q; K/V in dense mode) and, in sparse mode, the
-//               key metadata (position, eviction row) of each KV tile
+//               key metadata of each KV tile: (position, eviction row) per key
+//               and, per 32-key chunk, the latest position and the earliest
+//               eviction row, so that rows inside that range skip masking
 //   warp 1      TMEM allocation and the single-thread tcgen05.mma issuer
-//   warps 2-3   sparse mode: gather of the retained K/V rows with cp.async
-//               into the 128-byte-swizzled operand layout
+//   warps 2-3   sparse mode: K/V rows of sinks and long-range keys gathered
+//               with cp.async into the 128B-swizzled operand layout; the
+//               contiguous span (window and recent tokens) by TMA tiles
 //   warps 4-7   softmax for query tile 0 (one thread per row / TMEM lane)
 //   warps 8-11  softmax for query tile 1
 // S = Q K^T lands in TMEM (fp32); the softmax warps turn it into bf16 P in
 // place and the MMA warp accumulates O += P V with A read from TMEM.  The two
 // query tiles ping-pong so that the tensor core works on one tile while the
-// softmax warps work on the other.  Running max updates are lazy: O and the
+// softmax warps work on the other.  Running-max updates are lazy: O and the
 // row sum are rescaled only when the max grows by more than 2^8.
+//
+// Sparse key plan of a CTA covering rows [qb0, qb1] with list i = qb0 / 64
+// (taken at row q0 = 64 i <= qb0):
+//   [0, s)                          sinks
+//   list i                          long-range keys held at row q0
+//   [max(s, q0 - w + 1), qb1]       every later token (window + new entries)
+// and row q keeps key t exactly when t <= q < evict_at[t].
 #include "common.cuh"
 
 namespace kvpop {
@@ -33,7 +44,7 @@ struct AttnParams {
   const __nv_bfloat16* k;
   const __nv_bfloat16* v;
   const int32_t* evict_at;
-  const int32_t* lists;
+  const int2* lists;
   __nv_bfloat16* O;
   float* lse;
   int* status;
@@ -42,17 +53,17 @@ struct AttnParams {
   float scale_log2;
 };
 
-template <int D, bool WITH_O, bool SPARSE>
+template <int D, bool SPARSE>
 struct Layout {
   static constexpr int DH = D / 64;
-  static constexpr int NS = WITH_O ? (D == 128 ? 2 : 4) : (D == 128 ? 4 : 8);
+  static constexpr int NS = D == 128 ? 2 : 4;
   static constexpr int q_off = 0;
   static constexpr int k_off = q_off + 2 * DH * kBlockBytes;
   static constexpr int v_off = k_off + NS * DH * kBlockBytes;
-  static constexpr int meta_off = v_off + (WITH_O ? NS * DH * kBlockBytes : 0);
-  static constexpr int bar_off = meta_off + (SPARSE ? kMetaStages * kKeys * 8 : 0);
-  // barrier block
-  static constexpr int nbar = 1 + 4 * NS + 4 + 4 + 2 + 1 + 2 * kMetaStages + 1;
+  static constexpr int meta_off = v_off + NS * DH * kBlockBytes;
+  static constexpr int meta_bytes = kMetaStages * (kKeys + 4) * 8;  // entries + chunk summaries
+  static constexpr int bar_off = meta_off + (SPARSE ? meta_bytes : 0);
+  static constexpr int nbar = 1 + 4 * NS + 2 + 2 + 1 + 2 * kMetaStages + 1;
   static constexpr int misc_off = bar_off + nbar * 8;
   static constexpr int total = misc_off + 64 + 1024;  // + alignment slack
 };
@@ -61,7 +72,7 @@ template <int NS>
 struct Bars {
   uint64_t q_full;
   uint64_t k_full[NS], k_empty[NS], v_full[NS], v_empty[NS];
-  uint64_t s_full[2][2], s_empty[2][2];
+  uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t o_final;
   uint64_t meta_full[kMetaStages], meta_empty[kMetaStages];
@@ -70,9 +81,9 @@ struct Bars {
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 
-template <int D, bool WITH_O, bool SPARSE>
+template <int D, bool SPARSE>
 __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant__ AttnParams p) {
-  using L = Layout<D, WITH_O, SPARSE>;
+  using L = Layout<D, SPARSE>;
   constexpr int DH = L::DH;
   constexpr int NS = L::NS;
   extern __shared__ uint8_t smem_raw[];
@@ -80,7 +91,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   Bars<NS>* bars = reinterpret_cast<Bars<NS>*>(smem + L::bar_off);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::misc_off + 4);
-  int2* meta = reinterpret_cast<int2*>(smem + L::meta_off);
+  int2* meta = reinterpret_cast<int2*>(smem + L::meta_off);  // [stage][128 entries + 4 summaries]
   const uint32_t sbase = smem_u32(smem);
 
   const int warp = warp_id(), lane = lane_id();
@@ -90,32 +101,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   const int qb0 = qblock * 2 * P;
   const int qb1 = min(qb0 + 2 * P, S) - 1;
 
-  // keys of this CTA: [sinks][long-range list][contiguous span] or [0, qb1]
-  int n_sink = 0, n_list = 0, sp0 = 0, NK;
-  const int32_t* list = nullptr;
+  // key plan: NTg gathered tiles ([sinks][list]) then the span tiles (TMA)
+  int n_sink = 0, n_sl = 0, sp0 = 0, n_span = 0, NTg = 0, NT;
+  const int2* list = nullptr;
   if (SPARSE) {
     const int jl = qb0 / KVPOP_LIST_QBLOCK;
     const int q0l = jl * KVPOP_LIST_QBLOCK;
     n_sink = min(p.s, qb1 + 1);
-    n_list = p.kk > 0 ? min(p.kk, max(0, q0l - p.w - p.s + 1)) : 0;
+    const int n_list = p.kk > 0 ? min(p.kk, max(0, q0l - p.w - p.s + 1)) : 0;
     list = p.lists + ((size_t)(b * p.H + h) * p.nL + jl) * (size_t)max(p.kk, 1);
+    n_sl = n_sink + n_list;
     sp0 = max(p.s, q0l - p.w + 1);
-    NK = n_sink + n_list + max(0, qb1 - sp0 + 1);
+    n_span = max(0, qb1 - sp0 + 1);
+    NTg = (n_sl + kKeys - 1) / kKeys;
+    NT = NTg + (n_span + kKeys - 1) / kKeys;
   } else {
-    NK = qb1 + 1;
+    NT = (qb1 + 1 + kKeys - 1) / kKeys;
   }
-  const int NT = (NK + kKeys - 1) / kKeys;
-  auto key_pos = [&](int i) -> int {
-    int pos = -1;
-    if (i < n_sink) pos = i;
-    else if (i < n_sink + n_list) pos = __ldg(list + (i - n_sink));
-    else if (i < NK) pos = sp0 + (i - n_sink - n_list);
-    if (pos >= S || pos < -1) {  // a corrupt list entry: never read outside [0, S)
-      report_error(p.status, KVPOP_ERR_INTERNAL, SITE_INTERNAL_CHECK, 10);
-      pos = -1;
-    }
-    return pos;
-  };
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
@@ -125,17 +127,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
       mbar_init(&bars->k_empty[i], 1);
       mbar_init(&bars->v_empty[i], 1);
     }
-    for (int a = 0; a < 2; ++a)
-      for (int c = 0; c < 2; ++c) {
-        mbar_init(&bars->s_full[a][c], 1);
-        mbar_init(&bars->s_empty[a][c], 4);
-      }
+    mbar_init(&bars->s_full[0], 1);
+    mbar_init(&bars->s_full[1], 1);
     mbar_init(&bars->p_full[0], 4);
     mbar_init(&bars->p_full[1], 4);
     mbar_init(&bars->o_final, 1);
     for (int i = 0; i < kMetaStages; ++i) {
       mbar_init(&bars->meta_full[i], 1);
-      mbar_init(&bars->meta_empty[i], 8);
+      mbar_init(&bars->meta_empty[i], 10);  // 8 softmax warps + 2 loader warps
     }
     mbar_init(&bars->drain, 1);
     *abort_flag = 0;
@@ -160,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   const uint32_t v_addr = sbase + L::v_off;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ producer / metadata
     if (lane == 0) {
       tma_prefetch_desc(&p.tq);
       mbar_arrive_expect_tx(&bars->q_full, 2 * DH * kBlockBytes);
@@ -182,16 +181,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
           for (int dh = 0; dh < DH; ++dh)
             tma_load_4d(smem + L::k_off + (st * DH + dh) * kBlockBytes, &p.tk, &bars->k_full[st],
                         dh * 64, h, j * kKeys, b);
-          if (WITH_O) {
-            if (!mbar_wait(&bars->v_empty[st], ph ^ 1, abort_flag)) {
-              fail(SITE_ATTN_PRODUCER, 2);
-              break;
-            }
-            mbar_arrive_expect_tx(&bars->v_full[st], DH * kBlockBytes);
-            for (int dh = 0; dh < DH; ++dh)
-              tma_load_4d(smem + L::v_off + (st * DH + dh) * kBlockBytes, &p.tv, &bars->v_full[st],
-                          dh * 64, h, j * kKeys, b);
+          if (!mbar_wait(&bars->v_empty[st], ph ^ 1, abort_flag)) {
+            fail(SITE_ATTN_PRODUCER, 2);
+            break;
           }
+          mbar_arrive_expect_tx(&bars->v_full[st], DH * kBlockBytes);
+          for (int dh = 0; dh < DH; ++dh)
+            tma_load_4d(smem + L::v_off + (st * DH + dh) * kBlockBytes, &p.tv, &bars->v_full[st],
+                        dh * 64, h, j * kKeys, b);
         }
       }
     } else {
@@ -202,9 +199,32 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
           if (lane == 0) fail(SITE_ATTN_PRODUCER, 3);
           break;
         }
-        for (int e = lane; e < kKeys; e += 32) {
-          const int pos = key_pos(j * kKeys + e);
-          meta[ms * kKeys + e] = pos >= 0 ? make_int2(pos, __ldg(ev + pos)) : make_int2(0x7fffffff, 0);
+        int2* m = meta + ms * (kKeys + 4);
+        // lane owns entries lane + 32 c: chunk c has one entry per lane
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int r = lane + 32 * c;
+          int2 e = make_int2(0x7fffffff, 0);  // padding: never visible
+          if (j < NTg) {
+            const int i = j * kKeys + r;
+            if (i < n_sink) e = make_int2(i, S);
+            else if (i < n_sl) e = __ldg(list + (i - n_sink));
+          } else {
+            const int pos = sp0 + (j - NTg) * kKeys + r;
+            if (pos <= qb1) e = make_int2(pos, __ldg(ev + pos));
+          }
+          if (e.x != 0x7fffffff && (e.x < 0 || e.x >= S)) {  // a corrupt list entry: never gathered
+            report_error(p.status, KVPOP_ERR_INTERNAL, SITE_INTERNAL_CHECK, 10);
+            e = make_int2(0x7fffffff, 0);
+          }
+          m[r] = e;
+          int lo = e.x, hi = e.y;  // rows in [lo, hi) see every key of the chunk
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            lo = max(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+            hi = min(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+          }
+          if (lane == 0) m[kKeys + c] = make_int2(lo, hi);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->meta_full[ms]);
@@ -218,14 +238,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
       tc_fence_after();
       constexpr uint32_t idesc_qk = idesc_bf16(128, 128, 0);
       constexpr uint32_t idesc_pv = idesc_bf16(128, D, 1);
-      auto issue_s = [&](int qt, int st, uint32_t d_tmem) {
+      auto issue_s = [&](int qt, int st) {
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const int dh = ks >> 2;
           const uint32_t w32 = (uint32_t)(ks & 3) * 32;
           const uint64_t a = smem_desc_sw128(q_addr + (qt * DH + dh) * kBlockBytes + w32, 16, 1024);
           const uint64_t bd = smem_desc_sw128(k_addr + (st * DH + dh) * kBlockBytes + w32, 16, 1024);
-          mma_ss(d_tmem, a, bd, idesc_qk, ks > 0 ? 1u : 0u);
+          mma_ss(tbase + 128 * qt, a, bd, idesc_qk, ks > 0 ? 1u : 0u);
         }
       };
       auto wait_kv = [&](uint64_t* bar, uint32_t ph, int detail) -> bool {
@@ -233,71 +253,50 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
           fail(SITE_ATTN_MMA, detail);
           return false;
         }
-        if (SPARSE) fence_proxy_async_smem();
+        if (SPARSE) fence_proxy_async_smem();  // cp.async rows -> tensor-core reads
         tc_fence_after();
         return true;
       };
-      if (ok && WITH_O) {
-        // S tiles at columns 0 / 128, O tiles at 256 / 384
-        if (NT > 0) {
-          ok = wait_kv(&bars->k_full[0], 0, 2);
-          if (ok) {
-            issue_s(0, 0, tbase + 0);
-            mma_commit(&bars->s_full[0][0]);
-            issue_s(1, 0, tbase + 128);
-            mma_commit(&bars->s_full[1][0]);
-            mma_commit(&bars->k_empty[0]);
-          }
-        }
-        for (int j = 0; ok && j < NT; ++j) {
-          const int st = j % NS;
-          const uint32_t ph = (j / NS) & 1;
-          for (int qt = 0; qt < 2 && ok; ++qt) {
-            if (!mbar_wait(&bars->p_full[qt], j & 1, abort_flag)) {
-              fail(SITE_ATTN_MMA, 3);
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            if (qt == 0 && !(ok = wait_kv(&bars->v_full[st], ph, 4))) break;
-#pragma unroll
-            for (int ks = 0; ks < kKeys / 16; ++ks) {
-              const uint64_t bd = smem_desc_sw128(v_addr + st * DH * kBlockBytes + ks * 2048,
-                                                  DH > 1 ? kBlockBytes : 16, 1024);
-              mma_ts(tbase + 256 + 128 * qt, tbase + 128 * qt + ks * 8, bd, idesc_pv,
-                     (j > 0 || ks > 0) ? 1u : 0u);
-            }
-            if (qt == 1) mma_commit(&bars->v_empty[st]);
-            if (j + 1 < NT) {
-              const int st1 = (j + 1) % NS;
-              if (qt == 0 && !(ok = wait_kv(&bars->k_full[st1], ((j + 1) / NS) & 1, 5))) break;
-              issue_s(qt, st1, tbase + 128 * qt);
-              mma_commit(&bars->s_full[qt][0]);
-              if (qt == 1) mma_commit(&bars->k_empty[st1]);
-            }
-          }
-        }
-        mma_commit(&bars->o_final);
-      } else if (ok) {
-        for (int j = 0; j < NT; ++j) {
-          const int st = j % NS;
-          if (!wait_kv(&bars->k_full[st], (j / NS) & 1, 6)) break;
-          const int buf = j & 1;
-          bool ok2 = true;
-          for (int qt = 0; qt < 2; ++qt) {
-            if (!mbar_wait(&bars->s_empty[qt][buf], ((j >> 1) & 1) ^ 1, abort_flag)) {
-              fail(SITE_ATTN_MMA, 7);
-              ok2 = false;
-              break;
-            }
-            tc_fence_after();
-            issue_s(qt, st, tbase + 128 * (2 * qt + buf));
-            mma_commit(&bars->s_full[qt][buf]);
-          }
-          if (!ok2) break;
-          mma_commit(&bars->k_empty[st]);
+      // S tiles at columns 0 / 128 (P written over them), O tiles at 256 / 384
+      if (ok && NT > 0) {
+        ok = wait_kv(&bars->k_full[0], 0, 2);
+        if (ok) {
+          issue_s(0, 0);
+          mma_commit(&bars->s_full[0]);
+          issue_s(1, 0);
+          mma_commit(&bars->s_full[1]);
+          mma_commit(&bars->k_empty[0]);
         }
       }
+      for (int j = 0; ok && j < NT; ++j) {
+        const int st = j % NS;
+        const uint32_t ph = (j / NS) & 1;
+        for (int qt = 0; qt < 2 && ok; ++qt) {
+          if (!mbar_wait(&bars->p_full[qt], j & 1, abort_flag)) {
+            fail(SITE_ATTN_MMA, 3);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (qt == 0 && !(ok = wait_kv(&bars->v_full[st], ph, 4))) break;
+#pragma unroll
+          for (int ks = 0; ks < kKeys / 16; ++ks) {
+            const uint64_t bd = smem_desc_sw128(v_addr + st * DH * kBlockBytes + ks * 2048,
+                                                DH > 1 ? kBlockBytes : 16, 1024);
+            mma_ts(tbase + 256 + 128 * qt, tbase + 128 * qt + ks * 8, bd, idesc_pv,
+                   (j > 0 || ks > 0) ? 1u : 0u);
+          }
+          if (qt == 1) mma_commit(&bars->v_empty[st]);
+          if (j + 1 < NT) {
+            const int st1 = (j + 1) % NS;
+            if (qt == 0 && !(ok = wait_kv(&bars->k_full[st1], ((j + 1) / NS) & 1, 5))) break;
+            issue_s(qt, st1);
+            mma_commit(&bars->s_full[qt]);
+            if (qt == 1) mma_commit(&bars->k_empty[st1]);
+          }
+        }
+      }
+      mma_commit(&bars->o_final);
       // drain every issued MMA before teardown
       mma_commit(&bars->drain);
       mbar_wait(&bars->drain, 0, nullptr);
@@ -309,148 +308,35 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     const int row = quarter * 32 + lane;
     const int p_row = row / G, g = row - p_row * G;
     const int q = qb0 + qt * P + p_row;
+    const int q_first = qb0 + qt * P;
     const int jh = h * G + g;
     const uint32_t tl = tbase + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t s_col = 128 * qt, o_col = 256 + 128 * qt;
     const float sl2 = p.scale_log2;
+    const uint64_t s2 = pack2(sl2, sl2);
     float m_ref = neg_inf(), l = 0.0f;
     bool ok = true;
-    if (WITH_O) {
-      const uint32_t s_col = 128 * qt, o_col = 256 + 128 * qt;
-      for (int j = 0; j < NT; ++j) {
-        if (!warp_wait(&bars->s_full[qt][0], j & 1, abort_flag)) {
-          if (lane == 0) fail(SITE_ATTN_SOFTMAX, 1);
+    for (int j = 0; j < NT; ++j) {
+      if (!warp_wait(&bars->s_full[qt], j & 1, abort_flag)) {
+        if (lane == 0) fail(SITE_ATTN_SOFTMAX, 1);
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int ms = j % kMetaStages;
+      const int2* km = meta + ms * (kKeys + 4);
+      if (SPARSE) {
+        if (!warp_wait(&bars->meta_full[ms], (j / kMetaStages) & 1, abort_flag)) {
+          if (lane == 0) fail(SITE_ATTN_SOFTMAX, 2);
           ok = false;
           break;
         }
-        tc_fence_after();
-        const int2* km = nullptr;
-        const int ms = j % kMetaStages;
-        if (SPARSE) {
-          if (!warp_wait(&bars->meta_full[ms], (j / kMetaStages) & 1, abort_flag)) {
-            if (lane == 0) fail(SITE_ATTN_SOFTMAX, 2);
-            ok = false;
-            break;
-          }
-          km = meta + ms * kKeys;
-        }
-        // pass 1: visibility bits and the tile max
-        uint32_t vis[4];
-        float mt = neg_inf();
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          uint32_t r[32];
-          tmem_ld32(tl + s_col + ch * 32, r);
-          tmem_wait_ld();
-          uint32_t bits = 0;
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const int col = ch * 32 + c;
-            bool visible;
-            if (SPARSE) {
-              const int2 m = km[col];
-              visible = (m.x <= q) && (q < m.y);
-            } else {
-              visible = (j * kKeys + col) <= q;
-            }
-            if (visible) {
-              bits |= 1u << c;
-              mt = fmaxf(mt, __uint_as_float(r[c]));
-            }
-          }
-          vis[ch] = bits;
-        }
-        // lazy rescale of the running max
-        const float m_new = fmaxf(m_ref, mt);
-        const bool need = (m_new - m_ref) * sl2 > kRescaleLog2;  // true when m_ref == -inf and mt finite
-        float alpha = 1.0f;
-        if (need) {
-          alpha = ex2_approx((m_ref - m_new) * sl2);
-          l *= alpha;
-          m_ref = m_new;
-        }
-        if (__any_sync(0xffffffffu, need) && j > 0) {
-#pragma unroll
-          for (int cd = 0; cd < D / 32; ++cd) {
-            uint32_t r[32];
-            tmem_ld32(tl + o_col + cd * 32, r);
-            tmem_wait_ld();
-#pragma unroll
-            for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * alpha);
-            tmem_st32(tl + o_col + cd * 32, r);
-          }
-          tmem_wait_st();
-        }
-        // pass 2: P = exp2(s * scale_log2 - m) as bf16, written over S
-        const float neg = (m_ref == neg_inf()) ? 0.0f : -m_ref * sl2;
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          uint32_t r[32];
-          tmem_ld32(tl + s_col + ch * 32, r);
-          tmem_wait_ld();
-          uint32_t pk[16];
-#pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            float p0 = ((vis[ch] >> c) & 1u) ? ex2_approx(fmaf(__uint_as_float(r[c]), sl2, neg)) : 0.0f;
-            float p1 = ((vis[ch] >> (c + 1)) & 1u) ? ex2_approx(fmaf(__uint_as_float(r[c + 1]), sl2, neg))
-                                                   : 0.0f;
-            l += p0 + p1;
-            pk[c >> 1] = pack_bf16x2(p0, p1);
-          }
-          tmem_st16(tl + s_col + ch * 16, pk);
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&bars->p_full[qt]);
-          if (SPARSE) mbar_arrive(&bars->meta_empty[ms]);
-        }
       }
-      // epilogue: O / l and the LSE
-      if (ok) {
-        if (!warp_wait(&bars->o_final, 0, abort_flag)) {
-          if (lane == 0) fail(SITE_ATTN_EPILOGUE, 1);
-          ok = false;
-        }
-      }
-      if (ok) {
-        tc_fence_after();
-        const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-        __nv_bfloat16* orow = p.O + (((size_t)b * S + q) * p.Hq + jh) * D;
-#pragma unroll
-        for (int cd = 0; cd < D / 32; ++cd) {
-          uint32_t r[32];
-          tmem_ld32(tl + o_col + cd * 32, r);
-          tmem_wait_ld();
-          uint32_t pk[16];
-#pragma unroll
-          for (int c = 0; c < 32; c += 2)
-            pk[c >> 1] = pack_bf16x2(__uint_as_float(r[c]) * inv, __uint_as_float(r[c + 1]) * inv);
-          if (q <= qb1) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + cd * 32);
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-              dst[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-          }
-        }
-        if (q <= qb1)
-          p.lse[((size_t)b * p.Hq + jh) * S + q] =
-              l > 0.0f ? (m_ref * sl2 + __log2f(l)) * 0.69314718055994531f : neg_inf();
-      }
-    } else {
-      // LSE only: per row l = sum 2^(s*sl2 - m_ref*sl2) against a lazily moved
-      // reference m_ref; a 32-column chunk that would overflow moves it.
-      const int q_first = qb0 + qt * P;
-      for (int j = 0; j < NT; ++j) {
-        const int buf = j & 1;
-        if (!warp_wait(&bars->s_full[qt][buf], (j >> 1) & 1, abort_flag)) {
-          if (lane == 0) fail(SITE_ATTN_SOFTMAX, 3);
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t s_col = 128 * (2 * qt + buf);
-        const bool diag = (j * kKeys + kKeys - 1) > q_first;  // some key may lie after some row
+      const bool diag = !SPARSE && (j * kKeys + kKeys - 1) > q_first;
+      // pass 1: visibility of the 32-key chunks and the tile max
+      uint32_t vis[4];
+      float mt = neg_inf();
+      {
         uint32_t ra[32], rb[32];
         tmem_ld32(tl + s_col, ra);
 #pragma unroll
@@ -459,37 +345,134 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
           uint32_t(&nxt)[32] = (ch & 1) ? ra : rb;
           tmem_wait_ld_dep(cur);
           if (ch < 3) tmem_ld32(tl + s_col + (ch + 1) * 32, nxt);
-          if (diag) {
-            const int t0 = j * kKeys + ch * 32;
+          bool fast;
+          if (SPARSE) {
+            const int2 sum = km[kKeys + ch];
+            fast = q >= sum.x && q < sum.y;
+          } else {
+            fast = !diag || (j * kKeys + ch * 32 + 31) <= q;
+          }
+          uint32_t bits = 0xffffffffu;
+          if (!fast) {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              bool visible;
+              if (SPARSE) {
+                const int2 e = km[ch * 32 + c];
+                visible = e.x <= q && q < e.y;
+              } else {
+                visible = j * kKeys + ch * 32 + c <= q;
+              }
+              if (!visible) {
+                bits &= ~(1u << c);
+                cur[c] = 0xff800000u;
+              }
+            }
+          }
+          vis[ch] = bits;
+          mt = fmaxf(mt, max32(cur));
+        }
+      }
+      // lazy rescale of the running max
+      const float m_new = fmaxf(m_ref, mt);
+      const bool need = (m_new - m_ref) * sl2 > kRescaleLog2;  // true when m_ref == -inf and mt finite
+      float alpha = 1.0f;
+      if (need) {
+        alpha = ex2_approx((m_ref - m_new) * sl2);
+        l *= alpha;
+        m_ref = m_new;
+      }
+      if (__any_sync(0xffffffffu, need) && j > 0) {
+        // O of tile j-1 is complete: s_full for tile j was committed after it
+#pragma unroll
+        for (int cd = 0; cd < D / 32; ++cd) {
+          uint32_t r[32];
+          tmem_ld32(tl + o_col + cd * 32, r);
+          tmem_wait_ld_dep(r);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * alpha);
+          tmem_st32(tl + o_col + cd * 32, r);
+        }
+        tmem_wait_st();
+      }
+      // pass 2: P = exp2(s * scale_log2 - m) as bf16, written over S
+      const float nm = (m_ref == neg_inf()) ? 0.0f : -m_ref * sl2;
+      const uint64_t n2 = pack2(nm, nm);
+      uint64_t lacc = 0;
+      {
+        uint32_t ra[32], rb[32];
+        tmem_ld32(tl + s_col, ra);
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t(&cur)[32] = (ch & 1) ? rb : ra;
+          uint32_t(&nxt)[32] = (ch & 1) ? ra : rb;
+          tmem_wait_ld_dep(cur);
+          if (ch < 3) tmem_ld32(tl + s_col + (ch + 1) * 32, nxt);
+          const uint32_t bits = vis[ch];
+          if (bits != 0xffffffffu) {
 #pragma unroll
             for (int c = 0; c < 32; ++c)
-              if (t0 + c > q) cur[c] = 0xff800000u;
+              if (!((bits >> c) & 1u)) cur[c] = 0xff800000u;
           }
-          if (m_ref == neg_inf()) {
-            const float cm = max32(cur);
-            if (cm == neg_inf()) continue;
-            m_ref = cm;
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            const uint64_t x = fma2(pack2(__uint_as_float(cur[c]), __uint_as_float(cur[c + 1])), s2, n2);
+            float e0, e1;
+            unpack2(x, e0, e1);
+            const float p0 = ex2_approx(e0), p1 = ex2_approx(e1);
+            lacc = add2(lacc, pack2(p0, p1));
+            pk[c >> 1] = pack_bf16x2(p0, p1);
           }
-          const uint64_t s2 = pack2(sl2, sl2);
-          float sum = exp2_sum32(cur, s2, pack2(-m_ref * sl2, -m_ref * sl2));
-          if (!(sum <= 0x1p64f)) {  // a score far above the reference: move it
-            const float cm = max32(cur);
-            l *= ex2_approx((m_ref - cm) * sl2);
-            m_ref = cm;
-            sum = exp2_sum32(cur, s2, pack2(-m_ref * sl2, -m_ref * sl2));
-          }
-          l += sum;
+          tmem_st16(tl + s_col + ch * 16, pk);
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->s_empty[qt][buf]);
       }
-      if (ok && q <= qb1)
+      {
+        float l0, l1;
+        unpack2(lacc, l0, l1);
+        l += l0 + l1;
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bars->p_full[qt]);
+        if (SPARSE) mbar_arrive(&bars->meta_empty[ms]);
+      }
+    }
+    // epilogue: O / l and the LSE
+    if (ok) {
+      if (!warp_wait(&bars->o_final, 0, abort_flag)) {
+        if (lane == 0) fail(SITE_ATTN_EPILOGUE, 1);
+        ok = false;
+      }
+    }
+    if (ok) {
+      tc_fence_after();
+      const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+      __nv_bfloat16* orow = p.O + (((size_t)b * S + q) * p.Hq + jh) * D;
+#pragma unroll
+      for (int cd = 0; cd < D / 32; ++cd) {
+        uint32_t r[32];
+        tmem_ld32(tl + o_col + cd * 32, r);
+        tmem_wait_ld_dep(r);
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 2)
+          pk[c >> 1] = pack_bf16x2(__uint_as_float(r[c]) * inv, __uint_as_float(r[c + 1]) * inv);
+        if (q <= qb1) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + cd * 32);
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            dst[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        }
+      }
+      if (q <= qb1)
         p.lse[((size_t)b * p.Hq + jh) * S + q] =
             l > 0.0f ? (m_ref * sl2 + __log2f(l)) * 0.69314718055994531f : neg_inf();
     }
   } else if (SPARSE) {
-    // ------------------------------------------------------------ gather warps 2-3
+    // ------------------------------------------------------------ K/V loaders (warps 2-3)
     constexpr int CH = D / 8;  // 16-byte chunks per row
     constexpr int RSTEP = 64 / CH;
     const int gt = (warp - 2) * 32 + lane;
@@ -501,37 +484,71 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     for (int j = 0; j < NT; ++j) {
       const int st = j % NS;
       const uint32_t ph = (j / NS) & 1;
+      const int ms = j % kMetaStages;
+      const bool gathered = j < NTg;
       int pos[kKeys / RSTEP];
+      if (!warp_wait(&bars->meta_full[ms], (j / kMetaStages) & 1, abort_flag)) {
+        if (lane == 0) fail(SITE_ATTN_PRODUCER, 6);
+        break;
+      }
+      if (gathered) {
+        const int2* km = meta + ms * (kKeys + 4);
 #pragma unroll
-      for (int i = 0; i < kKeys / RSTEP; ++i) pos[i] = key_pos(j * kKeys + rg + i * RSTEP);
+        for (int i = 0; i < kKeys / RSTEP; ++i) pos[i] = km[rg + i * RSTEP].x;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->meta_empty[ms]);
       if (!mbar_wait(&bars->k_empty[st], ph ^ 1, abort_flag)) {
         fail(SITE_ATTN_PRODUCER, 4);
         break;
       }
-      uint8_t* kdst = smem + L::k_off + (st * DH + dh) * kBlockBytes;
+      const int span_row = sp0 + (j - NTg) * kKeys;
+      if (gathered) {
+        uint8_t* kdst = smem + L::k_off + (st * DH + dh) * kBlockBytes;
 #pragma unroll
-      for (int i = 0; i < kKeys / RSTEP; ++i) {
-        const int r = rg + i * RSTEP;
-        const bool valid = pos[i] >= 0;
-        cp_async_16(kdst + sw128_offset(r, cc), valid ? (const void*)(kb + (size_t)pos[i] * kv_stride)
-                                                       : (const void*)p.k,
-                    valid ? 16u : 0u);
+        for (int i = 0; i < kKeys / RSTEP; ++i) {
+          const int r = rg + i * RSTEP;
+          const bool valid = pos[i] != 0x7fffffff;
+          cp_async_16(kdst + sw128_offset(r, cc), valid ? (const void*)(kb + (size_t)pos[i] * kv_stride)
+                                                         : (const void*)p.k,
+                      valid ? 16u : 0u);
+        }
+        cp_async_arrive_noinc(&bars->k_full[st]);
+      } else {
+        if (gt == 0) {
+          mbar_arrive_expect_tx(&bars->k_full[st], DH * kBlockBytes);
+          for (int d2 = 0; d2 < DH; ++d2)
+            tma_load_4d(smem + L::k_off + (st * DH + d2) * kBlockBytes, &p.tk, &bars->k_full[st], d2 * 64,
+                        h, span_row, b);
+        } else {
+          mbar_arrive(&bars->k_full[st]);
+        }
       }
-      cp_async_arrive_noinc(&bars->k_full[st]);
       if (!mbar_wait(&bars->v_empty[st], ph ^ 1, abort_flag)) {
         fail(SITE_ATTN_PRODUCER, 5);
         break;
       }
-      uint8_t* vdst = smem + L::v_off + (st * DH + dh) * kBlockBytes;
+      if (gathered) {
+        uint8_t* vdst = smem + L::v_off + (st * DH + dh) * kBlockBytes;
 #pragma unroll
-      for (int i = 0; i < kKeys / RSTEP; ++i) {
-        const int r = rg + i * RSTEP;
-        const bool valid = pos[i] >= 0;
-        cp_async_16(vdst + sw128_offset(r, cc), valid ? (const void*)(vb + (size_t)pos[i] * kv_stride)
-                                                       : (const void*)p.v,
-                    valid ? 16u : 0u);
+        for (int i = 0; i < kKeys / RSTEP; ++i) {
+          const int r = rg + i * RSTEP;
+          const bool valid = pos[i] != 0x7fffffff;
+          cp_async_16(vdst + sw128_offset(r, cc), valid ? (const void*)(vb + (size_t)pos[i] * kv_stride)
+                                                         : (const void*)p.v,
+                      valid ? 16u : 0u);
+        }
+        cp_async_arrive_noinc(&bars->v_full[st]);
+      } else {
+        if (gt == 0) {
+          mbar_arrive_expect_tx(&bars->v_full[st], DH * kBlockBytes);
+          for (int d2 = 0; d2 < DH; ++d2)
+            tma_load_4d(smem + L::v_off + (st * DH + d2) * kBlockBytes, &p.tv, &bars->v_full[st], d2 * 64,
+                        h, span_row, b);
+        } else {
+          mbar_arrive(&bars->v_full[st]);
+        }
       }
-      cp_async_arrive_noinc(&bars->v_full[st]);
     }
     cp_async_wait_all();
   }
@@ -546,10 +563,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   }
 }
 
-template <int D, bool WITH_O, bool SPARSE>
+template <int D, bool SPARSE>
 kvpop_status launch(const AttnParams& prm, int b, int H, cudaStream_t stream) {
-  using L = Layout<D, WITH_O, SPARSE>;
-  auto kern = attn_kernel<D, WITH_O, SPARSE>;
+  using L = Layout<D, SPARSE>;
+  auto kern = attn_kernel<D, SPARSE>;
   kvpop_status st = cuda_check(
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::total),
       "kvpop_attn_fwd: smem attribute");
@@ -606,6 +623,11 @@ extern "C" kvpop_status kvpop_attn_fwd(const void* q, const void* k, const void*
     set_last_error("kvpop_attn_fwd: q, k, v, O must be 16-byte aligned");
     return KVPOP_ERR_UNSUPPORTED;
   }
+  const float sc = scale > 0.0f ? scale : 1.0f / sqrtf((float)D);
+  const float scale_log2 = sc * 1.4426950408889634f;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (!sparse && !O) return launch_dense_lse(q, k, b, S, Hq, H, D, scale_log2, lse, cs);
+
   AttnParams prm;
   memset(&prm, 0, sizeof(prm));
   const int P = 128 / G;
@@ -617,13 +639,13 @@ extern "C" kvpop_status kvpop_attn_fwd(const void* q, const void* k, const void*
     uint64_t sk[3] = {(uint64_t)D * 2, (uint64_t)H * D * 2, (uint64_t)S * H * D * 2};
     uint32_t bk[4] = {64, 1, 128, 1};
     if (!make_tmap_4d(&prm.tq, q, dq, sq, bq) || !make_tmap_4d(&prm.tk, k, dk, sk, bk) ||
-        (v && !make_tmap_4d(&prm.tv, v, dk, sk, bk)))
+        !make_tmap_4d(&prm.tv, v, dk, sk, bk))
       return KVPOP_ERR_CUDA;
   }
   prm.k = static_cast<const __nv_bfloat16*>(k);
   prm.v = static_cast<const __nv_bfloat16*>(v);
   prm.evict_at = evict_at;
-  prm.lists = lists;
+  prm.lists = reinterpret_cast<const int2*>(lists);
   prm.O = static_cast<__nv_bfloat16*>(O);
   prm.lse = lse;
   prm.status = device_status_ptr();
@@ -637,12 +659,7 @@ extern "C" kvpop_status kvpop_attn_fwd(const void* q, const void* k, const void*
   prm.w = bud.w;
   prm.kk = bud.k;
   prm.nL = (S + KVPOP_LIST_QBLOCK - 1) / KVPOP_LIST_QBLOCK;
-  const float sc = scale > 0.0f ? scale : 1.0f / sqrtf((float)D);
-  prm.scale_log2 = sc * 1.4426950408889634f;
-  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  if (sparse) {
-    return D == 128 ? launch<128, true, true>(prm, b, H, cs) : launch<64, true, true>(prm, b, H, cs);
-  }
-  if (O) return D == 128 ? launch<128, true, false>(prm, b, H, cs) : launch<64, true, false>(prm, b, H, cs);
-  return launch_dense_lse(q, k, b, S, Hq, H, D, prm.scale_log2, lse, cs);
+  prm.scale_log2 = scale_log2;
+  if (sparse) return D == 128 ? launch<128, true>(prm, b, H, cs) : launch<64, true>(prm, b, H, cs);
+  return D == 128 ? launch<128, false>(prm, b, H, cs) : launch<64, false>(prm, b, H, cs);
 }

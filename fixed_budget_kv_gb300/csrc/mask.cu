@@ -386,10 +386,11 @@ __global__ void evict_search(const int32_t* __restrict__ rank, const int32_t* __
 // ---------------------------------------------------------------------------
 
 // Ordered compaction of candidates in [0, n) where `cand(i)` gives the
-// position; keeps those with evict_at > q0; returns the count.
-template <typename Cand>
-__device__ int compact_alive(Cand cand, int n, int S, const int32_t* __restrict__ ev, int q0,
-                             int32_t* __restrict__ out, int out_cap, int out_start) {
+// position: keeps those with lo < evict_at <= hi, calls emit(slot, pos, ev)
+// with slots counted from out_start (only below out_cap); returns the end.
+template <typename Cand, typename Emit>
+__device__ int compact_alive(Cand cand, int n, int S, const int32_t* __restrict__ ev, int lo, int hi,
+                             Emit emit, int out_cap, int out_start) {
   __shared__ int wtot[32];
   __shared__ int running;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -398,11 +399,14 @@ __device__ int compact_alive(Cand cand, int n, int S, const int32_t* __restrict_
   __syncthreads();
   for (int c0 = 0; c0 < n; c0 += blockDim.x) {
     int i = c0 + tid;
-    int pos = 0;
+    int pos = 0, e = 0;
     bool keep = false;
     if (i < n) {
       pos = cand(i);
-      keep = pos >= 0 && pos < S && ev[pos] > q0;
+      if (pos >= 0 && pos < S) {
+        e = ev[pos];
+        keep = e > lo && e <= hi;
+      }
     }
     uint32_t bal = __ballot_sync(0xffffffffu, keep);
     if (lane == 0) wtot[warp] = __popc(bal);
@@ -410,7 +414,7 @@ __device__ int compact_alive(Cand cand, int n, int S, const int32_t* __restrict_
     int before = running;
     for (int w2 = 0; w2 < warp; ++w2) before += wtot[w2];
     before += __popc(bal & ((1u << lane) - 1u));
-    if (keep && before < out_cap) out[before] = pos;
+    if (keep && before < out_cap) emit(before, pos, e);
     __syncthreads();
     if (tid == 0) {
       int tot = 0;
@@ -432,29 +436,36 @@ __global__ void __launch_bounds__(256)
   const int32_t* ev = evict_at + (size_t)seg * S;
   const int n = x0 >= s ? x0 - s + 1 : 0;
   int32_t* out = gbase + ((size_t)seg * ngroups + g) * k;
-  int cnt = compact_alive([=](int i) { return s + i; }, n, S, ev, q0, out, k, 0);
+  int cnt = compact_alive([=](int i) { return s + i; }, n, S, ev, q0, 0x7fffffff,
+                          [=](int slot, int pos, int) { out[slot] = pos; }, k, 0);
   if (threadIdx.x == 0) {
     gcount[(size_t)seg * ngroups + g] = cnt;
     if (cnt > k) report_error(status, KVPOP_ERR_INTERNAL, SITE_INTERNAL_CHECK, 1);
   }
 }
 
+// List j: keys of E(64 j) held at row 64 j as (position, evict_at) pairs --
+// first those held through row 64 j + 63, then those dropped inside the block,
+// each group in increasing position.
 __global__ void __launch_bounds__(256)
     lists_build(const int32_t* __restrict__ evict_at, int S, int s, int w, int k, int nL,
                 int ngroups, const int32_t* __restrict__ gbase, const int32_t* __restrict__ gcount,
-                int32_t* __restrict__ lists, int* status) {
+                int2* __restrict__ lists, int* status) {
   const int j = blockIdx.x, seg = blockIdx.y;
   const int g = j / kListGroup;
   const int q0 = j * KVPOP_LIST_QBLOCK, x0 = q0 - w;
+  const int q1 = q0 + KVPOP_LIST_QBLOCK - 1;
   const int qg = g * kListGroup * KVPOP_LIST_QBLOCK, xg = qg - w;
   const int32_t* ev = evict_at + (size_t)seg * S;
   const int32_t* gb = gbase + ((size_t)seg * ngroups + g) * k;
   const int nb = gcount[(size_t)seg * ngroups + g];
   const int r0 = max(s, xg + 1);
   const int nr = x0 >= r0 ? x0 - r0 + 1 : 0;
-  int32_t* out = lists + ((size_t)seg * nL + j) * k;
-  int cnt = compact_alive([=](int i) { return i < nb ? gb[i] : r0 + (i - nb); }, nb + nr, S, ev, q0,
-                          out, k, 0);
+  int2* out = lists + ((size_t)seg * nL + j) * k;
+  auto cand = [=](int i) { return i < nb ? gb[i] : r0 + (i - nb); };
+  auto emit = [=](int slot, int pos, int e) { out[slot] = make_int2(pos, e); };
+  const int na = compact_alive(cand, nb + nr, S, ev, q1, 0x7fffffff, emit, k, 0);
+  const int cnt = compact_alive(cand, nb + nr, S, ev, q0, q1, emit, k, na);
   if (threadIdx.x == 0) {
     const int expect = min(k, x0 >= s ? x0 - s + 1 : 0);
     if (cnt != expect) report_error(status, KVPOP_ERR_INTERNAL, SITE_INTERNAL_CHECK, 2);
@@ -545,7 +556,7 @@ extern "C" kvpop_status kvpop_mask_lists_size(int b, int H, int S, kvpop_budget 
   MaskPlan p;
   kvpop_status st = plan_mask(b, H, S, bud, &p);
   if (st != KVPOP_OK) return st;
-  *bytes = (size_t)p.nseg * p.nL * (size_t)bud.k * 4;
+  *bytes = (size_t)p.nseg * p.nL * (size_t)bud.k * 8;
   return KVPOP_OK;
 }
 
@@ -641,7 +652,8 @@ extern "C" kvpop_status kvpop_mask(const float* prio, int b, int H, int S, kvpop
     lists_group_base<<<dim3(p.ngroups, p.nseg), 256, 0, cs>>>(evict_at, S, bud.s, bud.w, bud.k,
                                                               p.ngroups, gbase, gcount, status);
     lists_build<<<dim3(p.nL, p.nseg), 256, 0, cs>>>(evict_at, S, bud.s, bud.w, bud.k, p.nL,
-                                                    p.ngroups, gbase, gcount, lists, status);
+                                                    p.ngroups, gbase, gcount,
+                                                    reinterpret_cast<int2*>(lists), status);
   }
   return cuda_check(cudaGetLastError(), "kvpop_mask: launch");
 }

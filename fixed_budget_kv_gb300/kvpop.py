@@ -147,7 +147,8 @@ def mask_lists_size(b, H, S, s, w, k) -> int:
 
 def mask(prio: torch.Tensor, s: int, w: int, k: int, lists: bool = True, workspace=None, out=None,
          stream=None):
-    """rank, tau, evict_at [b,H,S] int32 (and the long-range lists) for priorities [b,H,S] fp32."""
+    """rank, tau, evict_at [b,H,S] int32 and the long-range lists [b,H,ceil(S/64),k,2]
+    (position, evict_at) for priorities [b,H,S] fp32."""
     _need(prio, torch.float32, "prio")
     b, H, S = prio.shape
     lib = load()
@@ -157,7 +158,7 @@ def mask(prio: torch.Tensor, s: int, w: int, k: int, lists: bool = True, workspa
         tau = torch.empty_like(rank)
         ev = torch.empty_like(rank)
         nl = (S + LIST_QBLOCK - 1) // LIST_QBLOCK
-        lst = torch.empty((b, H, nl, max(k, 0)), dtype=torch.int32, device=dev) if (lists and k > 0) else None
+        lst = torch.empty((b, H, nl, max(k, 0), 2), dtype=torch.int32, device=dev) if (lists and k > 0) else None
     else:
         rank, tau, ev, lst = out
     if workspace is None:

@@ -93,11 +93,14 @@ kvpop_status kvpop_device_status(int32_t out[4], int reset);
  *               (S if never; S for sinks).  Row q retains t exactly when
  *               t <= q < evict_at[t], so the retained set of row q is
  *               {t <= q : q < evict_at[t]} and holds min(q+1, B) keys.
- *   lists       (nullable) [b, H, ceil(S/64), k] int32: list i holds the
- *               long-range keys retained at row 64*i, i.e.
- *               {t in E(64 i) : q < evict_at[t] for q = 64 i}, in increasing
- *               position; its length is min(k, max(0, 64 i - w - s + 1)) and
- *               the rest of the row is unspecified.  kvpop_attn_fwd reads it.
+ *   lists       (nullable) [b, H, ceil(S/64), k] pairs of int32
+ *               (position, evict_at): list i holds the long-range keys
+ *               retained at row 64*i, i.e. {t in E(64 i) : 64 i < evict_at[t]};
+ *               first those still retained at row 64 i + 63, then those
+ *               dropped inside rows 64 i .. 64 i + 63, each group in
+ *               increasing position.  Its length is
+ *               min(k, max(0, 64 i - w - s + 1)); the rest of the row is
+ *               unspecified.  kvpop_attn_fwd reads it.
  * prio [b, H, S] fp32.  workspace: device scratch of at least
  * kvpop_mask_workspace_size() bytes, 256-byte aligned.
  * Supported S: 1 .. 131072.  Errors: INVALID_ARG, UNSUPPORTED, CUDA.

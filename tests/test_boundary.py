@@ -28,9 +28,9 @@ def test_status_strings(lib):
 
 
 def test_sizes(lib):
-    # mask workspace and lists grow with the problem; lists are [b,H,ceil(S/64),k] int32
-    assert kvpop.mask_lists_size(1, 8, 16384, 16, 512, 1520) == 8 * 256 * 1520 * 4
-    assert kvpop.mask_lists_size(2, 1, 100, 0, 0, 3) == 2 * 2 * 3 * 4
+    # mask workspace and lists grow with the problem; lists are [b,H,ceil(S/64),k] int32 pairs
+    assert kvpop.mask_lists_size(1, 8, 16384, 16, 512, 1520) == 8 * 256 * 1520 * 8
+    assert kvpop.mask_lists_size(2, 1, 100, 0, 0, 3) == 2 * 2 * 3 * 8
     assert kvpop.mask_workspace_size(1, 1, 256, 4, 32, 32) > 0
     assert kvpop.target_workspace_size(1, 16384, 32, 8) == 16384 * 32 * 4
 

@@ -21,12 +21,15 @@ def _built():
 
 
 def expected_lists(ev, s, w, k, S):
-    """list i = sorted {t in [s, 64 i - w] : evict_at[t] > 64 i} (from the oracle's evict_at)."""
+    """list i = {t in [s, 64 i - w] : evict_at[t] > 64 i} (from the oracle's evict_at): first
+    the keys still held at row 64 i + 63, then those dropped inside the block, each sorted."""
     out = []
     for i in range((S + 63) // 64):
         q0 = 64 * i
         t = np.arange(s, max(s, q0 - w + 1))
-        out.append(t[ev[t] > q0])
+        held = t[ev[t] > q0]
+        order = np.concatenate([held[ev[held] > q0 + 63], held[ev[held] <= q0 + 63]])
+        out.append(np.stack([order, ev[order]], axis=1) if order.size else np.zeros((0, 2), np.int64))
     return out
 
 
@@ -46,8 +49,8 @@ def check(prio, s, w, k, lists=True, full_lists=True):
             for h in range(H) if full_lists else [0, H - 1]:
                 exp = expected_lists(eo[bi, h], s, w, k, S)
                 for i, e in enumerate(exp):
-                    assert e.size == min(k, max(0, 64 * i - w - s + 1))
-                    assert np.array_equal(lh[bi, h, i, :e.size], e), f"list {bi},{h},{i}"
+                    assert e.shape[0] == min(k, max(0, 64 * i - w - s + 1))
+                    assert np.array_equal(lh[bi, h, i, :e.shape[0]], e), f"list {bi},{h},{i}"
     return r, tau, ev
 
 
