@@ -11,8 +11,9 @@
 //               and, per 32-key chunk, the latest position and the earliest
 //               eviction row, so that rows inside that range skip masking
 //   warp 1      TMEM allocation and the single-thread tcgen05.mma issuer
-//   warps 2-3   sparse mode: K/V rows of sinks and long-range keys gathered
-//               with cp.async into the 128B-swizzled operand layout; the
+//   warps 2-3   sparse mode: K (warp 2) and V (warp 3) rows of sinks and
+//               long-range keys gathered by TMA (tile::gather4, four rows per
+//               instruction) into the 128B-swizzled operand layout; the
 //               contiguous span (window and recent tokens) by TMA tiles
 //   warps 4-7   softmax for query tile 0 (one thread per row / TMEM lane)
 //   warps 8-11  softmax for query tile 1
@@ -41,6 +42,7 @@ constexpr float kRescaleLog2 = 8.0f;
 
 struct AttnParams {
   CUtensorMap tq, tk, tv;
+  CUtensorMap tkr, tvr;  // K, V as [b*S*H rows, D] with one-row boxes (gather4)
   const __nv_bfloat16* k;
   const __nv_bfloat16* v;
   const int32_t* evict_at;
@@ -122,8 +124,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
     for (int i = 0; i < NS; ++i) {
-      mbar_init(&bars->k_full[i], SPARSE ? 64 : 1);
-      mbar_init(&bars->v_full[i], SPARSE ? 64 : 1);
+      mbar_init(&bars->k_full[i], 1);
+      mbar_init(&bars->v_full[i], 1);
       mbar_init(&bars->k_empty[i], 1);
       mbar_init(&bars->v_empty[i], 1);
     }
@@ -193,26 +195,38 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
       }
     } else {
       const int32_t* ev = p.evict_at + (size_t)(b * p.H + h) * S;
+      // lane owns entries lane + 32 c of a tile: chunk c has one entry per lane.
+      // The loads of tile j + 1 are issued before tile j is written out, so
+      // one L2 round trip per tile hides behind the previous tile.
+      auto load_tile = [&](int j, int2 (&e)[4]) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int r = lane + 32 * c;
+          e[c] = make_int2(0x7fffffff, 0);  // padding: never visible
+          if (j < NTg) {
+            const int i = j * kKeys + r;
+            if (i < n_sink) e[c] = make_int2(i, S);
+            else if (i < n_sl) e[c] = __ldg(list + (i - n_sink));
+          } else {
+            const int pos = sp0 + (j - NTg) * kKeys + r;
+            if (pos <= qb1) e[c] = make_int2(pos, __ldg(ev + pos));
+          }
+        }
+      };
+      int2 cur_e[4], nxt_e[4];
+      if (NT > 0) load_tile(0, cur_e);
       for (int j = 0; j < NT; ++j) {
         const int ms = j % kMetaStages;
+        if (j + 1 < NT) load_tile(j + 1, nxt_e);
         if (!warp_wait(&bars->meta_empty[ms], ((j / kMetaStages) & 1) ^ 1, abort_flag)) {
           if (lane == 0) fail(SITE_ATTN_PRODUCER, 3);
           break;
         }
         int2* m = meta + ms * (kKeys + 4);
-        // lane owns entries lane + 32 c: chunk c has one entry per lane
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const int r = lane + 32 * c;
-          int2 e = make_int2(0x7fffffff, 0);  // padding: never visible
-          if (j < NTg) {
-            const int i = j * kKeys + r;
-            if (i < n_sink) e = make_int2(i, S);
-            else if (i < n_sl) e = __ldg(list + (i - n_sink));
-          } else {
-            const int pos = sp0 + (j - NTg) * kKeys + r;
-            if (pos <= qb1) e = make_int2(pos, __ldg(ev + pos));
-          }
+          int2 e = cur_e[c];
           if (e.x != 0x7fffffff && (e.x < 0 || e.x >= S)) {  // a corrupt list entry: never gathered
             report_error(p.status, KVPOP_ERR_INTERNAL, SITE_INTERNAL_CHECK, 10);
             e = make_int2(0x7fffffff, 0);
@@ -228,6 +242,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->meta_full[ms]);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) cur_e[c] = nxt_e[c];
       }
     }
   } else if (warp == 1) {
@@ -253,7 +269,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
           fail(SITE_ATTN_MMA, detail);
           return false;
         }
-        if (SPARSE) fence_proxy_async_smem();  // cp.async rows -> tensor-core reads
         tc_fence_after();
         return true;
       };
@@ -472,85 +487,51 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
             l > 0.0f ? (m_ref * sl2 + __log2f(l)) * 0.69314718055994531f : neg_inf();
     }
   } else if (SPARSE) {
-    // ------------------------------------------------------------ K/V loaders (warps 2-3)
-    constexpr int CH = D / 8;  // 16-byte chunks per row
-    constexpr int RSTEP = 64 / CH;
-    const int gt = (warp - 2) * 32 + lane;
-    const int c = gt % CH, rg = gt / CH;
-    const int dh = c >> 3, cc = c & 7;
-    const size_t kv_stride = (size_t)p.H * D;
-    const __nv_bfloat16* kb = p.k + ((size_t)b * S * p.H + h) * D + c * 8;
-    const __nv_bfloat16* vb = p.v + ((size_t)b * S * p.H + h) * D + c * 8;
+    // ------------------------------------------------------------ loaders: warp 2 streams K, warp 3 V
+    // Each runs its own sequence of stages, so K tiles run ahead of the V tiles.
+    // Sinks and long-range keys: TMA gather4 (four scattered rows per
+    // instruction, lane l takes rows 4l..4l+3); the span: one tiled TMA box.
+    const bool is_v = warp == 3;
+    const CUtensorMap* rmap = is_v ? &p.tvr : &p.tkr;
+    const CUtensorMap* tmap = is_v ? &p.tv : &p.tk;
+    uint64_t* full = is_v ? bars->v_full : bars->k_full;
+    uint64_t* empty = is_v ? bars->v_empty : bars->k_empty;
+    const int off = is_v ? L::v_off : L::k_off;
+    const int row_base = b * S * p.H + h;  // row of position t is row_base + t * H
     for (int j = 0; j < NT; ++j) {
       const int st = j % NS;
       const uint32_t ph = (j / NS) & 1;
       const int ms = j % kMetaStages;
-      const bool gathered = j < NTg;
-      int pos[kKeys / RSTEP];
       if (!warp_wait(&bars->meta_full[ms], (j / kMetaStages) & 1, abort_flag)) {
         if (lane == 0) fail(SITE_ATTN_PRODUCER, 6);
         break;
       }
-      if (gathered) {
+      if (!warp_wait(&empty[st], ph ^ 1, abort_flag)) {
+        if (lane == 0) fail(SITE_ATTN_PRODUCER, 4);
+        break;
+      }
+      if (lane == 0) mbar_arrive_expect_tx(&full[st], DH * kBlockBytes);
+      __syncwarp();
+      if (j < NTg) {
         const int2* km = meta + ms * (kKeys + 4);
+        int rows[4];
 #pragma unroll
-        for (int i = 0; i < kKeys / RSTEP; ++i) pos[i] = km[rg + i * RSTEP].x;
+        for (int u = 0; u < 4; ++u) {
+          const int pos = km[4 * lane + u].x;
+          rows[u] = pos != 0x7fffffff ? row_base + pos * p.H : row_base;  // padding: any row, masked
+        }
+#pragma unroll
+        for (int d2 = 0; d2 < DH; ++d2)
+          tma_gather4(smem + off + (st * DH + d2) * kBlockBytes + lane * 512, rmap, &full[st], d2 * 64,
+                      rows[0], rows[1], rows[2], rows[3]);
+      } else if (lane == 0) {
+        const int span_row = sp0 + (j - NTg) * kKeys;
+        for (int d2 = 0; d2 < DH; ++d2)
+          tma_load_4d(smem + off + (st * DH + d2) * kBlockBytes, tmap, &full[st], d2 * 64, h, span_row, b);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->meta_empty[ms]);
-      if (!mbar_wait(&bars->k_empty[st], ph ^ 1, abort_flag)) {
-        fail(SITE_ATTN_PRODUCER, 4);
-        break;
-      }
-      const int span_row = sp0 + (j - NTg) * kKeys;
-      if (gathered) {
-        uint8_t* kdst = smem + L::k_off + (st * DH + dh) * kBlockBytes;
-#pragma unroll
-        for (int i = 0; i < kKeys / RSTEP; ++i) {
-          const int r = rg + i * RSTEP;
-          const bool valid = pos[i] != 0x7fffffff;
-          cp_async_16(kdst + sw128_offset(r, cc), valid ? (const void*)(kb + (size_t)pos[i] * kv_stride)
-                                                         : (const void*)p.k,
-                      valid ? 16u : 0u);
-        }
-        cp_async_arrive_noinc(&bars->k_full[st]);
-      } else {
-        if (gt == 0) {
-          mbar_arrive_expect_tx(&bars->k_full[st], DH * kBlockBytes);
-          for (int d2 = 0; d2 < DH; ++d2)
-            tma_load_4d(smem + L::k_off + (st * DH + d2) * kBlockBytes, &p.tk, &bars->k_full[st], d2 * 64,
-                        h, span_row, b);
-        } else {
-          mbar_arrive(&bars->k_full[st]);
-        }
-      }
-      if (!mbar_wait(&bars->v_empty[st], ph ^ 1, abort_flag)) {
-        fail(SITE_ATTN_PRODUCER, 5);
-        break;
-      }
-      if (gathered) {
-        uint8_t* vdst = smem + L::v_off + (st * DH + dh) * kBlockBytes;
-#pragma unroll
-        for (int i = 0; i < kKeys / RSTEP; ++i) {
-          const int r = rg + i * RSTEP;
-          const bool valid = pos[i] != 0x7fffffff;
-          cp_async_16(vdst + sw128_offset(r, cc), valid ? (const void*)(vb + (size_t)pos[i] * kv_stride)
-                                                         : (const void*)p.v,
-                      valid ? 16u : 0u);
-        }
-        cp_async_arrive_noinc(&bars->v_full[st]);
-      } else {
-        if (gt == 0) {
-          mbar_arrive_expect_tx(&bars->v_full[st], DH * kBlockBytes);
-          for (int d2 = 0; d2 < DH; ++d2)
-            tma_load_4d(smem + L::v_off + (st * DH + d2) * kBlockBytes, &p.tv, &bars->v_full[st], d2 * 64,
-                        h, span_row, b);
-        } else {
-          mbar_arrive(&bars->v_full[st]);
-        }
-      }
     }
-    cp_async_wait_all();
   }
 
   // ------------------------------------------------------------ teardown
@@ -639,7 +620,9 @@ extern "C" kvpop_status kvpop_attn_fwd(const void* q, const void* k, const void*
     uint64_t sk[3] = {(uint64_t)D * 2, (uint64_t)H * D * 2, (uint64_t)S * H * D * 2};
     uint32_t bk[4] = {64, 1, 128, 1};
     if (!make_tmap_4d(&prm.tq, q, dq, sq, bq) || !make_tmap_4d(&prm.tk, k, dk, sk, bk) ||
-        !make_tmap_4d(&prm.tv, v, dk, sk, bk))
+        !make_tmap_4d(&prm.tv, v, dk, sk, bk) ||
+        !make_tmap_rows(&prm.tkr, k, (uint64_t)D, (uint64_t)b * S * H, 64) ||
+        !make_tmap_rows(&prm.tvr, v, (uint64_t)D, (uint64_t)b * S * H, 64))
       return KVPOP_ERR_CUDA;
   }
   prm.k = static_cast<const __nv_bfloat16*>(k);

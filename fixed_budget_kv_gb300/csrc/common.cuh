@@ -137,6 +137,18 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// Four rows (r0..r3, each one box of a 2-D tensor map whose box is one row
+// high) gathered into four consecutive 128-byte rows of shared memory.
+__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, uint64_t* bar, int x,
+                                            int r0, int r1, int r2, int r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(r0), "r"(r1), "r"(r2),
+      "r"(r3)
+      : "memory");
+}
+
 // 1-D bulk copy global -> shared (16-byte aligned, size a multiple of 16).
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(
@@ -396,6 +408,9 @@ namespace kvpop {
 // cuTensorMapEncodeTiled fetched through the runtime (no direct libcuda link).
 bool make_tmap_4d(CUtensorMap* map, const void* base, const uint64_t dims[4],
                   const uint64_t strides_bytes[3], const uint32_t box[4]);
+// 2-D bf16 map with a one-row box of `box_cols` elements, 128-byte swizzle (for gather4).
+bool make_tmap_rows(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
+                    uint32_t box_cols);
 
 int current_device();
 int num_sms();

@@ -94,6 +94,27 @@ bool make_tmap_4d(CUtensorMap* map, const void* base, const uint64_t dims[4],
   return true;
 }
 
+bool make_tmap_rows(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
+                    uint32_t box_cols) {
+  auto fn = get_encode_fn();
+  if (!fn) {
+    set_last_error("cuTensorMapEncodeTiled is not available");
+    return false;
+  }
+  cuuint64_t gdim[2] = {cols, rows};
+  cuuint64_t gstride[1] = {cols * 2};
+  cuuint32_t bdim[2] = {box_cols, 1};
+  cuuint32_t estride[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, bdim,
+                  estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_last_error("cuTensorMapEncodeTiled (rows) failed (%d)", (int)r);
+    return false;
+  }
+  return true;
+}
+
 }  // namespace kvpop
 
 extern "C" {
