@@ -32,7 +32,7 @@ sys.path.insert(0, ROOT)
 METRIC = "prefill tokens/s (sparse attn + future target) & decode tokens/s; % of roofline"
 LAUNCHES_MASK = 4 * 3 + 1 + 1 + 1 + 2   # radix passes, wavelet, tau, evict_at, lists
 LAUNCHES_STEP = LAUNCHES_MASK + 1 + 1 + 3  # + sparse attention, dense LSE, target (prep, kernel, log)
-LAUNCHES_DECODE_STEP = 3
+LAUNCHES_DECODE_STEP = 2
 
 
 def parse():

@@ -11,7 +11,8 @@
 //   2. split attention (flash-decoding): each CTA reads a contiguous range of
 //      slots once -- K for the G query heads' scores, then V -- with 16-byte
 //      coalesced loads; HBM-bound at 4 flop/byte;
-//   3. combine the splits' (max, sum, partial O) into O and the LSE.
+//   3. the last split CTA of each (sequence, head) combines the splits' (max,
+//      sum, partial O) into O and the LSE.
 #include "common.cuh"
 
 struct kvpop_cache {
@@ -24,6 +25,8 @@ struct kvpop_cache {
   int32_t* slot_pos;  // [n, H, B]
   float* slot_prio;   // [n, H, B]
   int32_t* topk_cnt;  // [n, H]
+  int32_t* done_cnt;  // [n, H] split CTAs finished in this step (reset by the last one)
+  int* status;        // device status words
   float* part_ml;     // [n, Hq, nsplit, 2]  (max in log2 units, sum)
   float* part_o;      // [n, Hq, nsplit, D]
 };
@@ -31,9 +34,11 @@ struct kvpop_cache {
 namespace kvpop {
 namespace {
 
-constexpr int kSplit = 256;
+constexpr int kSplit = 512;  // slots per attention CTA
 constexpr int kUpdThreads = 256;
-constexpr int kAttnThreads = 128;
+constexpr int kAttnThreads = 160;  // 4 compute warps + 1 producer warp
+
+__device__ __forceinline__ int* device_status_from(const kvpop_cache& c) { return c.status; }
 
 __device__ __forceinline__ float prio_val(float p) { return p != p ? __int_as_float(0xff800000) : p; }
 
@@ -103,14 +108,23 @@ __global__ void __launch_bounds__(kUpdThreads)
       // worst held long-range token
       float bv = __int_as_float(0x7f800000);
       int bp = -1, bs = -1;
-      for (int i = tid; i < k; i += kUpdThreads) {
-        const int sl = s + w + i;
-        const float v = prio_val(sprio[sl]);
-        const int ps = spos[sl];
-        if (bs < 0 || worse(v, ps, bv, bp)) {
-          bv = v;
-          bp = ps;
-          bs = sl;
+      for (int i0 = tid; i0 < k; i0 += kUpdThreads * 8) {
+        float vv[8];
+        int pp[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {  // all loads of the batch in flight together
+          const int i = i0 + u * kUpdThreads;
+          vv[u] = i < k ? prio_val(sprio[s + w + i]) : 0.0f;
+          pp[u] = i < k ? spos[s + w + i] : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int i = i0 + u * kUpdThreads;
+          if (i < k && (bs < 0 || worse(vv[u], pp[u], bv, bp))) {
+            bv = vv[u];
+            bp = pp[u];
+            bs = s + w + i;
+          }
         }
       }
       for (int o = 16; o > 0; o >>= 1) {
@@ -172,148 +186,269 @@ __global__ void __launch_bounds__(kUpdThreads)
   if (tid == 0 && evicted_pos) evicted_pos[nh] = s_evicted;
 }
 
-// One CTA per (split, KV head, sequence).  D / 8 lanes cover one slot row with
-// 16-byte loads; G query heads share every row.
+// One CTA per (split of kSplit slots, KV head, sequence), 5 warps.  Warp 4
+// streams the split's K rows and then its V rows (contiguous kSplit x D bf16
+// blocks) through a kStages-deep ring of 8 KB chunks in shared memory
+// with bulk TMA copies, so every CTA keeps kStages chunks of HBM reads in
+// flight from start to end.  Warps 0-3 turn K chunks into scores (D / 8 lanes
+// per slot row, G query heads per row, packed f32x2 FMAs), take the softmax
+// over the whole split, then accumulate P.V from the V chunks.  Empty slots
+// hold finite data (zeros or stale rows) and get weight 0.  The last CTA of a
+// (sequence, head) to finish merges the splits' (max, sum, partial O).
+constexpr int kChunkBytes = 8192;  // one ring chunk: 8 KB of slot rows
+constexpr int kStages = 6;         // ring depth
+constexpr int kCompute = 128; // compute threads (warps 0-3)
+
 template <int D, int G>
 __global__ void __launch_bounds__(kAttnThreads)
-    decode_attn(kvpop_cache c, const __nv_bfloat16* __restrict__ q_new, float scale_log2) {
+    decode_attn(kvpop_cache c, const __nv_bfloat16* __restrict__ q_new, float scale_log2,
+                __nv_bfloat16* __restrict__ O, float* __restrict__ lse) {
   constexpr int LPR = D / 8;                 // lanes per row
-  constexpr int RPW = 32 / LPR;              // rows per warp step
-  constexpr int NW = kAttnThreads / 32;
-  __shared__ float sc[G][kSplit];
+  constexpr int RPW = 32 / LPR;              // rows per warp instruction
+  constexpr int NW = kCompute / 32;
+  constexpr int NG = kCompute / LPR;         // row groups for P.V
+  constexpr int kChunk = kChunkBytes / (D * 2);  // slot rows per ring chunk
+  constexpr int CB = kChunkBytes;
+  static_assert(NG * G * D * 4 <= kStages * CB, "partial O must fit in the ring");
+  extern __shared__ __align__(128) uint8_t dsm[];  // ring: kStages x CB bytes
+  float* opart = reinterpret_cast<float*>(dsm);    // [NG][G][D], reuses the ring at the end
+  __shared__ __align__(16) float sct[kSplit * G];  // scores, then weights: [slot][head]
   __shared__ float red[G][NW];
   __shared__ float m_s[G], l_s[G];
-  __shared__ float opart[kAttnThreads / LPR][G][D];
+  __shared__ int s_last;
+  __shared__ __align__(8) uint64_t full[kStages], empty[kStages];
+  __shared__ volatile int abort_flag;
   const int sp = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int H = c.H, B = c.B;
   const int nh = n * H + h;
   const int slot_lo = sp * c.split_len;
-  const int slot_hi = min(B, slot_lo + c.split_len);
-  const int nslots = slot_hi - slot_lo;
-  const __nv_bfloat16* kc = c.kc + ((size_t)nh * B) * D;
-  const __nv_bfloat16* vc = c.vc + ((size_t)nh * B) * D;
-  const int32_t* spos = c.slot_pos + (size_t)nh * B;
-  const int sub = lane / LPR, li = lane % LPR;
-
-  // query chunk of this lane for each head
-  float qf[G][8];
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    const uint4 raw = *reinterpret_cast<const uint4*>(q_new + ((size_t)n * H * G + h * G + g) * D + li * 8);
-    const __nv_bfloat162* pr = reinterpret_cast<const __nv_bfloat162*>(&raw);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 f = __bfloat1622float2(pr[e]);
-      qf[g][2 * e] = f.x * scale_log2;
-      qf[g][2 * e + 1] = f.y * scale_log2;
+  const int nslots = min(B, slot_lo + c.split_len) - slot_lo;
+  const int nch = (nslots + kChunk - 1) / kChunk;  // chunks of K, then as many of V
+  if (tid == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], NW);
     }
+    abort_flag = 0;
+    fence_mbar_init();
   }
-  // phase 1: scores (log2 units)
-  for (int r0 = warp * RPW; r0 < nslots; r0 += NW * RPW) {
-    const int r = r0 + sub;
-    const bool valid = r < nslots && spos[slot_lo + r] >= 0;
-    float part[G];
+  __syncthreads();
+  bool ok = true;
+  if (warp == NW) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      const __nv_bfloat16* kb = c.kc + ((size_t)nh * B + slot_lo) * D;
+      const __nv_bfloat16* vb = c.vc + ((size_t)nh * B + slot_lo) * D;
+      for (int i = 0; i < 2 * nch; ++i) {
+        const int st = i % kStages;
+        if (!mbar_wait(&empty[st], ((i / kStages) & 1) ^ 1, &abort_flag)) {
+          ok = false;
+          abort_flag = 1;
+          break;
+        }
+        const int ci = i < nch ? i : i - nch;
+        const int rows = min(kChunk, nslots - ci * kChunk);
+        const uint32_t bytes = (uint32_t)rows * D * 2;
+        mbar_arrive_expect_tx(&full[st], bytes);
+        bulk_load(dsm + st * CB, (i < nch ? kb : vb) + (size_t)ci * kChunk * D, bytes, &full[st]);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- compute
+    const int sub = lane / LPR, li = lane % LPR;
+    const int32_t* spos = c.slot_pos + (size_t)nh * B + slot_lo;
+    uint64_t qp[G][4];  // this lane's query chunk per head, log2 units, as pairs
 #pragma unroll
-    for (int g = 0; g < G; ++g) part[g] = 0.f;
-    if (valid) {
-      const uint4 raw = *reinterpret_cast<const uint4*>(kc + (size_t)(slot_lo + r) * D + li * 8);
+    for (int g = 0; g < G; ++g) {
+      const uint4 raw = *reinterpret_cast<const uint4*>(q_new + ((size_t)n * H * G + h * G + g) * D + li * 8);
       const __nv_bfloat162* pr = reinterpret_cast<const __nv_bfloat162*>(&raw);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const float2 f = __bfloat1622float2(pr[e]);
-#pragma unroll
-        for (int g = 0; g < G; ++g) part[g] = fmaf(f.x, qf[g][2 * e], fmaf(f.y, qf[g][2 * e + 1], part[g]));
+        qp[g][e] = pack2(f.x * scale_log2, f.y * scale_log2);
       }
     }
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-#pragma unroll
-      for (int o = LPR / 2; o > 0; o >>= 1) part[g] += __shfl_xor_sync(0xffffffffu, part[g], o);
-    }
-    if (li == 0 && r < nslots) {
-#pragma unroll
-      for (int g = 0; g < G; ++g) sc[g][r] = valid ? part[g] : __int_as_float(0xff800000);
-    }
-  }
-  __syncthreads();
-  // phase 2: per-head max and sum
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    float m = __int_as_float(0xff800000);
-    for (int r = tid; r < nslots; r += kAttnThreads) m = fmaxf(m, sc[g][r]);
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (lane == 0) red[g][warp] = m;
-  }
-  __syncthreads();
-  if (tid < G) {
-    float m = red[tid][0];
-    for (int i = 1; i < NW; ++i) m = fmaxf(m, red[tid][i]);
-    m_s[tid] = m;
-  }
-  __syncthreads();
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    const float m = m_s[g];
-    float l = 0.f;
-    if (m != __int_as_float(0xff800000)) {
-      for (int r = tid; r < nslots; r += kAttnThreads) {
-        const float e = ex2_approx(sc[g][r] - m);
-        sc[g][r] = e;
-        l += e;
+    // phase 1: scores of every slot of the split (warp-uniform loops: the
+    // shuffles need all lanes; rows past the split compute on zeros)
+    for (int ci = 0; ci < nch; ++ci) {
+      const int st = ci % kStages;
+      if (ok && !mbar_wait(&full[st], (ci / kStages) & 1, &abort_flag)) {
+        ok = false;
+        abort_flag = 1;
       }
-    } else {
-      for (int r = tid; r < nslots; r += kAttnThreads) sc[g][r] = 0.f;
+      const __nv_bfloat16* kcs = reinterpret_cast<const __nv_bfloat16*>(dsm + st * CB);
+      constexpr int RW = kChunk / NW;  // rows per warp per chunk
+      uint4 raw[RW / RPW];
+#pragma unroll
+      for (int u = 0; u < RW / RPW; ++u) {
+        const int rl = warp * RW + u * RPW + sub;
+        raw[u] = ci * kChunk + rl < nslots ? *reinterpret_cast<const uint4*>(kcs + (size_t)rl * D + li * 8)
+                                           : make_uint4(0, 0, 0, 0);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);  // the chunk is in registers
+#pragma unroll
+      for (int u = 0; u < RW / RPW; ++u) {
+        const int r = ci * kChunk + warp * RW + u * RPW + sub;
+        const __nv_bfloat162* pr = reinterpret_cast<const __nv_bfloat162*>(&raw[u]);
+        uint64_t part[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) part[g] = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __bfloat1622float2(pr[e]);
+          const uint64_t kp = pack2(f.x, f.y);
+#pragma unroll
+          for (int g = 0; g < G; ++g) part[g] = fma2(kp, qp[g][e], part[g]);
+        }
+        // transposed butterfly over the LPR lanes of a row: each halving step
+        // sends half of the remaining heads to the partner and keeps the other
+        // half, so the lane ends with the full sum of one head
+        float v[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          float a, b2;
+          unpack2(part[g], a, b2);
+          v[g] = a + b2;
+        }
+        int head = 0;
+#pragma unroll
+        for (int lev = 0, o = LPR / 2; (G >> lev) > 1; ++lev, o >>= 1) {
+          const int half = (G >> lev) / 2;
+          const bool up = (li & o) != 0;
+#pragma unroll
+          for (int i = 0; i < half; ++i) {
+            const float send = up ? v[i] : v[i + half];
+            const float keep = up ? v[i + half] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+          }
+          if (up) head += half;
+        }
+#pragma unroll
+        for (int o = LPR / (2 * G); o > 0; o >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+        if ((li & (LPR / G - 1)) == 0 && r < nslots) sct[r * G + head] = v[0];
+      }
     }
-    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-    if (lane == 0) red[g][warp] = l;
-  }
-  __syncthreads();
-  if (tid < G) {
-    float l = 0.f;
-    for (int i = 0; i < NW; ++i) l += red[tid][i];
-    l_s[tid] = l;
-  }
-  // phase 3: partial O = sum_r p_r v_r
-  float acc[G][8];
+    named_barrier_sync(1, kCompute);
+    // phase 2: per-head max and sum over the split (empty slots get weight 0);
+    // scores become weights.  Thread t owns slots t + 128 j.
+    constexpr int kPer = kSplit / kCompute;
+    bool occ[kPer];
 #pragma unroll
-  for (int g = 0; g < G; ++g)
-#pragma unroll
-    for (int e = 0; e < 8; ++e) acc[g][e] = 0.f;
-  const int grp = tid / LPR;                 // row group of this thread
-  constexpr int NG = kAttnThreads / LPR;
-  for (int r = grp; r < nslots; r += NG) {
-    float pr_[G];
-    bool any = false;
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      pr_[g] = sc[g][r];
-      any |= pr_[g] != 0.f;
+    for (int j = 0; j < kPer; ++j) {
+      const int r = tid + j * kCompute;
+      occ[j] = r < nslots && spos[r] >= 0;
     }
-    if (!any) continue;
-    const uint4 raw = *reinterpret_cast<const uint4*>(vc + (size_t)(slot_lo + r) * D + li * 8);
-    const __nv_bfloat162* pv = reinterpret_cast<const __nv_bfloat162*>(&raw);
+    {
+      float m[G];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 f = __bfloat1622float2(pv[e]);
+      for (int g = 0; g < G; ++g) m[g] = __int_as_float(0xff800000);
+#pragma unroll
+      for (int j = 0; j < kPer; ++j)
+        if (occ[j]) {
+#pragma unroll
+          for (int g = 0; g < G; ++g) m[g] = fmaxf(m[g], sct[(tid + j * kCompute) * G + g]);
+        }
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        acc[g][2 * e] = fmaf(pr_[g], f.x, acc[g][2 * e]);
-        acc[g][2 * e + 1] = fmaf(pr_[g], f.y, acc[g][2 * e + 1]);
+        for (int o = 16; o > 0; o >>= 1) m[g] = fmaxf(m[g], __shfl_xor_sync(0xffffffffu, m[g], o));
+        if (lane == 0) red[g][warp] = m[g];
       }
     }
+    named_barrier_sync(1, kCompute);
+    if (tid < G) {
+      float m = red[tid][0];
+      for (int i = 1; i < NW; ++i) m = fmaxf(m, red[tid][i]);
+      m_s[tid] = m;
+    }
+    named_barrier_sync(1, kCompute);
+    {
+      float l[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) l[g] = 0.f;
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        const int r = tid + j * kCompute;
+        if (r >= nslots) break;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float m = m_s[g];
+          const float e = (occ[j] && m != __int_as_float(0xff800000)) ? ex2_approx(sct[r * G + g] - m) : 0.f;
+          sct[r * G + g] = e;
+          l[g] += e;
+        }
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        for (int o = 16; o > 0; o >>= 1) l[g] += __shfl_xor_sync(0xffffffffu, l[g], o);
+        if (lane == 0) red[g][warp] = l[g];
+      }
+    }
+    named_barrier_sync(1, kCompute);
+    if (tid < G) {
+      float l = 0.f;
+      for (int i = 0; i < NW; ++i) l += red[tid][i];
+      l_s[tid] = l;
+    }
+    // phase 3: partial O = sum_r p_r v_r
+    uint64_t acc[G][4];
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[g][e] = 0;
+    const int grp = tid / LPR;
+    for (int ci = 0; ci < nch; ++ci) {
+      const int i = nch + ci;
+      const int st = i % kStages;
+      if (ok && !mbar_wait(&full[st], (i / kStages) & 1, &abort_flag)) {
+        ok = false;
+        abort_flag = 1;
+      }
+      const __nv_bfloat16* vcs = reinterpret_cast<const __nv_bfloat16*>(dsm + st * CB);
+#pragma unroll
+      for (int u = 0; u < kChunk / NG; ++u) {
+        const int rl = grp + u * NG;
+        const int r = ci * kChunk + rl;
+        if (r >= nslots) break;
+        const uint4 raw = *reinterpret_cast<const uint4*>(vcs + (size_t)rl * D + li * 8);
+        const __nv_bfloat162* pv = reinterpret_cast<const __nv_bfloat162*>(&raw);
+        uint64_t wp[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float w = sct[r * G + g];
+          wp[g] = pack2(w, w);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __bfloat1622float2(pv[e]);
+          const uint64_t vp = pack2(f.x, f.y);
+#pragma unroll
+          for (int g = 0; g < G; ++g) acc[g][e] = fma2(vp, wp[g], acc[g][e]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
+    }
+    named_barrier_sync(1, kCompute);  // every chunk consumed: the ring becomes opart
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float a, b2;
+        unpack2(acc[g][e], a, b2);
+        opart[(grp * G + g) * D + li * 8 + 2 * e] = a;
+        opart[(grp * G + g) * D + li * 8 + 2 * e + 1] = b2;
+      }
   }
-#pragma unroll
-  for (int g = 0; g < G; ++g)
-#pragma unroll
-    for (int e = 0; e < 8; ++e) opart[grp][g][li * 8 + e] = acc[g][e];
   __syncthreads();
+  if (!ok) report_error(device_status_from(c), KVPOP_ERR_TIMEOUT, SITE_DECODE, 1);
   const int Hq = H * G;
   for (int i = tid; i < G * D; i += kAttnThreads) {
     const int g = i / D, d = i % D;
     float o = 0.f;
 #pragma unroll
-    for (int r = 0; r < NG; ++r) o += opart[r][g][d];
+    for (int r = 0; r < NG; ++r) o += opart[(r * G + g) * D + d];
     c.part_o[(((size_t)n * Hq + h * G + g) * c.nsplit + sp) * D + d] = o;
   }
   if (tid < G) {
@@ -321,27 +456,48 @@ __global__ void __launch_bounds__(kAttnThreads)
     ml[0] = m_s[tid];
     ml[1] = l_s[tid];
   }
-}
-
-__global__ void decode_combine(kvpop_cache c, __nv_bfloat16* __restrict__ O, float* __restrict__ lse) {
-  const int row = blockIdx.x;  // n * Hq + j
-  const int D = c.D, ns = c.nsplit;
-  const float* ml = c.part_ml + (size_t)row * ns * 2;
-  float M = __int_as_float(0xff800000);
-  for (int i = 0; i < ns; ++i) M = fmaxf(M, ml[2 * i]);
-  float Lsum = 0.f;
-  for (int i = 0; i < ns; ++i)
-    if (ml[2 * i] != __int_as_float(0xff800000)) Lsum += ml[2 * i + 1] * ex2_approx(ml[2 * i] - M);
-  const float inv = Lsum > 0.f ? 1.0f / Lsum : 0.f;
-  for (int d = threadIdx.x; d < D; d += blockDim.x) {
-    float o = 0.f;
-    for (int i = 0; i < ns; ++i)
-      if (ml[2 * i] != __int_as_float(0xff800000))
-        o += c.part_o[((size_t)row * ns + i) * D + d] * ex2_approx(ml[2 * i] - M);
-    O[(size_t)row * D + d] = __float2bfloat16_rn(o * inv);
+  // the last split CTA of this (sequence, head) merges all splits
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const int prev = atomicAdd(c.done_cnt + nh, 1);
+    s_last = prev == c.nsplit - 1;
   }
-  if (threadIdx.x == 0)
-    lse[row] = Lsum > 0.f ? (M + __log2f(Lsum)) * 0.69314718055994531f : __int_as_float(0xff800000);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  // merge: split weights per head in shared memory, then every output element
+  // issues its nsplit partial loads together
+  const int ns = c.nsplit;
+  float* wgt = sct;  // [G][ns] weight of each split, reuses the score buffer
+  __shared__ float inv_s[G], lse_s[G];
+  const size_t row0 = (size_t)n * Hq + h * G;
+  for (int i = tid; i < G * ns; i += kAttnThreads) wgt[i] = __ldcg(c.part_ml + (row0 * ns + i) * 2);
+  __syncthreads();
+  if (tid < G) {
+    float M = __int_as_float(0xff800000);
+    for (int i = 0; i < ns; ++i) M = fmaxf(M, wgt[tid * ns + i]);
+    float Lsum = 0.f;
+    for (int i = 0; i < ns; ++i) {
+      const float mi = wgt[tid * ns + i];
+      const float wi = mi != __int_as_float(0xff800000) ? ex2_approx(mi - M) : 0.f;
+      Lsum += __ldcg(c.part_ml + ((row0 + tid) * ns + i) * 2 + 1) * wi;
+      wgt[tid * ns + i] = wi;
+    }
+    inv_s[tid] = Lsum > 0.f ? 1.0f / Lsum : 0.f;
+    lse_s[tid] = Lsum > 0.f ? (M + __log2f(Lsum)) * 0.69314718055994531f : __int_as_float(0xff800000);
+  }
+  __syncthreads();
+  for (int i = tid; i < G * D; i += kAttnThreads) {
+    const int g = i / D, d = i % D;
+    const float* po = c.part_o + ((row0 + g) * ns) * D + d;
+    float o = 0.f;
+#pragma unroll 8
+    for (int sidx = 0; sidx < ns; ++sidx) o += __ldcg(po + (size_t)sidx * D) * wgt[g * ns + sidx];
+    O[(row0 + g) * D + d] = __float2bfloat16_rn(o * inv_s[g]);
+  }
+  if (tid < G) lse[row0 + tid] = lse_s[tid];
+  if (tid == 0) c.done_cnt[nh] = 0;  // ready for the next step
 }
 
 // Prefill: the retained set of row P-1 from evict_at over the prefix.
@@ -414,19 +570,31 @@ __global__ void __launch_bounds__(256)
   if (tid == 0) c.topk_cnt[nh] = min(running, c.k);
 }
 
-template <int D>
-kvpop_status launch_attn(const kvpop_cache& c, const void* q_new, float sl2, cudaStream_t cs) {
+template <int D, int G>
+kvpop_status launch_attn_g(const kvpop_cache& c, const void* q_new, float sl2, void* O, float* lse,
+                           cudaStream_t cs) {
+  auto kern = decode_attn<D, G>;
+  const int smem = kStages * kChunkBytes;
+  kvpop_status st = cuda_check(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem),
+                               "kvpop_decode_step: smem attribute");
+  if (st != KVPOP_OK) return st;
   dim3 grid(c.nsplit, c.H, c.n);
+  kern<<<grid, kAttnThreads, smem, cs>>>(c, (const __nv_bfloat16*)q_new, sl2, (__nv_bfloat16*)O, lse);
+  return cuda_check(cudaGetLastError(), "kvpop_decode_step: attention launch");
+}
+
+template <int D>
+kvpop_status launch_attn(const kvpop_cache& c, const void* q_new, float sl2, void* O, float* lse,
+                         cudaStream_t cs) {
   switch (c.G) {
-    case 1: decode_attn<D, 1><<<grid, kAttnThreads, 0, cs>>>(c, (const __nv_bfloat16*)q_new, sl2); break;
-    case 2: decode_attn<D, 2><<<grid, kAttnThreads, 0, cs>>>(c, (const __nv_bfloat16*)q_new, sl2); break;
-    case 4: decode_attn<D, 4><<<grid, kAttnThreads, 0, cs>>>(c, (const __nv_bfloat16*)q_new, sl2); break;
-    case 8: decode_attn<D, 8><<<grid, kAttnThreads, 0, cs>>>(c, (const __nv_bfloat16*)q_new, sl2); break;
+    case 1: return launch_attn_g<D, 1>(c, q_new, sl2, O, lse, cs);
+    case 2: return launch_attn_g<D, 2>(c, q_new, sl2, O, lse, cs);
+    case 4: return launch_attn_g<D, 4>(c, q_new, sl2, O, lse, cs);
+    case 8: return launch_attn_g<D, 8>(c, q_new, sl2, O, lse, cs);
     default:
       set_last_error("kvpop_decode_step: G=%d unsupported (1, 2, 4 or 8)", c.G);
       return KVPOP_ERR_UNSUPPORTED;
   }
-  return cuda_check(cudaGetLastError(), "kvpop_decode_step: attention launch");
 }
 
 }  // namespace
@@ -441,7 +609,7 @@ extern "C" kvpop_status kvpop_cache_create(int n, int H, int G, int D, kvpop_bud
     return KVPOP_ERR_INVALID_ARG;
   }
   if (bud.s < 0 || bud.w < 0 || bud.k < 0 || (long long)bud.s + bud.w + bud.k < 1 ||
-      (long long)bud.s + bud.w + bud.k > (1 << 24)) {
+      (long long)bud.s + bud.w + bud.k > (long long)kSplit * kSplit) {  // the merge holds kSplit splits
     set_last_error("kvpop_cache_create: invalid budget");
     return KVPOP_ERR_INVALID_ARG;
   }
@@ -470,6 +638,7 @@ extern "C" kvpop_status kvpop_cache_create(int n, int H, int G, int D, kvpop_bud
   c->split_len = kSplit;
   c->nsplit = (c->B + kSplit - 1) / kSplit;
   c->device = current_device();
+  c->status = device_status_ptr();
   const size_t slots = (size_t)n * H * c->B;
   const size_t Hq = (size_t)H * G;
   kvpop_status st = KVPOP_OK;
@@ -481,10 +650,12 @@ extern "C" kvpop_status kvpop_cache_create(int n, int H, int G, int D, kvpop_bud
   alloc((void**)&c->slot_pos, slots * 4, "kvpop_cache_create: slot_pos");
   alloc((void**)&c->slot_prio, slots * 4, "kvpop_cache_create: slot_prio");
   alloc((void**)&c->topk_cnt, (size_t)n * H * 4, "kvpop_cache_create: count");
+  alloc((void**)&c->done_cnt, (size_t)n * H * 4, "kvpop_cache_create: split counters");
   alloc((void**)&c->part_ml, (size_t)n * Hq * c->nsplit * 2 * 4, "kvpop_cache_create: partials");
   alloc((void**)&c->part_o, (size_t)n * Hq * c->nsplit * D * 4, "kvpop_cache_create: partials");
   if (st == KVPOP_OK) st = cuda_check(cudaMemset(c->slot_pos, 0xff, slots * 4), "kvpop_cache_create: init");
   if (st == KVPOP_OK) st = cuda_check(cudaMemset(c->topk_cnt, 0, (size_t)n * H * 4), "kvpop_cache_create: init");
+  if (st == KVPOP_OK) st = cuda_check(cudaMemset(c->done_cnt, 0, (size_t)n * H * 4), "kvpop_cache_create: init");
   if (st == KVPOP_OK) st = cuda_check(cudaMemset(c->kc, 0, slots * D * 2), "kvpop_cache_create: init");
   if (st == KVPOP_OK) st = cuda_check(cudaMemset(c->vc, 0, slots * D * 2), "kvpop_cache_create: init");
   if (st != KVPOP_OK) {
@@ -502,6 +673,7 @@ extern "C" kvpop_status kvpop_cache_destroy(kvpop_cache* c) {
   cudaFree(c->slot_pos);
   cudaFree(c->slot_prio);
   cudaFree(c->topk_cnt);
+  cudaFree(c->done_cnt);
   cudaFree(c->part_ml);
   cudaFree(c->part_o);
   delete c;
@@ -555,10 +727,7 @@ extern "C" kvpop_status kvpop_decode_step(kvpop_cache* c, const void* q_new, con
   kvpop_status st = cuda_check(cudaGetLastError(), "kvpop_decode_step: update launch");
   if (st != KVPOP_OK) return st;
   const float sl2 = 1.4426950408889634f / sqrtf((float)c->D);
-  st = c->D == 128 ? launch_attn<128>(*c, q_new, sl2, cs) : launch_attn<64>(*c, q_new, sl2, cs);
-  if (st != KVPOP_OK) return st;
-  decode_combine<<<c->n * c->H * c->G, 128, 0, cs>>>(*c, (__nv_bfloat16*)O, lse);
-  st = cuda_check(cudaGetLastError(), "kvpop_decode_step: combine launch");
+  st = c->D == 128 ? launch_attn<128>(*c, q_new, sl2, O, lse, cs) : launch_attn<64>(*c, q_new, sl2, O, lse, cs);
   if (st == KVPOP_OK) c->q_next = q + 1;
   return st;
 }
