@@ -9,8 +9,9 @@
 //      (lowest priority, later position on ties) when its priority is strictly
 //      greater, or is dropped; then token q is written into the ring;
 //   2. split attention (flash-decoding): each CTA reads a contiguous range of
-//      slots once -- K for the G query heads' scores, then V -- with 16-byte
-//      coalesced loads; HBM-bound at 4 flop/byte;
+//      slots once -- K for the G query heads' scores, then V -- through a TMA
+//      ring; the two small GEMMs run on warp-level tensor-core MMAs; HBM-bound
+//      at 2G flop/byte;
 //   3. the last split CTA of each (sequence, head) combines the splits' (max,
 //      sum, partial O) into O and the LSE.
 #include "common.cuh"
@@ -29,6 +30,9 @@ struct kvpop_cache {
   int* status;        // device status words
   float* part_ml;     // [n, Hq, nsplit, 2]  (max in log2 units, sum)
   float* part_o;      // [n, Hq, nsplit, D]
+  // K / V as 3-D bf16 tensors (D, B, n*H); box 64 columns x one 8 KB chunk of
+  // slots, 128-byte swizzle; slots past B read as zeros
+  CUtensorMap tk, tv;
 };
 
 namespace kvpop {
@@ -187,40 +191,69 @@ __global__ void __launch_bounds__(kUpdThreads)
 }
 
 // One CTA per (split of kSplit slots, KV head, sequence), 5 warps.  Warp 4
-// streams the split's K rows and then its V rows (contiguous kSplit x D bf16
-// blocks) through a kStages-deep ring of 8 KB chunks in shared memory
-// with bulk TMA copies, so every CTA keeps kStages chunks of HBM reads in
-// flight from start to end.  Warps 0-3 turn K chunks into scores (D / 8 lanes
-// per slot row, G query heads per row, packed f32x2 FMAs), take the softmax
-// over the whole split, then accumulate P.V from the V chunks.  Empty slots
-// hold finite data (zeros or stale rows) and get weight 0.  The last CTA of a
-// (sequence, head) to finish merges the splits' (max, sum, partial O).
+// streams the split's K rows and then its V rows through a kStages-deep ring
+// of 8 KB chunks with 2-D TMA boxes in the 128-byte-swizzled layout, so every
+// CTA keeps kStages chunks of HBM reads in flight.  The G query heads of a KV
+// head against a chunk of keys, and the probabilities against a chunk of
+// values, are small GEMMs (G x D x 32 keys): warps 0-3 run them with
+// mma.sync m16n8k16 (bf16 in, fp32 accumulate; the heads fill the first G of
+// 16 rows) fed by conflict-free ldmatrix from the swizzled chunks, which
+// keeps the instruction count far below the HBM time.  Softmax over the split
+// in fp32.  Empty slots hold finite data (zeros or stale rows) and get weight
+// 0.  The last CTA of a (sequence, head) to finish merges the splits' (max,
+// sum, partial O).
 constexpr int kChunkBytes = 8192;  // one ring chunk: 8 KB of slot rows
 constexpr int kStages = 6;         // ring depth
-constexpr int kCompute = 128; // compute threads (warps 0-3)
+constexpr int kCompute = 128;      // compute threads (warps 0-3)
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+// C (16x8 fp32) += A (16x16 bf16, row-major) * B (16x8 bf16, col-major)
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
 
 template <int D, int G>
 __global__ void __launch_bounds__(kAttnThreads)
-    decode_attn(kvpop_cache c, const __nv_bfloat16* __restrict__ q_new, float scale_log2,
-                __nv_bfloat16* __restrict__ O, float* __restrict__ lse) {
-  constexpr int LPR = D / 8;                 // lanes per row
-  constexpr int RPW = 32 / LPR;              // rows per warp instruction
+    decode_attn(const __grid_constant__ kvpop_cache c, const __nv_bfloat16* __restrict__ q_new, float scale_log2, __nv_bfloat16* __restrict__ O,
+                float* __restrict__ lse) {
   constexpr int NW = kCompute / 32;
-  constexpr int NG = kCompute / LPR;         // row groups for P.V
-  constexpr int kChunk = kChunkBytes / (D * 2);  // slot rows per ring chunk
-  constexpr int CB = kChunkBytes;
-  static_assert(NG * G * D * 4 <= kStages * CB, "partial O must fit in the ring");
-  extern __shared__ __align__(128) uint8_t dsm[];  // ring: kStages x CB bytes
-  float* opart = reinterpret_cast<float*>(dsm);    // [NG][G][D], reuses the ring at the end
-  __shared__ __align__(16) float sct[kSplit * G];  // scores, then weights: [slot][head]
+  constexpr int DH = D / 64;                     // 64-column halves
+  constexpr int kChunk = kChunkBytes / (D * 2);  // slot rows per chunk (32 or 64)
+  constexpr int HALF = kChunk * 128;             // bytes of one 64-column half of a chunk
+  constexpr int NTW = kChunk / 8 / NW;           // key n-tiles per warp in the score GEMM
+  constexpr int DW = D / NW;                     // output columns per warp in the P.V GEMM
+  constexpr int NDW = DW / 8;                    // d n-tiles per warp
+  constexpr int kPer = kSplit / kCompute;
+  static_assert(G <= 8, "at most 8 query heads fill the 16 MMA rows");
+  static_assert(NTW >= 1 && NDW % 2 == 0, "tile split");
+  extern __shared__ __align__(1024) uint8_t dsm[];  // ring: kStages x 8 KB, 1024-byte aligned
+  __shared__ __align__(16) float sct[kSplit * G];   // scores, then weights: [slot][head]
   __shared__ float red[G][NW];
-  __shared__ float m_s[G], l_s[G];
+  __shared__ float m_s[G], l_s[G], inv_s[G], lse_s[G];
   __shared__ int s_last;
   __shared__ __align__(8) uint64_t full[kStages], empty[kStages];
   __shared__ volatile int abort_flag;
+  uint8_t* ring = dsm + ((1024 - (smem_u32(dsm) & 1023)) & 1023);
+  const uint32_t ring_addr = smem_u32(ring);
   const int sp = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int H = c.H, B = c.B;
+  const int H = c.H, B = c.B, Hq = H * G;
   const int nh = n * H + h;
   const int slot_lo = sp * c.split_len;
   const int nslots = min(B, slot_lo + c.split_len) - slot_lo;
@@ -238,8 +271,8 @@ __global__ void __launch_bounds__(kAttnThreads)
   if (warp == NW) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
-      const __nv_bfloat16* kb = c.kc + ((size_t)nh * B + slot_lo) * D;
-      const __nv_bfloat16* vb = c.vc + ((size_t)nh * B + slot_lo) * D;
+      tma_prefetch_desc(&c.tk);
+      tma_prefetch_desc(&c.tv);
       for (int i = 0; i < 2 * nch; ++i) {
         const int st = i % kStages;
         if (!mbar_wait(&empty[st], ((i / kStages) & 1) ^ 1, &abort_flag)) {
@@ -247,113 +280,84 @@ __global__ void __launch_bounds__(kAttnThreads)
           abort_flag = 1;
           break;
         }
-        const int ci = i < nch ? i : i - nch;
-        const int rows = min(kChunk, nslots - ci * kChunk);
-        const uint32_t bytes = (uint32_t)rows * D * 2;
-        mbar_arrive_expect_tx(&full[st], bytes);
-        bulk_load(dsm + st * CB, (i < nch ? kb : vb) + (size_t)ci * kChunk * D, bytes, &full[st]);
+        const bool is_k = i < nch;
+        const int ci = is_k ? i : i - nch;
+        mbar_arrive_expect_tx(&full[st], kChunkBytes);
+        for (int dh = 0; dh < DH; ++dh)
+          tma_load_4d(ring + st * kChunkBytes + dh * HALF, is_k ? &c.tk : &c.tv, &full[st], dh * 64,
+                      slot_lo + ci * kChunk, nh, 0);
       }
     }
   } else {
     // ---------------------------------------------------------------- compute
-    const int sub = lane / LPR, li = lane % LPR;
+    const int g = lane >> 2, t = lane & 3;  // MMA fragment coordinates
     const int32_t* spos = c.slot_pos + (size_t)nh * B + slot_lo;
-    uint64_t qp[G][4];  // this lane's query chunk per head, log2 units, as pairs
+    // Q as MMA A fragments: row g < G holds query head h*G+g, columns are d
+    uint32_t aq[D / 16][2];
+    {
+      const __nv_bfloat16* qrow = q_new + ((size_t)n * Hq + h * G + (g < G ? g : 0)) * D;
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const uint4 raw = *reinterpret_cast<const uint4*>(q_new + ((size_t)n * H * G + h * G + g) * D + li * 8);
-      const __nv_bfloat162* pr = reinterpret_cast<const __nv_bfloat162*>(&raw);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 f = __bfloat1622float2(pr[e]);
-        qp[g][e] = pack2(f.x * scale_log2, f.y * scale_log2);
+      for (int ks = 0; ks < D / 16; ++ks) {
+        aq[ks][0] = g < G ? *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * t) : 0u;
+        aq[ks][1] = g < G ? *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 + 2 * t) : 0u;
       }
     }
-    // phase 1: scores of every slot of the split (warp-uniform loops: the
-    // shuffles need all lanes; rows past the split compute on zeros)
-    for (int ci = 0; ci < nch; ++ci) {
-      const int st = ci % kStages;
-      if (ok && !mbar_wait(&full[st], (ci / kStages) & 1, &abort_flag)) {
-        ok = false;
-        abort_flag = 1;
-      }
-      const __nv_bfloat16* kcs = reinterpret_cast<const __nv_bfloat16*>(dsm + st * CB);
-      constexpr int RW = kChunk / NW;  // rows per warp per chunk
-      uint4 raw[RW / RPW];
-#pragma unroll
-      for (int u = 0; u < RW / RPW; ++u) {
-        const int rl = warp * RW + u * RPW + sub;
-        raw[u] = ci * kChunk + rl < nslots ? *reinterpret_cast<const uint4*>(kcs + (size_t)rl * D + li * 8)
-                                           : make_uint4(0, 0, 0, 0);
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[st]);  // the chunk is in registers
-#pragma unroll
-      for (int u = 0; u < RW / RPW; ++u) {
-        const int r = ci * kChunk + warp * RW + u * RPW + sub;
-        const __nv_bfloat162* pr = reinterpret_cast<const __nv_bfloat162*>(&raw[u]);
-        uint64_t part[G];
-#pragma unroll
-        for (int g = 0; g < G; ++g) part[g] = 0;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 f = __bfloat1622float2(pr[e]);
-          const uint64_t kp = pack2(f.x, f.y);
-#pragma unroll
-          for (int g = 0; g < G; ++g) part[g] = fma2(kp, qp[g][e], part[g]);
-        }
-        // transposed butterfly over the LPR lanes of a row: each halving step
-        // sends half of the remaining heads to the partner and keeps the other
-        // half, so the lane ends with the full sum of one head
-        float v[G];
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          float a, b2;
-          unpack2(part[g], a, b2);
-          v[g] = a + b2;
-        }
-        int head = 0;
-#pragma unroll
-        for (int lev = 0, o = LPR / 2; (G >> lev) > 1; ++lev, o >>= 1) {
-          const int half = (G >> lev) / 2;
-          const bool up = (li & o) != 0;
-#pragma unroll
-          for (int i = 0; i < half; ++i) {
-            const float send = up ? v[i] : v[i + half];
-            const float keep = up ? v[i + half] : v[i];
-            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-          }
-          if (up) head += half;
-        }
-#pragma unroll
-        for (int o = LPR / (2 * G); o > 0; o >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
-        if ((li & (LPR / G - 1)) == 0 && r < nslots) sct[r * G + head] = v[0];
-      }
-    }
-    named_barrier_sync(1, kCompute);
-    // phase 2: per-head max and sum over the split (empty slots get weight 0);
-    // scores become weights.  Thread t owns slots t + 128 j.
-    constexpr int kPer = kSplit / kCompute;
     bool occ[kPer];
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
       const int r = tid + j * kCompute;
       occ[j] = r < nslots && spos[r] >= 0;
     }
+    // phase 1: S = Q K^T per chunk; warp w takes key n-tiles w*NTW .. w*NTW+NTW-1
+    for (int ci = 0; ci < nch; ++ci) {
+      const int st = ci % kStages;
+      if (ok && !mbar_wait(&full[st], (ci / kStages) & 1, &abort_flag)) {
+        ok = false;
+        abort_flag = 1;
+      }
+      const uint32_t cb = ring_addr + st * kChunkBytes;
+      float sacc[NTW][4];
+#pragma unroll
+      for (int j = 0; j < NTW; ++j) {
+        sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0.f;
+        const int r = (warp * NTW + j) * 8 + (lane & 7);  // key row this lane addresses
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ks += 2) {
+          const int cc16 = 2 * ks + (lane >> 3);  // 16-byte column chunk 0 .. D/8-1
+          const uint32_t addr = cb + (cc16 >> 3) * HALF + r * 128 + (((cc16 & 7) ^ (r & 7)) << 4);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(addr, b0, b1, b2, b3);
+          mma16816(sacc[j], aq[ks][0], 0u, aq[ks][1], 0u, b0, b1);
+          mma16816(sacc[j], aq[ks + 1][0], 0u, aq[ks + 1][1], 0u, b2, b3);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
+      if (g < G) {
+#pragma unroll
+        for (int j = 0; j < NTW; ++j) {
+          const int key = ci * kChunk + (warp * NTW + j) * 8 + 2 * t;
+          if (key < nslots) sct[key * G + g] = sacc[j][0] * scale_log2;
+          if (key + 1 < nslots) sct[(key + 1) * G + g] = sacc[j][1] * scale_log2;
+        }
+      }
+    }
+    named_barrier_sync(1, kCompute);
+    // phase 2: per-head max and sum over the split; scores become weights
     {
       float m[G];
 #pragma unroll
-      for (int g = 0; g < G; ++g) m[g] = __int_as_float(0xff800000);
+      for (int gg = 0; gg < G; ++gg) m[gg] = __int_as_float(0xff800000);
 #pragma unroll
       for (int j = 0; j < kPer; ++j)
         if (occ[j]) {
 #pragma unroll
-          for (int g = 0; g < G; ++g) m[g] = fmaxf(m[g], sct[(tid + j * kCompute) * G + g]);
+          for (int gg = 0; gg < G; ++gg) m[gg] = fmaxf(m[gg], sct[(tid + j * kCompute) * G + gg]);
         }
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        for (int o = 16; o > 0; o >>= 1) m[g] = fmaxf(m[g], __shfl_xor_sync(0xffffffffu, m[g], o));
-        if (lane == 0) red[g][warp] = m[g];
+      for (int gg = 0; gg < G; ++gg) {
+        for (int o = 16; o > 0; o >>= 1) m[gg] = fmaxf(m[gg], __shfl_xor_sync(0xffffffffu, m[gg], o));
+        if (lane == 0) red[gg][warp] = m[gg];
       }
     }
     named_barrier_sync(1, kCompute);
@@ -366,23 +370,23 @@ __global__ void __launch_bounds__(kAttnThreads)
     {
       float l[G];
 #pragma unroll
-      for (int g = 0; g < G; ++g) l[g] = 0.f;
+      for (int gg = 0; gg < G; ++gg) l[gg] = 0.f;
 #pragma unroll
       for (int j = 0; j < kPer; ++j) {
         const int r = tid + j * kCompute;
         if (r >= nslots) break;
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float m = m_s[g];
-          const float e = (occ[j] && m != __int_as_float(0xff800000)) ? ex2_approx(sct[r * G + g] - m) : 0.f;
-          sct[r * G + g] = e;
-          l[g] += e;
+        for (int gg = 0; gg < G; ++gg) {
+          const float mg = m_s[gg];
+          const float e = (occ[j] && mg != __int_as_float(0xff800000)) ? ex2_approx(sct[r * G + gg] - mg) : 0.f;
+          sct[r * G + gg] = e;
+          l[gg] += e;
         }
       }
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        for (int o = 16; o > 0; o >>= 1) l[g] += __shfl_xor_sync(0xffffffffu, l[g], o);
-        if (lane == 0) red[g][warp] = l[g];
+      for (int gg = 0; gg < G; ++gg) {
+        for (int o = 16; o > 0; o >>= 1) l[gg] += __shfl_xor_sync(0xffffffffu, l[gg], o);
+        if (lane == 0) red[gg][warp] = l[gg];
       }
     }
     named_barrier_sync(1, kCompute);
@@ -391,13 +395,10 @@ __global__ void __launch_bounds__(kAttnThreads)
       for (int i = 0; i < NW; ++i) l += red[tid][i];
       l_s[tid] = l;
     }
-    // phase 3: partial O = sum_r p_r v_r
-    uint64_t acc[G][4];
+    // phase 3: O = P V per chunk; warp w owns output columns w*DW .. w*DW+DW-1
+    float oacc[NDW][4];
 #pragma unroll
-    for (int g = 0; g < G; ++g)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[g][e] = 0;
-    const int grp = tid / LPR;
+    for (int j = 0; j < NDW; ++j) oacc[j][0] = oacc[j][1] = oacc[j][2] = oacc[j][3] = 0.f;
     for (int ci = 0; ci < nch; ++ci) {
       const int i = nch + ci;
       const int st = i % kStages;
@@ -405,60 +406,50 @@ __global__ void __launch_bounds__(kAttnThreads)
         ok = false;
         abort_flag = 1;
       }
-      const __nv_bfloat16* vcs = reinterpret_cast<const __nv_bfloat16*>(dsm + st * CB);
+      const uint32_t cb = ring_addr + st * kChunkBytes;
 #pragma unroll
-      for (int u = 0; u < kChunk / NG; ++u) {
-        const int rl = grp + u * NG;
-        const int r = ci * kChunk + rl;
-        if (r >= nslots) break;
-        const uint4 raw = *reinterpret_cast<const uint4*>(vcs + (size_t)rl * D + li * 8);
-        const __nv_bfloat162* pv = reinterpret_cast<const __nv_bfloat162*>(&raw);
-        uint64_t wp[G];
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float w = sct[r * G + g];
-          wp[g] = pack2(w, w);
+      for (int kk = 0; kk < kChunk; kk += 16) {
+        // A: probabilities of heads g (rows) for keys kk .. kk+15 (columns), bf16
+        uint32_t a0 = 0u, a2 = 0u;
+        if (g < G) {
+          const int k0 = ci * kChunk + kk + 2 * t;
+          const float p0 = k0 < nslots ? sct[k0 * G + g] : 0.f;
+          const float p1 = k0 + 1 < nslots ? sct[(k0 + 1) * G + g] : 0.f;
+          const float p8 = k0 + 8 < nslots ? sct[(k0 + 8) * G + g] : 0.f;
+          const float p9 = k0 + 9 < nslots ? sct[(k0 + 9) * G + g] : 0.f;
+          a0 = pack_bf16x2(p0, p1);
+          a2 = pack_bf16x2(p8, p9);
         }
+        const int r = kk + (lane & 7) + ((lane >> 3) & 1) * 8;  // value row this lane addresses
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 f = __bfloat1622float2(pv[e]);
-          const uint64_t vp = pack2(f.x, f.y);
-#pragma unroll
-          for (int g = 0; g < G; ++g) acc[g][e] = fma2(vp, wp[g], acc[g][e]);
+        for (int j = 0; j < NDW; j += 2) {
+          const int cc16 = (warp * DW + j * 8) / 8 + (lane >> 4);
+          const uint32_t addr = cb + (cc16 >> 3) * HALF + r * 128 + (((cc16 & 7) ^ (r & 7)) << 4);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(addr, b0, b1, b2, b3);
+          mma16816(oacc[j], a0, 0u, a2, 0u, b0, b1);
+          mma16816(oacc[j + 1], a0, 0u, a2, 0u, b2, b3);
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
     }
-    named_barrier_sync(1, kCompute);  // every chunk consumed: the ring becomes opart
+    // partial O: lane (g, t) holds O[g][d = warp*DW + j*8 + 2t, +1]
+    if (g < G) {
+      float* po = c.part_o + (((size_t)n * Hq + h * G + g) * c.nsplit + sp) * D + warp * DW + 2 * t;
 #pragma unroll
-    for (int g = 0; g < G; ++g)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float a, b2;
-        unpack2(acc[g][e], a, b2);
-        opart[(grp * G + g) * D + li * 8 + 2 * e] = a;
-        opart[(grp * G + g) * D + li * 8 + 2 * e + 1] = b2;
-      }
+      for (int j = 0; j < NDW; ++j) *reinterpret_cast<float2*>(po + j * 8) = make_float2(oacc[j][0], oacc[j][1]);
+    }
+    if (tid < G) {
+      float* ml = c.part_ml + (((size_t)n * Hq + h * G + tid) * c.nsplit + sp) * 2;
+      ml[0] = m_s[tid];
+      ml[1] = l_s[tid];
+    }
   }
-  __syncthreads();
-  if (!ok) report_error(device_status_from(c), KVPOP_ERR_TIMEOUT, SITE_DECODE, 1);
-  const int Hq = H * G;
-  for (int i = tid; i < G * D; i += kAttnThreads) {
-    const int g = i / D, d = i % D;
-    float o = 0.f;
-#pragma unroll
-    for (int r = 0; r < NG; ++r) o += opart[(r * G + g) * D + d];
-    c.part_o[(((size_t)n * Hq + h * G + g) * c.nsplit + sp) * D + d] = o;
-  }
-  if (tid < G) {
-    float* ml = c.part_ml + (((size_t)n * Hq + h * G + tid) * c.nsplit + sp) * 2;
-    ml[0] = m_s[tid];
-    ml[1] = l_s[tid];
-  }
-  // the last split CTA of this (sequence, head) merges all splits
+  // the last CTA of this (sequence, head) to finish merges all splits
   __threadfence();
   __syncthreads();
+  if (!ok) report_error(device_status_from(c), KVPOP_ERR_TIMEOUT, SITE_DECODE, 1);
   if (tid == 0) {
     const int prev = atomicAdd(c.done_cnt + nh, 1);
     s_last = prev == c.nsplit - 1;
@@ -466,11 +457,8 @@ __global__ void __launch_bounds__(kAttnThreads)
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  // merge: split weights per head in shared memory, then every output element
-  // issues its nsplit partial loads together
   const int ns = c.nsplit;
-  float* wgt = sct;  // [G][ns] weight of each split, reuses the score buffer
-  __shared__ float inv_s[G], lse_s[G];
+  float* wgt = sct;  // [G][ns] weight of each split
   const size_t row0 = (size_t)n * Hq + h * G;
   for (int i = tid; i < G * ns; i += kAttnThreads) wgt[i] = __ldcg(c.part_ml + (row0 * ns + i) * 2);
   __syncthreads();
@@ -489,12 +477,12 @@ __global__ void __launch_bounds__(kAttnThreads)
   }
   __syncthreads();
   for (int i = tid; i < G * D; i += kAttnThreads) {
-    const int g = i / D, d = i % D;
-    const float* po = c.part_o + ((row0 + g) * ns) * D + d;
+    const int gg = i / D, d = i % D;
+    const float* po = c.part_o + ((row0 + gg) * ns) * D + d;
     float o = 0.f;
 #pragma unroll 8
-    for (int sidx = 0; sidx < ns; ++sidx) o += __ldcg(po + (size_t)sidx * D) * wgt[g * ns + sidx];
-    O[(row0 + g) * D + d] = __float2bfloat16_rn(o * inv_s[g]);
+    for (int sidx = 0; sidx < ns; ++sidx) o += __ldcg(po + (size_t)sidx * D) * wgt[gg * ns + sidx];
+    O[(row0 + gg) * D + d] = __float2bfloat16_rn(o * inv_s[gg]);
   }
   if (tid < G) lse[row0 + tid] = lse_s[tid];
   if (tid == 0) c.done_cnt[nh] = 0;  // ready for the next step
@@ -574,7 +562,7 @@ template <int D, int G>
 kvpop_status launch_attn_g(const kvpop_cache& c, const void* q_new, float sl2, void* O, float* lse,
                            cudaStream_t cs) {
   auto kern = decode_attn<D, G>;
-  const int smem = kStages * kChunkBytes;
+  const int smem = kStages * kChunkBytes + 1024;  // + alignment slack for the swizzled ring
   kvpop_status st = cuda_check(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem),
                                "kvpop_decode_step: smem attribute");
   if (st != KVPOP_OK) return st;
@@ -658,6 +646,13 @@ extern "C" kvpop_status kvpop_cache_create(int n, int H, int G, int D, kvpop_bud
   if (st == KVPOP_OK) st = cuda_check(cudaMemset(c->done_cnt, 0, (size_t)n * H * 4), "kvpop_cache_create: init");
   if (st == KVPOP_OK) st = cuda_check(cudaMemset(c->kc, 0, slots * D * 2), "kvpop_cache_create: init");
   if (st == KVPOP_OK) st = cuda_check(cudaMemset(c->vc, 0, slots * D * 2), "kvpop_cache_create: init");
+  if (st == KVPOP_OK) {
+    const uint64_t dims[4] = {(uint64_t)D, (uint64_t)c->B, (uint64_t)n * H, 1};
+    const uint64_t strides[3] = {(uint64_t)D * 2, (uint64_t)c->B * D * 2, (uint64_t)n * H * c->B * D * 2};
+    const uint32_t box[4] = {64, (uint32_t)(kChunkBytes / (D * 2)), 1, 1};
+    if (!make_tmap_4d(&c->tk, c->kc, dims, strides, box) || !make_tmap_4d(&c->tv, c->vc, dims, strides, box))
+      st = KVPOP_ERR_CUDA;
+  }
   if (st != KVPOP_OK) {
     kvpop_cache_destroy(c);
     return st;
