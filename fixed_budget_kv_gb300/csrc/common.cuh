@@ -65,6 +65,14 @@ __device__ __forceinline__ int lane_id() { return threadIdx.x & 31; }
 
 __device__ __forceinline__ bool elect_one() { return lane_id() == 0; }
 
+// Programmatic dependent launch: a grid launched with programmatic stream
+// serialization may start while the previous kernel of its stream runs;
+// grid_dep_wait() returns once that kernel has completed and its writes are
+// visible (a no-op for a normal launch), grid_dep_launch() lets the next
+// kernel's CTAs be scheduled early.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Barrier over the first `nthreads` threads (whole warps) of the CTA.
 __device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

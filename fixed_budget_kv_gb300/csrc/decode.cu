@@ -38,7 +38,7 @@ struct kvpop_cache {
 namespace kvpop {
 namespace {
 
-constexpr int kSplit = 512;  // slots per attention CTA
+constexpr int kSplit = 256;  // slots per attention CTA
 constexpr int kUpdThreads = 256;
 constexpr int kAttnThreads = 160;  // 4 compute warps + 1 producer warp
 
@@ -51,37 +51,48 @@ __device__ __forceinline__ bool worse(float va, int pa, float vb, int pb) {
   return va < vb || (va == vb && pa > pb);
 }
 
-__device__ __forceinline__ void copy_row(__nv_bfloat16* dst, const __nv_bfloat16* src, int D, int tid,
-                                         int nthreads) {
-  const uint4* s = reinterpret_cast<const uint4*>(src);
-  uint4* d = reinterpret_cast<uint4*>(dst);
-  for (int i = tid; i < D / 8; i += nthreads) d[i] = s[i];
-}
-
+// One CTA per (sequence, head).  Every global value the step may need -- the
+// long-range count, the long-range priorities and positions, the leaving
+// token's priority and K/V row, the new K/V row -- is loaded up front in one
+// batch, so the kernel costs one memory round trip, a block arg-min and the
+// stores.
 __global__ void __launch_bounds__(kUpdThreads)
     decode_update(kvpop_cache c, int q, const __nv_bfloat16* __restrict__ k_new,
                   const __nv_bfloat16* __restrict__ v_new, const float* __restrict__ prio_new,
                   int32_t* __restrict__ evicted_pos) {
+  constexpr int kBatch = 8;  // long-range entries per thread per pass
   __shared__ float red_v[kUpdThreads / 32];
   __shared__ int red_p[kUpdThreads / 32];
   __shared__ int red_s[kUpdThreads / 32];
-  __shared__ int s_dst, s_evicted, s_cnt;
+  __shared__ int s_dst, s_evicted;
   const int nh = blockIdx.x;  // sequence * H + head
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  grid_dep_launch();
+  grid_dep_wait();  // nothing is read before the previous kernel has finished
   const int D = c.D, B = c.B, s = c.s, w = c.w, k = c.k;
+  const int CH = D / 8;  // 16-byte pieces per row
   const size_t slot0 = (size_t)nh * B;
-  __nv_bfloat16* kc = c.kc + slot0 * D;
-  __nv_bfloat16* vc = c.vc + slot0 * D;
+  uint4* kc = reinterpret_cast<uint4*>(c.kc + slot0 * D);
+  uint4* vc = reinterpret_cast<uint4*>(c.vc + slot0 * D);
   int32_t* spos = c.slot_pos + slot0;
   float* sprio = c.slot_prio + slot0;
-  const __nv_bfloat16* kin = k_new + (size_t)nh * D;
-  const __nv_bfloat16* vin = v_new + (size_t)nh * D;
   const float pin = prio_new[nh];
-
+  // the competing token: u = q - w from the ring, or q itself when w == 0
+  const int u = q - w;
+  const int ring = w > 0 && q >= s ? s + (q - s) % w : -1;
+  const bool compete = q >= s && u >= s;
+  // threads [0, CH) hold the new K piece, [CH, 2CH) the new V piece,
+  // [2CH, 3CH) the ring's K piece, [3CH, 4CH) the ring's V piece
+  const int role = tid < 4 * CH ? tid / CH : 4, piece = tid % CH;
+  uint4 row = make_uint4(0, 0, 0, 0);
+  if (role == 0) row = reinterpret_cast<const uint4*>(k_new + (size_t)nh * D)[piece];
+  if (role == 1) row = reinterpret_cast<const uint4*>(v_new + (size_t)nh * D)[piece];
+  if (role == 2 && compete && ring >= 0) row = kc[(size_t)ring * CH + piece];
+  if (role == 3 && compete && ring >= 0) row = vc[(size_t)ring * CH + piece];
   if (q < s) {
     // sink
-    copy_row(kc + (size_t)q * D, kin, D, tid, kUpdThreads);
-    copy_row(vc + (size_t)q * D, vin, D, tid, kUpdThreads);
+    if (role == 0) kc[(size_t)q * CH + piece] = row;
+    if (role == 1) vc[(size_t)q * CH + piece] = row;
     if (tid == 0) {
       spos[q] = q;
       sprio[q] = pin;
@@ -89,99 +100,90 @@ __global__ void __launch_bounds__(kUpdThreads)
     }
     return;
   }
-  // the competing token: u = q - w from the ring, or q itself when w == 0
-  const int u = q - w;
-  const int ring = w > 0 ? s + (q - s) % w : -1;
-  if (tid == 0) {
-    s_dst = -1;
-    s_evicted = -1;
-    s_cnt = c.topk_cnt[nh];
-  }
-  __syncthreads();
-  if (u >= s) {
-    const float pu = w > 0 ? sprio[ring] : pin;
-    const int cnt = s_cnt;  // block-uniform
-    if (k == 0) {
-      if (tid == 0) s_evicted = u;
-    } else if (cnt < k) {
-      if (tid == 0) {
+  int cnt = 0;
+  float pu = pin;
+  if (compete && k > 0) {
+    cnt = c.topk_cnt[nh];
+    if (ring >= 0) pu = sprio[ring];
+    // worst held long-range token: lowest priority, later position on ties
+    float bv = __int_as_float(0x7f800000);
+    int bp = -1, bs = -1;
+    for (int i0 = tid; i0 < k; i0 += kUpdThreads * kBatch) {
+      float vv[kBatch];
+      int pp[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {  // all loads of the batch in flight together
+        const int i = i0 + j * kUpdThreads;
+        vv[j] = i < k ? prio_val(sprio[s + w + i]) : 0.0f;
+        pp[j] = i < k ? spos[s + w + i] : -1;
+      }
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int i = i0 + j * kUpdThreads;
+        if (i < k && (bs < 0 || worse(vv[j], pp[j], bv, bp))) {
+          bv = vv[j];
+          bp = pp[j];
+          bs = s + w + i;
+        }
+      }
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int op = __shfl_xor_sync(0xffffffffu, bp, o);
+      const int os = __shfl_xor_sync(0xffffffffu, bs, o);
+      if (os >= 0 && (bs < 0 || worse(ov, op, bv, bp))) {
+        bv = ov;
+        bp = op;
+        bs = os;
+      }
+    }
+    if (lane == 0) {
+      red_v[warp] = bv;
+      red_p[warp] = bp;
+      red_s[warp] = bs;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      if (cnt < k) {  // a free long-range slot
         s_dst = s + w + cnt;
+        s_evicted = -1;
         c.topk_cnt[nh] = cnt + 1;
-      }
-    } else {
-      // worst held long-range token
-      float bv = __int_as_float(0x7f800000);
-      int bp = -1, bs = -1;
-      for (int i0 = tid; i0 < k; i0 += kUpdThreads * 8) {
-        float vv[8];
-        int pp[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {  // all loads of the batch in flight together
-          const int i = i0 + u * kUpdThreads;
-          vv[u] = i < k ? prio_val(sprio[s + w + i]) : 0.0f;
-          pp[u] = i < k ? spos[s + w + i] : -1;
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int i = i0 + u * kUpdThreads;
-          if (i < k && (bs < 0 || worse(vv[u], pp[u], bv, bp))) {
-            bv = vv[u];
-            bp = pp[u];
-            bs = s + w + i;
-          }
-        }
-      }
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int op = __shfl_xor_sync(0xffffffffu, bp, o);
-        const int os = __shfl_xor_sync(0xffffffffu, bs, o);
-        if (os >= 0 && (bs < 0 || worse(ov, op, bv, bp))) {
-          bv = ov;
-          bp = op;
-          bs = os;
-        }
-      }
-      if (lane == 0) {
-        red_v[warp] = bv;
-        red_p[warp] = bp;
-        red_s[warp] = bs;
-      }
-      __syncthreads();
-      if (tid == 0) {
+      } else {
         for (int i = 1; i < kUpdThreads / 32; ++i)
           if (red_s[i] >= 0 && (bs < 0 || worse(red_v[i], red_p[i], bv, bp))) {
             bv = red_v[i];
             bp = red_p[i];
             bs = red_s[i];
           }
-        if (prio_val(pu) > bv) {  // strictly better than the worst held token
-          s_dst = bs;
-          s_evicted = bp;
-        } else {
-          s_evicted = u;
-        }
+        const bool take = prio_val(pu) > bv;  // strictly better than the worst held token
+        s_dst = take ? bs : -1;
+        s_evicted = take ? bp : u;
       }
     }
     __syncthreads();
-    const int dst = s_dst;
-    if (dst >= 0) {
-      if (w > 0) {
-        copy_row(kc + (size_t)dst * D, kc + (size_t)ring * D, D, tid, kUpdThreads);
-        copy_row(vc + (size_t)dst * D, vc + (size_t)ring * D, D, tid, kUpdThreads);
-      } else {
-        copy_row(kc + (size_t)dst * D, kin, D, tid, kUpdThreads);
-        copy_row(vc + (size_t)dst * D, vin, D, tid, kUpdThreads);
-      }
-      if (tid == 0) {
-        spos[dst] = u;
-        sprio[dst] = pu;
-      }
+  } else if (tid == 0) {
+    s_dst = -1;
+    s_evicted = compete ? u : -1;  // k == 0: the leaving token is dropped
+  }
+  if (!(compete && k > 0)) __syncthreads();
+  const int dst = s_dst;
+  if (dst >= 0) {
+    // the competitor's row: the ring's old contents, or the new token when w == 0
+    if (w > 0) {
+      if (role == 2) kc[(size_t)dst * CH + piece] = row;
+      if (role == 3) vc[(size_t)dst * CH + piece] = row;
+    } else {
+      if (role == 0) kc[(size_t)dst * CH + piece] = row;
+      if (role == 1) vc[(size_t)dst * CH + piece] = row;
+    }
+    if (tid == 0) {
+      spos[dst] = u;
+      sprio[dst] = pu;
     }
   }
-  __syncthreads();
-  if (w > 0) {
-    copy_row(kc + (size_t)ring * D, kin, D, tid, kUpdThreads);
-    copy_row(vc + (size_t)ring * D, vin, D, tid, kUpdThreads);
+  if (ring >= 0) {
+    if (role == 0) kc[(size_t)ring * CH + piece] = row;
+    if (role == 1) vc[(size_t)ring * CH + piece] = row;
     if (tid == 0) {
       spos[ring] = q;
       sprio[ring] = pin;
@@ -192,7 +194,7 @@ __global__ void __launch_bounds__(kUpdThreads)
 
 // One CTA per (split of kSplit slots, KV head, sequence), 5 warps.  Warp 4
 // streams the split's K rows and then its V rows through a kStages-deep ring
-// of 8 KB chunks with 2-D TMA boxes in the 128-byte-swizzled layout, so every
+// of 8 KB chunks with 3-D TMA boxes in the 128-byte-swizzled layout, so every
 // CTA keeps kStages chunks of HBM reads in flight.  The G query heads of a KV
 // head against a chunk of keys, and the probabilities against a chunk of
 // values, are small GEMMs (G x D x 32 keys): warps 0-3 run them with
@@ -203,7 +205,7 @@ __global__ void __launch_bounds__(kUpdThreads)
 // 0.  The last CTA of a (sequence, head) to finish merges the splits' (max,
 // sum, partial O).
 constexpr int kChunkBytes = 8192;  // one ring chunk: 8 KB of slot rows
-constexpr int kStages = 6;         // ring depth
+constexpr int kStages = 4;         // ring depth (5 CTAs per SM fit)
 constexpr int kCompute = 128;      // compute threads (warps 0-3)
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
@@ -266,13 +268,17 @@ __global__ void __launch_bounds__(kAttnThreads)
     abort_flag = 0;
     fence_mbar_init();
   }
+  if (warp == NW && lane == 0) {
+    tma_prefetch_desc(&c.tk);
+    tma_prefetch_desc(&c.tv);
+  }
+  grid_dep_launch();
+  grid_dep_wait();  // the update of this step has finished: slots, K and V are final
   __syncthreads();
   bool ok = true;
   if (warp == NW) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
-      tma_prefetch_desc(&c.tk);
-      tma_prefetch_desc(&c.tv);
       for (int i = 0; i < 2 * nch; ++i) {
         const int st = i % kStages;
         if (!mbar_wait(&empty[st], ((i / kStages) & 1) ^ 1, &abort_flag)) {
@@ -566,9 +572,18 @@ kvpop_status launch_attn_g(const kvpop_cache& c, const void* q_new, float sl2, v
   kvpop_status st = cuda_check(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem),
                                "kvpop_decode_step: smem attribute");
   if (st != KVPOP_OK) return st;
-  dim3 grid(c.nsplit, c.H, c.n);
-  kern<<<grid, kAttnThreads, smem, cs>>>(c, (const __nv_bfloat16*)q_new, sl2, (__nv_bfloat16*)O, lse);
-  return cuda_check(cudaGetLastError(), "kvpop_decode_step: attention launch");
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(c.nsplit, c.H, c.n);
+  cfg.blockDim = dim3(kAttnThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = cs;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cuda_check(cudaLaunchKernelEx(&cfg, kern, c, (const __nv_bfloat16*)q_new, sl2, (__nv_bfloat16*)O, lse),
+                    "kvpop_decode_step: attention launch");
 }
 
 template <int D>
@@ -716,10 +731,20 @@ extern "C" kvpop_status kvpop_decode_step(kvpop_cache* c, const void* q_new, con
   }
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   const int q = c->q_next;
-  decode_update<<<c->n * c->H, kUpdThreads, 0, cs>>>(*c, q, (const __nv_bfloat16*)k_new,
-                                                     (const __nv_bfloat16*)v_new, prio_new,
-                                                     evicted_pos);
-  kvpop_status st = cuda_check(cudaGetLastError(), "kvpop_decode_step: update launch");
+  // both kernels use programmatic dependent launch: each starts while the
+  // previous kernel of the stream drains and waits for it before any read
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(c->n * c->H);
+  cfg.blockDim = dim3(kUpdThreads);
+  cfg.stream = cs;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  kvpop_status st = cuda_check(cudaLaunchKernelEx(&cfg, decode_update, *c, q, (const __nv_bfloat16*)k_new,
+                                                  (const __nv_bfloat16*)v_new, prio_new, evicted_pos),
+                               "kvpop_decode_step: update launch");
   if (st != KVPOP_OK) return st;
   const float sl2 = 1.4426950408889634f / sqrtf((float)c->D);
   st = c->D == 128 ? launch_attn<128>(*c, q_new, sl2, O, lse, cs) : launch_attn<64>(*c, q_new, sl2, O, lse, cs);

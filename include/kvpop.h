@@ -187,7 +187,10 @@ kvpop_status kvpop_future_target_noalloc(const void* q, const void* k, const flo
 typedef struct kvpop_cache kvpop_cache;
 
 /* Allocates the device state (K/V [n,H,B,D] bf16, slot positions and
- * priorities, split-softmax partials).  q starts at 0. */
+ * priorities, split-softmax partials); the caller owns the handle and frees it
+ * with kvpop_cache_destroy.  q starts at 0.  Limits: D in {64, 128}, G in
+ * {1, 2, 4, 8}, 1 <= B <= 65536, n*H <= 65535; otherwise
+ * KVPOP_ERR_INVALID_ARG (bad budget) or KVPOP_ERR_UNSUPPORTED. */
 kvpop_status kvpop_cache_create(int n, int H, int G, int D, kvpop_budget budget,
                                 kvpop_cache** out);
 kvpop_status kvpop_cache_destroy(kvpop_cache* cache);
@@ -199,7 +202,11 @@ kvpop_status kvpop_cache_prefill(kvpop_cache* cache, const void* k, const void* 
                                  const float* prio, int P, const int32_t* evict_at,
                                  kvpop_stream stream);
 
-/* One decode step at the cache's position q (then q += 1):
+/* One decode step at the cache's position q (then q += 1).  Two kernels on
+ * `stream` (the update, then the split attention with the split merge fused
+ * into its last CTA), both with programmatic dependent launch: neither reads
+ * any buffer before the previous kernel of the stream has completed.
+ * q_new, k_new, v_new must be 16-byte aligned (else KVPOP_ERR_UNSUPPORTED).
  *   1. the token u = q - w leaves the window; if u >= s it takes a free
  *      long-range slot, or replaces the worst held token m (lowest priority,
  *      later index on ties) when its priority is strictly greater, else it is

@@ -72,4 +72,6 @@ def test_target_and_cache_validation(lib):
     h = ctypes.c_void_p()
     assert lib.kvpop_cache_create(1, 1, 3, 64, kvpop.Budget(1, 1, 1), ctypes.byref(h)) == 2
     assert lib.kvpop_cache_create(1, 1, 4, 64, kvpop.Budget(0, 0, 0), ctypes.byref(h)) == 1
+    # at most 65536 slots per head (the split merge holds 256 splits of 256 slots)
+    assert lib.kvpop_cache_create(1, 1, 4, 64, kvpop.Budget(16, 1024, 65536 - 1040 + 1), ctypes.byref(h)) == 1
     assert lib.kvpop_decode_step(None, P, P, P, P, P, P, None, None) == 1
