@@ -45,6 +45,11 @@ constexpr int kKeys = 128;
 constexpr int kMetaStages = 4;
 constexpr int kBlockBytes = 128 * 128;  // 128 rows x 128 bytes
 constexpr float kRescaleLog2 = 8.0f;
+// Register split: warpgroup 0 (producer, MMA, loaders) drops to kRegsIo, the two
+// softmax warpgroups (one S row of 128 fp32 per thread) rise to kRegsSoftmax.
+constexpr int kRegsIo = 64;
+constexpr int kRegsSoftmax = 216;
+constexpr int kRegsNeeded = (128 * kRegsIo + 256 * kRegsSoftmax + kThreads - 1) / kThreads;  // per thread at launch
 
 struct AttnParams {
   CUtensorMap tq, tk, tv;
@@ -199,6 +204,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   const uint32_t k_addr = sbase + L::k_off;
   const uint32_t v_addr = sbase + L::v_off;
 
+  if (warp < 4) {
+    setmaxnreg_dec<kRegsIo>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer / metadata
     if (!SPARSE) {
@@ -374,180 +381,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
       mma_commit(&bars->drain);
       mbar_wait(&bars->drain, 0, nullptr);
     }
-  } else if (warp >= 4) {
-    // ------------------------------------------------------------ softmax
-    const int qt = (warp - 4) >> 2;
-    const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;
-    const int p_row = row / G, g = row - p_row * G;
-    const uint32_t tl = tbase + ((uint32_t)(quarter * 32) << 16);
-    const uint32_t s_col = 128 * qt, o_col = 256 + 128 * qt;
-    const float sl2 = p.scale_log2;
-    const uint64_t s2 = pack2(sl2, sl2);
-    bool ok = true;
-    int t = 0, n = 0;
-    for (int it = it0; ok && it < p.nitems; it += dit, ++n) {
-      const Item x = make_item<SPARSE>(p, it);
-      const int q = x.qb0 + qt * P + p_row;
-      const int q_first = x.qb0 + qt * P;
-      const int jh = x.h * G + g;
-      float m_ref = neg_inf(), l = 0.0f;
-      for (int j = 0; j < x.NT; ++j, ++t) {
-        if (!warp_wait(&bars->s_full[qt], t & 1, abort_flag)) {
-          if (lane == 0) fail(SITE_ATTN_SOFTMAX, 1);
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const int ms = t % kMetaStages;
-        const int2* km = meta + ms * (kKeys + 4);
-        if (SPARSE) {
-          if (!warp_wait(&bars->meta_full[ms], (t / kMetaStages) & 1, abort_flag)) {
-            if (lane == 0) fail(SITE_ATTN_SOFTMAX, 2);
-            ok = false;
-            break;
-          }
-        }
-        const bool diag = !SPARSE && (j * kKeys + kKeys - 1) > q_first;
-        // pass 1: visibility of the 32-key chunks and the tile max
-        uint32_t vis[4];
-        float mt = neg_inf();
-        {
-          uint32_t ra[32], rb[32];
-          tmem_ld32(tl + s_col, ra);
-#pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            uint32_t(&cur)[32] = (ch & 1) ? rb : ra;
-            uint32_t(&nxt)[32] = (ch & 1) ? ra : rb;
-            tmem_wait_ld_dep(cur);
-            if (ch < 3) tmem_ld32(tl + s_col + (ch + 1) * 32, nxt);
-            bool fast;
-            if (SPARSE) {
-              const int2 sum = km[kKeys + ch];
-              fast = q >= sum.x && q < sum.y;
-            } else {
-              fast = !diag || (j * kKeys + ch * 32 + 31) <= q;
-            }
-            uint32_t bits = 0xffffffffu;
-            if (!fast) {
-#pragma unroll
-              for (int c = 0; c < 32; ++c) {
-                bool visible;
-                if (SPARSE) {
-                  const int2 e = km[ch * 32 + c];
-                  visible = e.x <= q && q < e.y;
-                } else {
-                  visible = j * kKeys + ch * 32 + c <= q;
-                }
-                if (!visible) {
-                  bits &= ~(1u << c);
-                  cur[c] = 0xff800000u;
-                }
-              }
-            }
-            vis[ch] = bits;
-            mt = fmaxf(mt, max32(cur));
-          }
-        }
-        // lazy rescale of the running max
-        const float m_new = fmaxf(m_ref, mt);
-        const bool need = (m_new - m_ref) * sl2 > kRescaleLog2;  // true when m_ref == -inf and mt finite
-        float alpha = 1.0f;
-        if (need) {
-          alpha = ex2_approx((m_ref - m_new) * sl2);
-          l *= alpha;
-          m_ref = m_new;
-        }
-        if (__any_sync(0xffffffffu, need) && j > 0) {
-          // O of tile j-1 is complete: s_full for tile j was committed after it
-#pragma unroll
-          for (int cd = 0; cd < D / 32; ++cd) {
-            uint32_t r[32];
-            tmem_ld32(tl + o_col + cd * 32, r);
-            tmem_wait_ld_dep(r);
-#pragma unroll
-            for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * alpha);
-            tmem_st32(tl + o_col + cd * 32, r);
-          }
-          tmem_wait_st();
-        }
-        // pass 2: P = exp2(s * scale_log2 - m) as bf16, written over S
-        const float nm = (m_ref == neg_inf()) ? 0.0f : -m_ref * sl2;
-        const uint64_t n2 = pack2(nm, nm);
-        uint64_t lacc = 0;
-        {
-          uint32_t ra[32], rb[32];
-          tmem_ld32(tl + s_col, ra);
-#pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            uint32_t(&cur)[32] = (ch & 1) ? rb : ra;
-            uint32_t(&nxt)[32] = (ch & 1) ? ra : rb;
-            tmem_wait_ld_dep(cur);
-            if (ch < 3) tmem_ld32(tl + s_col + (ch + 1) * 32, nxt);
-            const uint32_t bits = vis[ch];
-            if (bits != 0xffffffffu) {
-#pragma unroll
-              for (int c = 0; c < 32; ++c)
-                if (!((bits >> c) & 1u)) cur[c] = 0xff800000u;
-            }
-            uint32_t pk[16];
-#pragma unroll
-            for (int c = 0; c < 32; c += 2) {
-              const uint64_t xx = fma2(pack2(__uint_as_float(cur[c]), __uint_as_float(cur[c + 1])), s2, n2);
-              float e0, e1;
-              unpack2(xx, e0, e1);
-              const float p0 = ex2_approx(e0), p1 = ex2_approx(e1);
-              lacc = add2(lacc, pack2(p0, p1));
-              pk[c >> 1] = pack_bf16x2(p0, p1);
-            }
-            tmem_st16(tl + s_col + ch * 16, pk);
-          }
-        }
-        {
-          float l0, l1;
-          unpack2(lacc, l0, l1);
-          l += l0 + l1;
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&bars->p_full[qt]);
-          if (SPARSE) mbar_arrive(&bars->meta_empty[ms]);
-        }
-      }
-      if (!ok) break;
-      // epilogue: O / l and the LSE; O's TMEM columns are released as soon as read
-      if (!warp_wait(&bars->o_full[qt], n & 1, abort_flag)) {
-        if (lane == 0) fail(SITE_ATTN_EPILOGUE, 1);
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-      __nv_bfloat16* orow = p.O + (((size_t)x.b * S + q) * p.Hq + jh) * D;
-      uint32_t pk[D / 2];
-#pragma unroll
-      for (int cd = 0; cd < D / 32; ++cd) {
-        uint32_t r[32];
-        tmem_ld32(tl + o_col + cd * 32, r);
-        tmem_wait_ld_dep(r);
-#pragma unroll
-        for (int c = 0; c < 32; c += 2)
-          pk[cd * 16 + (c >> 1)] = pack_bf16x2(__uint_as_float(r[c]) * inv, __uint_as_float(r[c + 1]) * inv);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->o_empty[qt]);
-      if (q <= x.qb1) {
-        uint4* dst = reinterpret_cast<uint4*>(orow);
-#pragma unroll
-        for (int u = 0; u < D / 8; ++u)
-          dst[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-        p.lse[((size_t)x.b * p.Hq + jh) * S + q] =
-            l > 0.0f ? (m_ref * sl2 + __log2f(l)) * 0.69314718055994531f : neg_inf();
-      }
-    }
   } else if (SPARSE) {
     // ------------------------------------------------------------ loaders: warp 2 streams K, warp 3 V
     // Each runs its own sequence of stages, so K tiles run ahead of the V tiles.
@@ -606,6 +439,160 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         if (lane == 0) mbar_arrive(&bars->meta_empty[ms]);
       }
     }
+  
+  }
+  } else {
+    setmaxnreg_inc<kRegsSoftmax>();
+    // ------------------------------------------------------------ softmax
+    const int qt = (warp - 4) >> 2;
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const int p_row = row / G, g = row - p_row * G;
+    const uint32_t tl = tbase + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t s_col = 128 * qt, o_col = 256 + 128 * qt;
+    const float sl2 = p.scale_log2;
+    const uint64_t s2 = pack2(sl2, sl2);
+    bool ok = true;
+    int t = 0, n = 0;
+    for (int it = it0; ok && it < p.nitems; it += dit, ++n) {
+      const Item x = make_item<SPARSE>(p, it);
+      const int q = x.qb0 + qt * P + p_row;
+      const int q_first = x.qb0 + qt * P;
+      const int jh = x.h * G + g;
+      float m_ref = neg_inf(), l = 0.0f;
+      for (int j = 0; j < x.NT; ++j, ++t) {
+        if (!warp_wait(&bars->s_full[qt], t & 1, abort_flag)) {
+          if (lane == 0) fail(SITE_ATTN_SOFTMAX, 1);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int ms = t % kMetaStages;
+        const int2* km = meta + ms * (kKeys + 4);
+        if (SPARSE) {
+          if (!warp_wait(&bars->meta_full[ms], (t / kMetaStages) & 1, abort_flag)) {
+            if (lane == 0) fail(SITE_ATTN_SOFTMAX, 2);
+            ok = false;
+            break;
+          }
+        }
+        const bool diag = !SPARSE && (j * kKeys + kKeys - 1) > q_first;
+        // the whole S row of this thread (128 fp32) in registers; invisible keys -> -inf
+        uint32_t sr[4][32];
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) tmem_ld32(tl + s_col + ch * 32, sr[ch]);
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) tmem_wait_ld_dep(sr[ch]);
+        float mt = neg_inf();
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          bool fast;
+          if (SPARSE) {
+            const int2 sum = km[kKeys + ch];
+            fast = q >= sum.x && q < sum.y;
+          } else {
+            fast = !diag || (j * kKeys + ch * 32 + 31) <= q;
+          }
+          if (!fast) {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              bool visible;
+              if (SPARSE) {
+                const int2 e = km[ch * 32 + c];
+                visible = e.x <= q && q < e.y;
+              } else {
+                visible = j * kKeys + ch * 32 + c <= q;
+              }
+              if (!visible) sr[ch][c] = 0xff800000u;
+            }
+          }
+          mt = fmaxf(mt, max32(sr[ch]));
+        }
+        // lazy rescale of the running max
+        const float m_new = fmaxf(m_ref, mt);
+        const bool need = (m_new - m_ref) * sl2 > kRescaleLog2;  // true when m_ref == -inf and mt finite
+        float alpha = 1.0f;
+        if (need) {
+          alpha = ex2_approx((m_ref - m_new) * sl2);
+          l *= alpha;
+          m_ref = m_new;
+        }
+        if (__any_sync(0xffffffffu, need) && j > 0) {
+          // O of tile j-1 is complete: s_full for tile j was committed after it
+#pragma unroll
+          for (int cd = 0; cd < D / 32; ++cd) {
+            uint32_t r[32];
+            tmem_ld32(tl + o_col + cd * 32, r);
+            tmem_wait_ld_dep(r);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * alpha);
+            tmem_st32(tl + o_col + cd * 32, r);
+          }
+          tmem_wait_st();
+        }
+        // P = exp2(s * scale_log2 - m) as bf16, written over S
+        const float nm = (m_ref == neg_inf()) ? 0.0f : -m_ref * sl2;
+        const uint64_t n2 = pack2(nm, nm);
+        uint64_t lacc = 0;
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            const uint64_t xx = fma2(pack2(__uint_as_float(sr[ch][c]), __uint_as_float(sr[ch][c + 1])), s2, n2);
+            float e0, e1;
+            unpack2(xx, e0, e1);
+            const float p0 = ex2_approx(e0), p1 = ex2_approx(e1);
+            lacc = add2(lacc, pack2(p0, p1));
+            pk[c >> 1] = pack_bf16x2(p0, p1);
+          }
+          tmem_st16(tl + s_col + ch * 16, pk);
+        }
+        {
+          float l0, l1;
+          unpack2(lacc, l0, l1);
+          l += l0 + l1;
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&bars->p_full[qt]);
+          if (SPARSE) mbar_arrive(&bars->meta_empty[ms]);
+        }
+      }
+      if (!ok) break;
+      // epilogue: O / l and the LSE; O's TMEM columns are released as soon as read
+      if (!warp_wait(&bars->o_full[qt], n & 1, abort_flag)) {
+        if (lane == 0) fail(SITE_ATTN_EPILOGUE, 1);
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+      __nv_bfloat16* orow = p.O + (((size_t)x.b * S + q) * p.Hq + jh) * D;
+      uint32_t pk[D / 2];
+#pragma unroll
+      for (int cd = 0; cd < D / 32; ++cd) {
+        uint32_t r[32];
+        tmem_ld32(tl + o_col + cd * 32, r);
+        tmem_wait_ld_dep(r);
+#pragma unroll
+        for (int c = 0; c < 32; c += 2)
+          pk[cd * 16 + (c >> 1)] = pack_bf16x2(__uint_as_float(r[c]) * inv, __uint_as_float(r[c + 1]) * inv);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->o_empty[qt]);
+      if (q <= x.qb1) {
+        uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+        for (int u = 0; u < D / 8; ++u)
+          dst[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        p.lse[((size_t)x.b * p.Hq + jh) * S + q] =
+            l > 0.0f ? (m_ref * sl2 + __log2f(l)) * 0.69314718055994531f : neg_inf();
+      }
+    }
   }
 
   // ------------------------------------------------------------ teardown
@@ -626,6 +613,14 @@ kvpop_status launch(const AttnParams& prm, cudaStream_t stream) {
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::total),
       "kvpop_attn_fwd: smem attribute");
   if (st != KVPOP_OK) return st;
+  // the register re-split must fit in the launch allocation (granule: 8 per thread)
+  cudaFuncAttributes fa;
+  st = cuda_check(cudaFuncGetAttributes(&fa, kern), "kvpop_attn_fwd: attributes");
+  if (st != KVPOP_OK) return st;
+  if (((fa.numRegs + 7) / 8) * 8 < kRegsNeeded) {
+    set_last_error("kvpop_attn_fwd: kernel built with %d registers per thread, %d needed", fa.numRegs, kRegsNeeded);
+    return KVPOP_ERR_INTERNAL;
+  }
   // persistent: one CTA per SM walks the items with a stride of the grid size
   dim3 grid(min(prm.nitems, num_sms()));
   kern<<<grid, kThreads, L::total, stream>>>(prm);
