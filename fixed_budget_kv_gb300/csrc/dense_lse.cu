@@ -2,43 +2,36 @@
 // the dense causal attention; section 2.3: its normaliser LSE_d), the
 // QK^T-only pass behind kvpop_attn_fwd(O = NULL, no mask).
 //
-// One CTA owns four 128-row query tiles of one (batch, KV head) -- 4 x 128/G
-// consecutive positions -- so every K tile fetched from L2 feeds four MMAs.
-// 576 threads: warp 0 TMA producer, warp 1 TMEM allocator and single-thread
-// tcgen05.mma issuer, warps 2-17 four softmax warpgroups (one per query
-// tile, one thread per row = TMEM lane).  Each query tile owns 128 TMEM
-// columns; its warpgroup releases them as soon as the last 32-column chunk
-// has been read, so the tensor core computes the next S of that tile while
-// the warpgroup still sums exponentials.  Per row, l = sum 2^(s*scale*log2e -
-// ref) against a reference that moves only when a chunk would overflow.
+// A pair of CTAs (cluster of 2 on one TPC, tcgen05 cta_group::2) owns four
+// 256-row query tiles of one (batch, KV head): tile u covers 2 x 128/G
+// consecutive positions, CTA r holding the second half's rows when r = 1.
+// Every K tile of 128 keys is split between the pair (64 keys per CTA), so
+// each SM fetches and reads from shared memory half of every K tile, and one
+// M = 256 MMA per query tile computes S for both SMs.  576 threads per CTA:
+// warp 0 TMA producer, warp 1 TMEM allocator and (leader only) the
+// single-thread MMA issuer, warps 2-17 four softmax warpgroups (one per query
+// tile, one thread per row = TMEM lane).  A query tile's 128 TMEM columns are
+// handed back to the issuer as soon as both CTAs have read them, so the tensor
+// core computes the next S of that tile while the warpgroups still sum
+// exponentials.  Per row, l = sum 2^(s*scale*log2e - ref) against a reference
+// that moves only when a chunk would overflow.
 #include "common.cuh"
 
 namespace kvpop {
 namespace {
 
-constexpr int kNQ = 4;  // query tiles per CTA
+constexpr int kNQ = 4;  // query tiles per pair (128 rows of each in each CTA)
 constexpr int kThreads = (2 + 4 * kNQ) * 32;
-constexpr int kKeys = 128;
-constexpr int kBlockBytes = 128 * 128;
+constexpr int kKeys = 128;             // keys per K tile (64 in each CTA)
+constexpr int kBlockBytes = 128 * 128;  // 128 rows x 128 bytes
+constexpr int kHalfBytes = 64 * 128;    // 64 key rows x 128 bytes
 
 struct LseParams {
-  CUtensorMap tq, tk;
+  CUtensorMap tq, tk;  // Q box 64 x G x P, K box 64 x 1 x 64 (half a K tile)
   float* lse;
   int* status;
-  int S, Hq, H, G, P, nqb, nbh;
+  int S, Hq, H, G, P, npb, nbh;
   float scale_log2;
-};
-
-template <int D>
-struct LLayout {
-  static constexpr int DH = D / 64;
-  static constexpr int NS = D == 128 ? 3 : 6;
-  static constexpr int q_off = 0;
-  static constexpr int k_off = q_off + kNQ * DH * kBlockBytes;
-  static constexpr int bar_off = k_off + NS * DH * kBlockBytes;
-  static constexpr int nbar = 1 + 2 * NS + 2 * kNQ + 1;
-  static constexpr int misc_off = bar_off + nbar * 8;
-  static constexpr int total = misc_off + 64 + 1024;
 };
 
 template <int NS>
@@ -49,10 +42,23 @@ struct LBars {
   uint64_t drain;
 };
 
+template <int D>
+struct LLayout {
+  static constexpr int DH = D / 64;
+  static constexpr int NS = D == 128 ? 6 : 12;
+  static constexpr int q_off = 0;
+  static constexpr int k_off = q_off + kNQ * DH * kBlockBytes;
+  static constexpr int bar_off = k_off + NS * DH * kHalfBytes;
+  static constexpr int misc_off = bar_off + (int)sizeof(LBars<NS>);
+  static constexpr int total = misc_off + 64 + 1024;
+  static_assert(total <= 232448, "shared memory");
+};
+
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1) dense_lse_kernel(const __grid_constant__ LseParams p) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    dense_lse_kernel(const __grid_constant__ LseParams p) {
   using L = LLayout<D>;
   constexpr int DH = L::DH;
   constexpr int NS = L::NS;
@@ -64,21 +70,25 @@ __global__ void __launch_bounds__(kThreads, 1) dense_lse_kernel(const __grid_con
   const uint32_t sbase = smem_u32(smem);
 
   const int warp = warp_id(), lane = lane_id();
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
   // heaviest query blocks first across all (batch, head) pairs
-  const int qblock = p.nqb - 1 - (int)(blockIdx.x / p.nbh);
-  const int bh = (int)(blockIdx.x % p.nbh);
+  const int cid = (int)(blockIdx.x >> 1);
+  const int pblock = p.npb - 1 - cid / p.nbh;
+  const int bh = cid % p.nbh;
   const int b = bh / p.H, h = bh % p.H;
   const int S = p.S, G = p.G, P = p.P;
-  const int qb0 = qblock * kNQ * P;
-  int nt[kNQ];  // KV tiles each query tile needs (causal)
+  const int qb0 = pblock * kNQ * 2 * P;
+  int nt[kNQ];  // K tiles each query tile needs (causal, up to the pair's last row)
 #pragma unroll
-  for (int qt = 0; qt < kNQ; ++qt) {
-    const int last = min(qb0 + (qt + 1) * P, S) - 1;
-    nt[qt] = last >= qb0 + qt * P ? last / kKeys + 1 : 0;
+  for (int u = 0; u < kNQ; ++u) {
+    const int first = qb0 + u * 2 * P;
+    const int last = min(first + 2 * P, S) - 1;
+    nt[u] = last >= first ? last / kKeys + 1 : 0;
   }
   int NT = 0;
 #pragma unroll
-  for (int qt = 0; qt < kNQ; ++qt) NT = max(NT, nt[qt]);
+  for (int u = 0; u < kNQ; ++u) NT = max(NT, nt[u]);
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
@@ -88,18 +98,19 @@ __global__ void __launch_bounds__(kThreads, 1) dense_lse_kernel(const __grid_con
     }
     for (int i = 0; i < kNQ; ++i) {
       mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->s_empty[i], 4);
+      mbar_init(&bars->s_empty[i], 8);  // 4 warps in each CTA
     }
     mbar_init(&bars->drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, 512);
-    tmem_relinquish();
+    tmem_alloc_pair(tmem_slot, 512);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
   auto fail = [&](int site, int detail) {
@@ -108,79 +119,86 @@ __global__ void __launch_bounds__(kThreads, 1) dense_lse_kernel(const __grid_con
   };
 
   if (warp == 0) {
+    // both CTAs load their own halves; completion counts on the leader's barriers
     if (lane == 0 && NT > 0) {
       tma_prefetch_desc(&p.tq);
       tma_prefetch_desc(&p.tk);
-      mbar_arrive_expect_tx(&bars->q_full, kNQ * DH * kBlockBytes);
-      for (int qt = 0; qt < kNQ; ++qt)
+      const uint32_t q_bar = cluster_addr(smem_u32(&bars->q_full), 0);
+      if (leader) mbar_arrive_expect_tx(&bars->q_full, 2 * kNQ * DH * kBlockBytes);
+      for (int u = 0; u < kNQ; ++u)
         for (int dh = 0; dh < DH; ++dh)
-          tma_load_4d(smem + L::q_off + (qt * DH + dh) * kBlockBytes, &p.tq, &bars->q_full, dh * 64,
-                      h * G, qb0 + qt * P, b);
+          tma_load_4d_pair(smem + L::q_off + (u * DH + dh) * kBlockBytes, &p.tq, q_bar, dh * 64, h * G,
+                           qb0 + u * 2 * P + (int)rank * P, b);
       for (int j = 0; j < NT; ++j) {
         const int st = j % NS;
         if (!mbar_wait(&bars->k_empty[st], ((j / NS) & 1) ^ 1, abort_flag)) {
           fail(SITE_ATTN_PRODUCER, 21);
           break;
         }
-        mbar_arrive_expect_tx(&bars->k_full[st], DH * kBlockBytes);
+        if (leader) mbar_arrive_expect_tx(&bars->k_full[st], 2 * DH * kHalfBytes);
+        const uint32_t k_bar = cluster_addr(smem_u32(&bars->k_full[st]), 0);
         for (int dh = 0; dh < DH; ++dh)
-          tma_load_4d(smem + L::k_off + (st * DH + dh) * kBlockBytes, &p.tk, &bars->k_full[st], dh * 64,
-                      h, j * kKeys, b);
+          tma_load_4d_pair(smem + L::k_off + (st * DH + dh) * kHalfBytes, &p.tk, k_bar, dh * 64, h,
+                           j * kKeys + (int)rank * 64, b);
       }
     }
   } else if (warp == 1) {
     if (lane == 0 && NT > 0) {
-      bool ok = mbar_wait(&bars->q_full, 0, abort_flag);
-      if (!ok) fail(SITE_ATTN_MMA, 21);
-      tc_fence_after();
-      constexpr uint32_t idesc = idesc_bf16(128, 128, 0);
-      const uint32_t q_addr = sbase + L::q_off, k_addr = sbase + L::k_off;
-      for (int j = 0; ok && j < NT; ++j) {
-        const int st = j % NS;
-        if (!mbar_wait(&bars->k_full[st], (j / NS) & 1, abort_flag)) {
-          fail(SITE_ATTN_MMA, 22);
-          break;
-        }
+      if (leader) {
+        bool ok = mbar_wait(&bars->q_full, 0, abort_flag);
+        if (!ok) fail(SITE_ATTN_MMA, 21);
         tc_fence_after();
-        for (int qt = 0; qt < kNQ; ++qt) {
-          if (j >= nt[qt]) continue;
-          if (!mbar_wait(&bars->s_empty[qt], (j & 1) ^ 1, abort_flag)) {
-            fail(SITE_ATTN_MMA, 23);
-            ok = false;
+        constexpr uint32_t idesc = idesc_bf16(256, 128, 0);
+        const uint32_t q_addr = sbase + L::q_off, k_addr = sbase + L::k_off;
+        for (int j = 0; ok && j < NT; ++j) {
+          const int st = j % NS;
+          if (!mbar_wait(&bars->k_full[st], (j / NS) & 1, abort_flag)) {
+            fail(SITE_ATTN_MMA, 22);
             break;
           }
           tc_fence_after();
+          for (int u = 0; u < kNQ; ++u) {
+            if (j >= nt[u]) continue;
+            if (!mbar_wait(&bars->s_empty[u], (j & 1) ^ 1, abort_flag)) {
+              fail(SITE_ATTN_MMA, 23);
+              ok = false;
+              break;
+            }
+            tc_fence_after();
 #pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const int dh = ks >> 2;
-            const uint32_t w32 = (uint32_t)(ks & 3) * 32;
-            const uint64_t a = smem_desc_sw128(q_addr + (qt * DH + dh) * kBlockBytes + w32, 16, 1024);
-            const uint64_t bd = smem_desc_sw128(k_addr + (st * DH + dh) * kBlockBytes + w32, 16, 1024);
-            mma_ss(tbase + 128 * qt, a, bd, idesc, ks > 0 ? 1u : 0u);
+            for (int ks = 0; ks < D / 16; ++ks) {
+              const int dh = ks >> 2;
+              const uint32_t w32 = (uint32_t)(ks & 3) * 32;
+              const uint64_t a = smem_desc_sw128(q_addr + (u * DH + dh) * kBlockBytes + w32, 16, 1024);
+              const uint64_t bd = smem_desc_sw128(k_addr + (st * DH + dh) * kHalfBytes + w32, 16, 1024);
+              mma_ss_pair(tbase + 128 * u, a, bd, idesc, ks > 0 ? 1u : 0u);
+            }
+            mma_commit_pair(&bars->s_full[u]);
           }
-          mma_commit(&bars->s_full[qt]);
+          mma_commit_pair(&bars->k_empty[st]);
         }
-        mma_commit(&bars->k_empty[st]);
+        mma_commit_pair(&bars->drain);
       }
-      mma_commit(&bars->drain);
+      // both CTAs: every pair MMA has finished with this CTA's memory
       mbar_wait(&bars->drain, 0, nullptr);
     }
   } else {
     // softmax warpgroups: warps 2-5 -> tile 0, 6-9 -> tile 1, ...
-    const int qt = (warp - 2) >> 2;
+    const int u = (warp - 2) >> 2;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const int p_row = row / G, g = row - p_row * G;
-    const int q = qb0 + qt * P + p_row;
-    const int q_first = qb0 + qt * P;
-    const uint32_t tl = tbase + ((uint32_t)(quarter * 32) << 16) + 128 * qt;
+    const int q_first = qb0 + u * 2 * P + (int)rank * P;
+    const int q = q_first + p_row;
+    const uint32_t tl = tbase + ((uint32_t)(quarter * 32) << 16) + 128 * u;
+    const uint32_t empty_bar = cluster_addr(smem_u32(&bars->s_empty[u]), 0);
     const float sl2 = p.scale_log2;
     const uint64_t s2 = pack2(sl2, sl2);
     float m_ref = neg_inf(), l = 0.0f;
     bool ok = true;
-    const int ntq = nt[qt];
+    const int ntq = nt[u];
     for (int j = 0; j < ntq; ++j) {
-      if (!warp_wait(&bars->s_full[qt], j & 1, abort_flag)) {
+      if (!warp_wait(&bars->s_full[u], j & 1, abort_flag)) {
         if (lane == 0) fail(SITE_ATTN_SOFTMAX, 21);
         ok = false;
         break;
@@ -199,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1) dense_lse_kernel(const __grid_con
         } else {  // every column of this tile is in registers: hand TMEM back
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&bars->s_empty[qt]);
+          if (lane == 0) mbar_arrive_cluster(empty_bar);
         }
         if (diag) {
           const int t0 = j * kKeys + ch * 32;
@@ -227,12 +245,13 @@ __global__ void __launch_bounds__(kThreads, 1) dense_lse_kernel(const __grid_con
           l > 0.0f ? (m_ref * sl2 + __log2f(l)) * 0.69314718055994531f : neg_inf();
   }
 
+  // neither CTA releases its tensor or shared memory while the pair still works
   tc_fence_before();
   __syncthreads();
+  cluster_sync();
   if (warp == 1) {
-    __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tbase, 512);
+    tmem_dealloc_pair(tbase, 512);
   }
 }
 
@@ -244,7 +263,7 @@ kvpop_status launch_d(const LseParams& prm, cudaStream_t cs) {
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::total),
       "dense LSE: smem attribute");
   if (st != KVPOP_OK) return st;
-  kern<<<prm.nqb * prm.nbh, kThreads, L::total, cs>>>(prm);
+  kern<<<2 * prm.npb * prm.nbh, kThreads, L::total, cs>>>(prm);
   return cuda_check(cudaGetLastError(), "dense LSE: launch");
 }
 
@@ -261,7 +280,7 @@ kvpop_status launch_dense_lse(const void* q, const void* k, int b, int S, int Hq
   uint32_t bq[4] = {64, (uint32_t)G, (uint32_t)P, 1};
   uint64_t dk[4] = {(uint64_t)D, (uint64_t)H, (uint64_t)S, (uint64_t)b};
   uint64_t sk[3] = {(uint64_t)D * 2, (uint64_t)H * D * 2, (uint64_t)S * H * D * 2};
-  uint32_t bk[4] = {64, 1, 128, 1};
+  uint32_t bk[4] = {64, 1, 64, 1};
   if (!make_tmap_4d(&prm.tq, q, dq, sq, bq) || !make_tmap_4d(&prm.tk, k, dk, sk, bk)) return KVPOP_ERR_CUDA;
   prm.lse = lse;
   prm.status = device_status_ptr();
@@ -270,10 +289,10 @@ kvpop_status launch_dense_lse(const void* q, const void* k, int b, int S, int Hq
   prm.H = H;
   prm.G = G;
   prm.P = P;
-  prm.nqb = (S + kNQ * P - 1) / (kNQ * P);
+  prm.npb = (S + kNQ * 2 * P - 1) / (kNQ * 2 * P);
   prm.nbh = b * H;
   prm.scale_log2 = scale_log2;
-  if ((long long)prm.nqb * prm.nbh > 0x7fffffffLL) {
+  if (2LL * prm.npb * prm.nbh > 0x7fffffffLL) {
     set_last_error("dense LSE: grid too large");
     return KVPOP_ERR_UNSUPPORTED;
   }
