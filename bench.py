@@ -35,6 +35,22 @@ LAUNCHES_STEP = LAUNCHES_MASK + 1 + 1 + 3  # + sparse attention, dense LSE, targ
 LAUNCHES_DECODE_STEP = 2
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest per-rank value of x over the process group (x itself on one rank)."""
+    if world == 1:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, world: int, step_ms_max: float) -> float:
+    """Whole-job rate: every rank processes `units_per_rank` per step; the job's
+    step ends when the slowest rank's does."""
+    return world * units_per_rank / (step_ms_max / 1e3)
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -196,12 +212,8 @@ def run_gpu(args, rank, world, local_rank):
     if st != 0:
         raise RuntimeError(f"device status after timing: {words}")
 
-    t = torch.tensor([step_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    step_ms_max = float(t.item())
-    tokens = b * S
-    value = world * tokens / (step_ms_max / 1e3)
+    step_ms_max = max_over_ranks(step_ms, world, dev)
+    value = job_throughput(b * S, world, step_ms_max)
 
     flops = prefill_flops(wl)
     pk = peaks()
@@ -236,7 +248,7 @@ def run_gpu(args, rank, world, local_rank):
     if not args.no_e2e:
         result["e2e"] = e2e(args, wl, q, k, v, prio, ws_mask, ws_tgt, dev, world)
     if not args.no_decode:
-        result["decode"] = run_decode(args, dev, pk)
+        result["decode"] = run_decode(args, dev, pk, world)
         result["gpu_launches"] += LAUNCHES_DECODE_STEP * result["decode"]["steps"]
     del q, k, v, O
     return result
@@ -278,18 +290,14 @@ def e2e(args, wl, q, k, v, prio, ws_mask, ws_tgt, dev, world):
         step()
     e1.record()
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / n
-    t = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1) / n, world, dev)
     h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hp))
     d2h = hO.numel() * hO.element_size() + ht.numel() * ht.element_size()
-    return {"value": round(world * b * S / (ms / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
+    return {"value": round(job_throughput(b * S, world, ms), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": n}
 
 
-def run_decode(args, dev, pk):
+def run_decode(args, dev, pk, world=1):
     import torch
     from fixed_budget_kv_gb300 import kvpop, synth
     wl = synth.DECODE
@@ -313,18 +321,20 @@ def run_decode(args, dev, pk):
         cache.step(qn[i], kn[i], vn[i], pn[i], out=(O, lse, evd))
     cache.prefill(kp, vp, pp, ev)
     torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for i in range(steps):
         cache.step(qn[i], kn[i], vn[i], pn[i], out=(O, lse, evd))
     e1.record()
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / steps
+    ms = max_over_ranks(e0.elapsed_time(e1) / steps, world, dev)
     cache.close()
     bytes_step = n * H * wl.B * D * 2 * 2
     gbs = bytes_step / (ms / 1e3) / 1e9
     return {"workload": wl.name, "sequences": n, "budget": {"s": wl.s, "w": wl.w, "k": wl.k}, "prefix": P,
-            "steps": steps, "us_per_step": round(ms * 1e3, 2), "value": round(n / (ms / 1e3), 1),
+            "steps": steps, "us_per_step": round(ms * 1e3, 2), "value": round(job_throughput(n, world, ms), 1),
             "unit": "tokens/s",
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                          "frac": round(gbs / pk["hbm_gbs"], 4), "traffic": None,
