@@ -33,6 +33,10 @@ METRIC = "prefill tokens/s (sparse attn + future target) & decode tokens/s; % of
 LAUNCHES_MASK = 4 * 3 + 1 + 1 + 1 + 2   # radix passes, wavelet, tau, evict_at, lists
 LAUNCHES_STEP = LAUNCHES_MASK + 1 + 1 + 3  # + sparse attention, dense LSE, target (prep, kernel, log)
 LAUNCHES_DECODE_STEP = 2
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum, one ncu
+# capture of `bench.py --only <pass>` on a GB300) for the kernels as they stand;
+# decode: update + attention of one step
+TRAFFIC_BYTES = {"sparse_attn": 322.46e6, "dense_lse": 173.46e6, "future_target": 170.12e6, "decode": 558.19e6}
 
 
 def max_over_ranks(x: float, world: int, device) -> float:
@@ -62,6 +66,9 @@ def parse():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--only", choices=["mask", "sparse", "dense", "target", "decode"],
+                    help="for a profiler: set up the workload, run that pass twice (decode: 24 steps), "
+                         "print one status line and exit")
     return ap.parse_args()
 
 
@@ -238,7 +245,8 @@ def run_gpu(args, rank, world, local_rank):
         "passes_ms": passes,
         "roofline": {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1),
                      "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                     "frac": round(achieved / pk["bf16_tflops_sustained"], 4), "traffic": None,
+                     "frac": round(achieved / pk["bf16_tflops_sustained"], 4),
+                     "traffic": TRAFFIC_BYTES.get(dom),
                      "peak_kind": f"bf16 sustained, {pk['source']}",
                      "algorithmic_flops_per_launch": flops[dom]},
         "gpu_launches": LAUNCHES_STEP * args.steps,
@@ -337,7 +345,7 @@ def run_decode(args, dev, pk, world=1):
             "steps": steps, "us_per_step": round(ms * 1e3, 2), "value": round(job_throughput(n, world, ms), 1),
             "unit": "tokens/s",
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                         "frac": round(gbs / pk["hbm_gbs"], 4), "traffic": None,
+                         "frac": round(gbs / pk["hbm_gbs"], 4), "traffic": TRAFFIC_BYTES["decode"],
                          "algorithmic_bytes_per_step": bytes_step,
                          "note": "whole step (update + split attention + combine) timed with CUDA events"}}
 
@@ -401,6 +409,57 @@ def cpu_sample(wl, seed=0, nrows=8192, nkeys=512):
     return 1.0 / per_token, sample
 
 
+def run_only(args):
+    """One pass of the hot path on the default workload, for ncu captures."""
+    import torch
+    from fixed_budget_kv_gb300 import kvpop, synth
+
+    import __graft_entry__
+    __graft_entry__.build()
+    dev = torch.device("cuda", 0)
+    if args.only == "decode":
+        wl = synth.DECODE
+        n, H, G, D, P = wl.n, wl.H, wl.G, wl.D, wl.P
+        kp = synth.normal_bf16_torch(wl.seed, synth.K, (n, P, H, D), dev)
+        vp = synth.normal_bf16_torch(wl.seed, synth.V, (n, P, H, D), dev)
+        pp = torch.from_numpy(synth.priorities("uniform", wl.seed, (n, H, P))).to(dev)
+        _, _, ev, _ = kvpop.mask(pp, wl.s, wl.w, wl.k, lists=False)
+        cache = kvpop.Cache(n, H, G, D, wl.s, wl.w, wl.k)
+        cache.prefill(kp, vp, pp, ev)
+        del kp, vp
+        steps = 24
+        qn = synth.normal_bf16_torch(wl.seed, synth.QN, (steps, n, wl.Hq, D), dev)
+        kn = synth.normal_bf16_torch(wl.seed, synth.KN, (steps, n, H, D), dev)
+        vn = synth.normal_bf16_torch(wl.seed, synth.VN, (steps, n, H, D), dev)
+        pn = torch.from_numpy(synth.priorities("uniform", wl.seed, (steps, n, H), stream=synth.PRION)).to(dev)
+        for i in range(steps):
+            cache.step(qn[i], kn[i], vn[i], pn[i])
+        torch.cuda.synchronize()
+        cache.close()
+    else:
+        wl = synth.PREFILL_WORKLOADS[args.workload]
+        q, k, v, prio = synth.make_prefill_device(wl, dev)
+        bud = (wl.s, wl.w, wl.k)
+        if args.only in ("sparse", "mask"):
+            _, _, ev, lists = kvpop.mask(prio, *bud)
+        if args.only in ("dense", "target"):
+            _, lse_d = kvpop.attn_fwd(q, k, None, 0.0, want_o=False)
+        for _ in range(2):
+            if args.only == "mask":
+                kvpop.mask(prio, *bud)
+            elif args.only == "sparse":
+                kvpop.attn_fwd(q, k, v, 0.0, ev, lists, bud)
+            elif args.only == "dense":
+                kvpop.attn_fwd(q, k, None, 0.0, want_o=False)
+            else:
+                kvpop.future_target(q, k, lse_d, wl.w)
+        torch.cuda.synchronize()
+    st, words = kvpop.device_status(reset=True)
+    print(json.dumps({"only": args.only, "device_status": words}), flush=True)
+    if st != 0:
+        raise SystemExit(1)
+
+
 def run_reference(args):
     """The reference arm: the fp64 oracle on the host cores, one bounded sample per step."""
     from fixed_budget_kv_gb300 import synth
@@ -436,6 +495,9 @@ def main():
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args)), flush=True)
+        return
+    if args.only:
+        run_only(args)
         return
     # the CPU baseline runs before the first CUDA call (the oracle uses OpenMP threads)
     cpu = None
