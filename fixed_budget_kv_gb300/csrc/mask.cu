@@ -15,7 +15,8 @@
 //      answers every q independently in log2(S) steps.
 //   3. evict_at: tau is non-increasing in q, so the first row that drops t is a
 //      binary search for the first q >= t + w with tau_q < rank[t].
-//   4. lists: the long-range keys retained at rows 64 i, in position order,
+//   4. lists: the long-range keys retained at rows 64 i as (position,
+//      evict_at) pairs -- those held through the whole 64-row block first --
 //      from group base lists (every 16 lists) plus the tokens that became
 //      eligible since.
 #include <cooperative_groups.h>
