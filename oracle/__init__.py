@@ -13,7 +13,9 @@ Every function restates a definition from the KVpop pages:
   * softmax attention and its log-sum-exp -- "KVpop ... 精读笔记", section 2.3;
   * future-attention mass and Eq. (8) -- "KVpop ... 精读笔记", sections 2.2-2.3;
   * decode-time eviction at the window boundary -- "KVpop ... 精读笔记",
-    section 2.4 (token u = q - w leaves the window) and section 2.3.
+    section 2.4 (token u = q - w leaves the window) and section 2.3;
+  * normalised target r_t, decayed scores, teacher boundary labels and the
+    pairwise boundary loss -- "KVpop ... 精读笔记", section 2.2.
 Readings where the pages are silent are listed in the header of ``oracle.c``.
 
 Pins: every function here is checked by ``tests/test_oracle_pins.py`` against
@@ -38,7 +40,8 @@ _lib = None
 def build(force: bool = False) -> str:
     """Compile oracle.c with gcc (fp64, OpenMP)."""
     if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
-        cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11", "-o", _SO, _SRC, "-lm"]
+        cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11", "-ffp-contract=off", "-o", _SO, _SRC,
+               "-lm"]
         subprocess.check_call(cmd)
     return _SO
 
@@ -61,6 +64,10 @@ def _load():
                                           P, i64, P, P]
         _lib.oracle_target_lse.argtypes = [P, P, P, i32, i32, i32, i32, i32, f64, i32, P, i64, P]
         _lib.oracle_target_colsum.argtypes = [P, P, i32, i32, i32, i32, i32, f64, i32, P]
+        _lib.oracle_target_normalize.argtypes = [P, i64, i32, i32, i32, f64, P]
+        _lib.oracle_teacher_labels.argtypes = [P, i32, i32, i32, i32, i32, ctypes.c_float, P, P]
+        _lib.oracle_boundary_loss.argtypes = [P, P, P, P, i64, i32, i32, i32, i32, P, f64, P, P]
+        _lib.oracle_boundary_loss.restype = i64
         _lib.oracle_num_threads.restype = i32
     return _lib
 
@@ -299,3 +306,51 @@ def _row_positions(rank_1d, tau_1d, s, w, q):
     t = np.arange(q + 1)
     keep = (t < s) | (q - t < w) | ((t >= s) & (t <= q - w) & (rank_1d[: q + 1] <= tau_1d[q]))
     return t[keep]
+
+
+# ----------------------------------------------------------------------------
+# normalised target, teacher boundary labels, pairwise boundary loss
+# ----------------------------------------------------------------------------
+
+def target_normalize(target: np.ndarray, G: int, w: int, eps: float) -> np.ndarray:
+    """r_t = log(eps + (1/G) sum_g (1/N_t) sum_{d>=t+w} A_{d,t}) from the
+    unnormalised log target [..., S]; N_t = S - t - w; no future -> log(eps)."""
+    t = np.ascontiguousarray(target, dtype=np.float64)
+    S = t.shape[-1]
+    out = np.empty_like(t)
+    _load().oracle_target_normalize(_p(t), t.size // S, S, G, w, float(eps), _p(out))
+    return out
+
+
+def teacher_labels(r_tgt: np.ndarray, s: int, w: int, k: int, n: int, log_gamma):
+    """(t_bnd, y) per row q for targets [b, H, S] (fp32) and log_gamma [H] (fp32):
+    the teacher's top-k of E(q) under the decayed target, the cutoff t_bnd that the
+    leaving token q - w has to beat, and y = +1 kept / -1 dropped / 0 no leaving token."""
+    r = np.ascontiguousarray(r_tgt, dtype=np.float32)
+    b, H, S = r.shape
+    lg = np.asarray(log_gamma, dtype=np.float32).reshape(H)
+    tb = np.empty((b, H, S), dtype=np.int32)
+    y = np.empty((b, H, S), dtype=np.int32)
+    lib = _load()
+    for bi in range(b):
+        for h in range(H):
+            lib.oracle_teacher_labels(_p(r[bi, h]), S, s, w, k, n, ctypes.c_float(lg[h]), _p(tb[bi, h]),
+                                      _p(y[bi, h]))
+    return tb, y
+
+
+def boundary_loss(r_hat: np.ndarray, t_bnd: np.ndarray, y: np.ndarray, w: int, n: int, log_gamma,
+                  tau: float, omega=None):
+    """Mean pairwise logistic loss over the labelled rows and its gradient
+    d loss / d r_hat, [b, H, S]; returns (loss, grad, number of pairs)."""
+    rh = np.ascontiguousarray(r_hat, dtype=np.float32)
+    b, H, S = rh.shape
+    tb = np.ascontiguousarray(t_bnd, dtype=np.int32)
+    yy = np.ascontiguousarray(y, dtype=np.int32)
+    lg = np.ascontiguousarray(np.asarray(log_gamma, dtype=np.float32).reshape(H))
+    om = None if omega is None else np.ascontiguousarray(omega, dtype=np.float32)
+    grad = np.empty((b, H, S), dtype=np.float64)
+    loss = ctypes.c_double()
+    pairs = _load().oracle_boundary_loss(_p(rh), _p(tb), _p(yy), None if om is None else _p(om), b * H, S, H,
+                                         w, n, _p(lg), float(tau), ctypes.byref(loss), _p(grad))
+    return loss.value, grad, int(pairs)

@@ -342,6 +342,143 @@ void oracle_target_colsum(const float* q, const float* k, int b, int S, int H, i
     }
 }
 
+/* ------------------------------------------------------------------------ */
+/* normalised target, teacher boundary labels, pairwise boundary loss        */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * [KVpop notes] 2.2: m_t^g = (1/N_t) sum_{d=t+w}^{S-1} A_{d,t}^g and
+ * r_t = log(eps + (1/G) sum_g m_t^g), with N_t = S - t - w future queries.
+ * Input: the unnormalised target log sum_g sum_d A (fp64), [nbh, S].
+ * A key with no future query (N_t <= 0) has mass 0: r = log(eps).
+ */
+void oracle_target_normalize(const double* target, int64_t nbh, int S, int G, int w, double eps,
+                             double* r) {
+    for (int64_t i = 0; i < nbh * (int64_t)S; ++i) {
+        int t = (int)(i % S);
+        int nt = S - t - w;
+        double mass = nt > 0 ? exp(target[i]) / ((double)G * nt) : 0.0;
+        double x = eps + mass;
+        r[i] = x > 0.0 ? log(x) : -INFINITY;
+    }
+}
+
+/* effective (decayed) score of token t at row q, [KVpop notes] 2.2:
+ * r_t + floor((q - t) / n) * log_gamma, in fp32 with one rounding after the
+ * product and one after the sum; NaN counts as -inf */
+static float decayed(float r, int q, int t, int n, float lg) {
+    float m = (float)((q - t) / n);
+    float dec = m * lg;
+    float sc = r + dec;
+    return isnan(sc) ? -INFINITY : sc;
+}
+
+typedef struct {
+    float v;
+    int32_t idx;
+} fkeyed_t;
+
+/* (score desc, index asc) */
+static int cmp_fkeyed(const void* a, const void* b) {
+    const fkeyed_t* x = (const fkeyed_t*)a;
+    const fkeyed_t* y = (const fkeyed_t*)b;
+    if (x->v > y->v) return -1;
+    if (x->v < y->v) return 1;
+    return (x->idx > y->idx) - (x->idx < y->idx);
+}
+
+/*
+ * Teacher boundary labels, [KVpop notes] 2.2: at row q the token
+ * t_new = q - w leaves the window; the teacher ranks E(q) = {s..q-w} by the
+ * decayed target score (ties: lower index first) and keeps its top k.
+ *   t_bnd[q] = the k-th best token of E(q) minus t_new (the cutoff t_new has to
+ *              beat; it is the lowest-scoring member of the teacher top-k whenever
+ *              t_new is dropped); -1 if fewer than k other tokens;
+ *   y[q]     = +1 if t_new is in the teacher top-k, -1 if not;
+ *   rows without a leaving token (q - w < s) get y = 0, t_bnd = -1.
+ * Sorting E(q) explicitly for every row: O(S^2 log S).
+ */
+void oracle_teacher_labels(const float* r, int S, int s, int w, int k, int n, float lg, int32_t* t_bnd,
+                           int32_t* y) {
+#pragma omp parallel
+    {
+        fkeyed_t* buf = (fkeyed_t*)malloc(sizeof(fkeyed_t) * (size_t)(S > 0 ? S : 1));
+#pragma omp for schedule(dynamic, 16)
+        for (int q = 0; q < S; ++q) {
+            int tn = q - w;
+            if (tn < s) {
+                t_bnd[q] = -1;
+                y[q] = 0;
+                continue;
+            }
+            int m = 0;
+            for (int t = s; t < tn; ++t) {
+                buf[m].v = decayed(r[t], q, t, n, lg);
+                buf[m].idx = t;
+                ++m;
+            }
+            if (k == 0) {
+                t_bnd[q] = -1;
+                y[q] = -1;
+                continue;
+            }
+            if (m < k) {
+                t_bnd[q] = -1;
+                y[q] = 1;
+                continue;
+            }
+            qsort(buf, (size_t)m, sizeof(fkeyed_t), cmp_fkeyed);
+            fkeyed_t me = {decayed(r[tn], q, tn, n, lg), tn};
+            t_bnd[q] = buf[k - 1].idx;
+            y[q] = cmp_fkeyed(&me, &buf[k - 1]) < 0 ? 1 : -1;
+        }
+        free(buf);
+    }
+}
+
+static double softplus(double z) { return z > 0.0 ? z + log1p(exp(-z)) : log1p(exp(z)); }
+static double sigmoid(double z) { return z >= 0.0 ? 1.0 / (1.0 + exp(-z)) : exp(z) / (1.0 + exp(z)); }
+
+/*
+ * Pairwise boundary loss, [KVpop notes] 2.2:
+ *   L = mean over rows q with y[q] != 0 and t_bnd[q] >= 0 of
+ *       omega[q] * softplus(-y[q] * (rh_new(q) - rh_bnd(q)) / tau),
+ *   rh_t(q) = rhat[t] + floor((q - t) / n) * log_gamma[h]  (the decay applies to the
+ *   predicted scores as to the targets), t_new = q - w.
+ * rhat, omega (NULL = 1), t_bnd, y: [nbh, S] with h = row index mod H.
+ * grad [nbh, S] = dL / drhat.  Returns the number of pairs; *loss = 0 when none.
+ */
+int64_t oracle_boundary_loss(const float* rhat, const int32_t* t_bnd, const int32_t* y, const float* omega,
+                             int64_t nbh, int S, int H, int w, int n, const float* lg, double tau,
+                             double* loss, double* grad) {
+    int64_t pairs = 0;
+    double sum = 0.0;
+    for (int64_t i = 0; i < nbh * (int64_t)S; ++i) grad[i] = 0.0;
+    for (int64_t bh = 0; bh < nbh; ++bh) {
+        double l = (double)lg[bh % H];
+        const float* rr = rhat + bh * S;
+        for (int q = 0; q < S; ++q) {
+            int64_t iq = bh * S + q;
+            int tb = t_bnd[iq], yy = y[iq];
+            if (yy == 0 || tb < 0) continue;
+            int tn = q - w;
+            double dn = (double)rr[tn] + (double)((q - tn) / n) * l;
+            double db = (double)rr[tb] + (double)((q - tb) / n) * l;
+            double z = -(double)yy * (dn - db) / tau;
+            double om = omega ? (double)omega[iq] : 1.0;
+            sum += om * softplus(z);
+            double g = om * sigmoid(z) * (-(double)yy / tau);
+            grad[bh * S + tn] += g;
+            grad[bh * S + tb] -= g;
+            ++pairs;
+        }
+    }
+    if (pairs > 0)
+        for (int64_t i = 0; i < nbh * (int64_t)S; ++i) grad[i] /= (double)pairs;
+    *loss = pairs > 0 ? sum / (double)pairs : 0.0;
+    return pairs;
+}
+
 int oracle_num_threads(void) {
 #ifdef _OPENMP
     extern int omp_get_max_threads(void);

@@ -398,3 +398,141 @@ def test_generator_matches_scalar_definition():
     x = np.array([1.0, 1.00390625, 1.01171875, -2.5, 3.0e-3], np.float32)
     b = synth.f32_to_bf16_bits(x)
     assert synth.bf16_bits_to_f32(b).tolist() == [1.0, 1.0, 1.015625, -2.5, np.float32(0.0030059814453125)]
+
+
+# ----------------------------------------------------------------------------
+# normalised target, teacher boundary labels, pairwise boundary loss
+# ("KVpop ... 精读笔记", section 2.2)
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("eps", [0.0, 1e-6])
+def test_target_normalize_zero_queries_closed_form(oracle_mod, eps):
+    """q = 0: A_{d,t} = 1/(d+1) for every head, so (1/G) sum_g m_t = (1/N_t) sum_{d=t+w}^{S-1} 1/(d+1)
+    with N_t = S - t - w; no future query -> log(eps)."""
+    S, H, G, D, w = 60, 1, 3, 8, 4
+    q, k, _, _ = _tiny_inputs(S, H, G, D, seed=5)
+    q[:] = 0
+    _, lse = oracle_mod.attn(q, k, k, 1.0, want_o=False)
+    r = oracle_mod.target_normalize(oracle_mod.target_lse(q, k, lse, w, 1.0), G, w, eps)
+    for t in range(S):
+        nt = S - t - w
+        if nt <= 0:
+            assert (np.isneginf(r[0, 0, t]) if eps == 0 else r[0, 0, t] == math.log(eps))
+        else:
+            ref = math.log(eps + sum(1.0 / (d + 1) for d in range(t + w, S)) / nt)
+            assert abs(r[0, 0, t] - ref) < 1e-12
+
+
+def test_teacher_labels_hand_example(oracle_mod):
+    f = _read_fixture("hand_labels_example.txt")
+    S, s, w, k, n = (int(f[x][0]) for x in ("S", "s", "w", "k", "n"))
+    r = np.array([float(v) for v in f["r"]], np.float32).reshape(1, 1, S)
+    tb, y = oracle_mod.teacher_labels(r, s, w, k, n, [float(f["log_gamma"][0])])
+    assert tb.ravel().tolist() == [int(v) for v in f["t_bnd"]]
+    assert y.ravel().tolist() == [int(v) for v in f["y"]]
+
+
+@pytest.mark.parametrize("s,w,k", [(2, 3, 4), (0, 0, 5), (3, 7, 1), (1, 2, 0), (0, 5, 200)])
+def test_teacher_labels_without_decay_follow_the_mask(oracle_mod, s, w, k):
+    """No decay (log_gamma = 0, or a step n beyond S): the teacher keeps the mask's
+    retained set, so t_new = q - w is kept at row q exactly when q < evict_at[t_new];
+    a dropped t_new faces the token of rank tau_q, and a kept one displaces the token
+    evicted at row q (evict_at == q), if any."""
+    rng = np.random.default_rng(11 + s + w + k)
+    S = 300
+    for prio in _prio_cases(rng, S):
+        rk, tau, ev = oracle_mod.mask(prio.reshape(1, 1, S), s, w, k)
+        for lg, n in ((0.0, 1), (-0.5, S + 1)):
+            tb, y = oracle_mod.teacher_labels(prio.reshape(1, 1, S), s, w, k, n, [lg])
+            tb, y = tb[0, 0], y[0, 0]
+            for q in range(S):
+                tn = q - w
+                if tn < s:
+                    assert y[q] == 0 and tb[q] == -1
+                    continue
+                kept = q < ev[0, 0, tn]
+                assert y[q] == (1 if kept else -1), (q, lg)
+                if k == 0:
+                    assert tb[q] == -1
+                elif not kept:
+                    assert rk[0, 0, tb[q]] == tau[0, 0, q]
+                elif tb[q] >= 0:
+                    assert ev[0, 0, tb[q]] == q
+                else:
+                    assert tn - s < k            # fewer than k other eligible tokens
+
+
+def test_teacher_labels_strong_decay_keeps_the_youngest(oracle_mod):
+    """n = 1 and a decay far larger than the spread of r: younger always wins, so the
+    leaving token is kept and the cutoff is the k-th youngest other token, q - w - k."""
+    S, s, w, k = 200, 3, 5, 7
+    r = np.random.default_rng(4).standard_normal((1, 2, S)).astype(np.float32)
+    tb, y = oracle_mod.teacher_labels(r, s, w, k, 1, [-1e6, -2e6])
+    for h in range(2):
+        for q in range(S):
+            tn = q - w
+            if tn < s:
+                assert y[0, h, q] == 0
+            else:
+                assert y[0, h, q] == 1
+                assert tb[0, h, q] == (q - w - k if tn - s >= k else -1)
+
+
+def _label_case(oracle_mod, seed, b=2, H=2, S=160, s=2, w=6, k=9, n=4):
+    rng = np.random.default_rng(seed)
+    r = rng.standard_normal((b, H, S)).astype(np.float32)
+    lg = np.log(np.array([0.9, 0.7][:H], np.float32)).astype(np.float32)
+    tb, y = oracle_mod.teacher_labels(r, s, w, k, n, lg)
+    return rng, tb, y, lg
+
+
+def test_boundary_loss_gradient_is_the_derivative(oracle_mod):
+    """Central differences of the loss match the returned gradient."""
+    rng, tb, y, lg = _label_case(oracle_mod, 8)
+    b, H, S = tb.shape
+    rh = rng.standard_normal((b, H, S)).astype(np.float32)
+    om = rng.random((b, H, S)).astype(np.float32) + 0.5
+    loss, grad, pairs = oracle_mod.boundary_loss(rh, tb, y, 6, 4, lg, 0.7, om)
+    assert pairs == int(((y != 0) & (tb >= 0)).sum()) and pairs > 100
+    h = 2.0 ** -10                     # exact in fp32 near |r| ~ 1
+    for idx in list(zip(*np.nonzero(np.abs(grad) > 1e-6)))[:40]:
+        up, dn = rh.copy(), rh.copy()
+        up[idx] += h
+        dn[idx] -= h
+        fd = (oracle_mod.boundary_loss(up, tb, y, 6, 4, lg, 0.7, om)[0]
+              - oracle_mod.boundary_loss(dn, tb, y, 6, 4, lg, 0.7, om)[0]) / (float(up[idx]) - float(dn[idx]))
+        assert abs(fd - grad[idx]) < 1e-6 + 1e-4 * abs(grad[idx])
+
+
+def test_boundary_loss_closed_forms(oracle_mod):
+    """Equal decayed scores give softplus(0) = log 2 per pair (weighted mean); a wide
+    margin on the labelled side gives ~0, on the wrong side ~margin / tau."""
+    rng, tb, y, _ = _label_case(oracle_mod, 9)
+    b, H, S = tb.shape
+    zero = np.zeros(H, np.float32)
+    om = rng.random((b, H, S)).astype(np.float32)
+    valid = (y != 0) & (tb >= 0)
+    loss, _, _ = oracle_mod.boundary_loss(np.zeros((b, H, S), np.float32), tb, y, 6, 4, zero, 1.3, om)
+    assert abs(loss - math.log(2) * om[valid].astype(np.float64).mean()) < 1e-12
+    # rhat = +/- 40 * position order: t_new (the later token) is far above / below t_bnd
+    pos = np.broadcast_to(np.arange(S, dtype=np.float32), (b, H, S)).copy()
+    for sign in (1.0, -1.0):
+        rh = (sign * 40.0 * pos).astype(np.float32)
+        loss, _, _ = oracle_mod.boundary_loss(rh, tb, y, 6, 4, zero, 2.0)
+        qs = np.nonzero(valid)
+        margins = sign * 40.0 * ((qs[2] - 6) - tb[valid]) * y[valid]     # y * (rhat_new - rhat_bnd)
+        ref = np.mean([max(0.0, -m / 2.0) for m in margins])
+        assert abs(loss - ref) < 1e-6 * max(1.0, ref)
+
+
+def test_boundary_loss_hand_example(oracle_mod):
+    """The decayed predictions of the worked example (all rhat = 0, n = 1)."""
+    f = _read_fixture("hand_labels_example.txt")
+    S = int(f["S"][0])
+    tb = np.array([int(v) for v in f["t_bnd"]], np.int32).reshape(1, 1, S)
+    y = np.array([int(v) for v in f["y"]], np.int32).reshape(1, 1, S)
+    loss, grad, pairs = oracle_mod.boundary_loss(np.zeros((1, 1, S), np.float32), tb, y, int(f["w"][0]),
+                                                 int(f["loss_n"][0]), [float(f["log_gamma"][0])],
+                                                 float(f["loss_tau"][0]))
+    assert pairs == 8
+    assert abs(loss - float(f["loss_mean"][0])) < 1e-9
