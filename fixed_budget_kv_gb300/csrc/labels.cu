@@ -1,0 +1,327 @@
+// Training-side passes built on the future-attention target ("KVpop ... 精读笔记",
+// section 2.2):
+//   kvpop_target_normalize -- r_t = log(eps + (1/G) sum_g m_t^g), m_t^g the
+//                             future mass averaged over its N_t = S - t - w queries;
+//   kvpop_teacher_labels   -- per row q, the teacher's top-k of E(q) = {s..q-w}
+//                             under the decayed score r_t + floor((q-t)/n) log gamma,
+//                             the cutoff t_bnd the leaving token t_new = q - w has
+//                             to beat, and y = +1 (kept) / -1 (dropped);
+//   kvpop_boundary_loss    -- the pairwise logistic loss on (t_new, t_bnd) with the
+//                             same decay on the predicted scores, and its gradient.
+//
+// Labels: one CTA per (row chunk, batch x head) walks its rows; per row the k-th
+// best "other" token is found by a radix select over a 64-bit key (decayed
+// score in order-preserving form, then the inverted index so that the lower
+// index wins ties), 8 bits per pass with a shared-memory histogram fed by
+// warp-aggregated increments, stopping as soon as one candidate is left.  The
+// decayed score is computed in fp32 with one rounding after the product and one
+// after the sum (no contraction), -0 read as +0 and NaN as -inf, so the integer
+// outputs are exactly those of that definition.
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace kvpop {
+namespace {
+
+constexpr int kLabelThreads = 512;
+constexpr int kLabelRowsPerCta = 64;
+constexpr int kCacheFloats = 32768;  // targets kept in shared memory when S fits (128 KB)
+
+__device__ __forceinline__ float decayed_score(float r, int q, int t, int n, float lg) {
+  const float m = (float)((q - t) / n);
+  const float dec = __fmul_rn(m, lg);
+  float sc = __fadd_rn(r, dec);
+  if (sc != sc) sc = __int_as_float(0xff800000);
+  return sc == 0.0f ? 0.0f : sc;  // -0 == +0
+}
+
+// larger key = better token: (score desc, index asc)
+__device__ __forceinline__ unsigned long long label_key(float sc, int t) {
+  uint32_t u = __float_as_uint(sc);
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return ((unsigned long long)u << 32) | (0xffffffffu - (uint32_t)t);
+}
+
+__global__ void __launch_bounds__(kLabelThreads)
+    teacher_labels_kernel(const float* __restrict__ r_tgt, int H, int S, int s, int w, int k, int n,
+                          const float* __restrict__ log_gamma, int32_t* __restrict__ t_bnd,
+                          int32_t* __restrict__ y, int cache, int* status) {
+  extern __shared__ float rs[];  // the row of targets, when it fits
+  __shared__ uint32_t hist[256];
+  __shared__ unsigned long long s_prefix;
+  __shared__ int s_need, s_left, s_found;
+  const int bh = blockIdx.y;
+  const int h = bh % H;
+  const float* r = r_tgt + (size_t)bh * S;
+  const float lg = log_gamma[h];
+  const int q0 = blockIdx.x * kLabelRowsPerCta;
+  const int q1 = min(S, q0 + kLabelRowsPerCta);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tmax = max(0, q1 - 1 - w);  // candidates of this CTA's rows are t < tmax
+  if (cache)
+    for (int t = tid; t < tmax; t += kLabelThreads) rs[t] = r[t];
+  __syncthreads();
+  for (int q = q0; q < q1; ++q) {
+    const int tn = q - w;
+    const size_t out = (size_t)bh * S + q;
+    if (tn < s || k == 0 || tn - s < k) {  // uniform over the CTA
+      if (tid == 0) {
+        t_bnd[out] = -1;
+        y[out] = tn < s ? 0 : (k == 0 ? -1 : 1);
+      }
+      continue;
+    }
+    // radix select of the k-th largest key among t in [s, tn)
+    unsigned long long prefix = 0, mask = 0;
+    int need = k;
+    int found = -1;
+    for (int shift = 56; shift >= 0; shift -= 8) {
+      for (int i = tid; i < 256; i += kLabelThreads) hist[i] = 0;
+      __syncthreads();
+      for (int t0 = s; t0 < tn; t0 += kLabelThreads) {  // warp-uniform loop
+        const int t = t0 + tid;
+        const bool valid = t < tn;
+        unsigned long long key = 0;
+        if (valid) key = label_key(decayed_score(cache ? rs[t] : __ldg(r + t), q, t, n, lg), t);
+        const bool match = valid && (key & mask) == prefix;
+        const uint32_t active = __ballot_sync(0xffffffffu, match);
+        if (match) {
+          const uint32_t bin = (uint32_t)(key >> shift) & 255u;
+          const uint32_t peers = __match_any_sync(active, bin);
+          if ((__ffs(peers) - 1) == lane) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
+        }
+      }
+      __syncthreads();
+      if (warp == 0) {
+        // bins from the top: lane l owns bins 255 - 8l .. 248 - 8l
+        uint32_t c[8], tot = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          c[i] = hist[255 - 8 * lane - i];
+          tot += c[i];
+        }
+        uint32_t incl = tot;  // inclusive scan over lanes (higher bins first)
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += v;
+        }
+        const uint32_t excl = incl - tot;
+        if (excl < (uint32_t)need && (uint32_t)need <= incl) {
+          uint32_t run = excl;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            if (run + c[i] >= (uint32_t)need) {
+              s_prefix = prefix | ((unsigned long long)(255 - 8 * lane - i) << shift);
+              s_need = need - (int)run;
+              s_left = (int)c[i];
+              break;
+            }
+            run += c[i];
+          }
+        }
+      }
+      __syncthreads();
+      prefix = s_prefix;
+      mask |= 255ull << shift;
+      need = s_need;
+      const int left = s_left;
+      __syncthreads();
+      if (left == 1 || shift == 0) {
+        // one candidate carries the prefix: find it
+        if (tid == 0) s_found = -1;
+        __syncthreads();
+        for (int t = s + tid; t < tn; t += kLabelThreads) {
+          const unsigned long long key = label_key(decayed_score(cache ? rs[t] : __ldg(r + t), q, t, n, lg), t);
+          if ((key & mask) == prefix) atomicMax(&s_found, t);
+        }
+        __syncthreads();
+        found = s_found;
+        __syncthreads();
+        break;
+      }
+    }
+    if (tid == 0) {
+      int yy = -1;
+      if (found >= 0) {
+        const float sb = decayed_score(cache ? rs[found] : __ldg(r + found), q, found, n, lg);
+        const float sn = decayed_score(__ldg(r + tn), q, tn, n, lg);
+        yy = sn > sb ? 1 : -1;  // t_new has the larger index: it loses ties
+      } else {
+        report_error(status, KVPOP_ERR_INTERNAL, SITE_INTERNAL_CHECK, 20);
+      }
+      t_bnd[out] = found;
+      y[out] = yy;
+    }
+  }
+}
+
+__global__ void target_normalize_kernel(const float* __restrict__ target, long long total, int S, int G, int w,
+                                        float eps, float* __restrict__ r) {
+  const float leps = eps > 0.0f ? logf(eps) : __int_as_float(0xff800000);
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int t = (int)(i % S);
+    const int nt = S - t - w;
+    // x = log((1/G) sum_g m_t^g) = target - log(G * N_t)
+    const float x = nt > 0 ? target[i] - logf((float)G * (float)nt) : __int_as_float(0xff800000);
+    float out;
+    if (!(eps > 0.0f)) {
+      out = x;
+    } else {  // log(eps + e^x), stably
+      const float hi = fmaxf(leps, x), lo = fminf(leps, x);
+      out = lo == __int_as_float(0xff800000) ? hi : hi + log1pf(expf(lo - hi));
+    }
+    r[i] = out;
+  }
+}
+
+__device__ __forceinline__ float softplus_f(float z) { return z > 0.0f ? z + log1pf(expf(-z)) : log1pf(expf(z)); }
+__device__ __forceinline__ float sigmoid_f(float z) {
+  return z >= 0.0f ? 1.0f / (1.0f + expf(-z)) : expf(z) / (1.0f + expf(z));
+}
+
+// Sum of the weighted pair losses and the unscaled gradient; acc[0] += loss sum,
+// acc[1] += number of pairs.
+__global__ void __launch_bounds__(256)
+    boundary_loss_kernel(const float* __restrict__ r_hat, const int32_t* __restrict__ t_bnd,
+                         const int32_t* __restrict__ y, const float* __restrict__ omega, int H, int S, int w,
+                         int n, const float* __restrict__ log_gamma, float inv_tau, long long total,
+                         float* __restrict__ acc, float* __restrict__ grad) {
+  __shared__ float red_l[8], red_c[8];
+  float lsum = 0.0f, cnt = 0.0f;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int yy = y[i], tb = t_bnd[i];
+    if (yy == 0 || tb < 0) continue;
+    const long long bh = i / S;
+    const int q = (int)(i - bh * S);
+    const int tn = q - w;
+    if (tn < 0 || tb >= S) continue;  // labels from kvpop_teacher_labels never do this
+    const float lg = log_gamma[bh % H];
+    const float* rr = r_hat + bh * S;
+    const float dn = __fadd_rn(rr[tn], __fmul_rn((float)((q - tn) / n), lg));
+    const float db = __fadd_rn(rr[tb], __fmul_rn((float)((q - tb) / n), lg));
+    const float z = -(float)yy * (dn - db) * inv_tau;
+    const float om = omega ? omega[i] : 1.0f;
+    lsum += om * softplus_f(z);
+    cnt += 1.0f;
+    const float g = om * sigmoid_f(z) * (-(float)yy * inv_tau);
+    atomicAdd(grad + bh * S + tn, g);
+    atomicAdd(grad + bh * S + tb, -g);
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+    cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) {
+    red_l[warp] = lsum;
+    red_c[warp] = cnt;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float a = 0.0f, c = 0.0f;
+    for (int i = 0; i < 8; ++i) {
+      a += red_l[i];
+      c += red_c[i];
+    }
+    if (c > 0.0f) {
+      atomicAdd(acc, a);
+      atomicAdd(acc + 1, c);
+    }
+  }
+}
+
+// loss = sum / pairs, grad /= pairs (the mean over pairs)
+__global__ void boundary_loss_finalize(float* __restrict__ acc, float* __restrict__ grad, long long total) {
+  const float c = acc[1];
+  const float inv = c > 0.0f ? 1.0f / c : 0.0f;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x)
+    grad[i] *= inv;
+}
+
+__global__ void boundary_loss_mean(float* __restrict__ acc) {
+  if (threadIdx.x == 0) acc[0] = acc[1] > 0.0f ? acc[0] / acc[1] : 0.0f;
+}
+
+int grid_for(long long total, int threads) {
+  const long long want = (total + threads - 1) / threads;
+  return (int)std::min<long long>(std::max<long long>(want, 1), (long long)num_sms() * 8);
+}
+
+}  // namespace
+}  // namespace kvpop
+
+using namespace kvpop;
+
+extern "C" kvpop_status kvpop_target_normalize(const float* target, int b, int H, int S, int G, int w, float eps,
+                                               float* r_tgt, kvpop_stream stream) {
+  if (!target || !r_tgt || b <= 0 || H <= 0 || S <= 0 || G <= 0 || w < 0 || !(eps >= 0.0f)) {
+    set_last_error("kvpop_target_normalize: bad arguments");
+    return KVPOP_ERR_INVALID_ARG;
+  }
+  const long long total = (long long)b * H * S;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  target_normalize_kernel<<<grid_for(total, 256), 256, 0, cs>>>(target, total, S, G, w, eps, r_tgt);
+  return cuda_check(cudaGetLastError(), "kvpop_target_normalize: launch");
+}
+
+extern "C" kvpop_status kvpop_teacher_labels(const float* r_tgt, int b, int H, int S, kvpop_budget bud, int n,
+                                             const float* log_gamma, int32_t* t_bnd, int32_t* y,
+                                             kvpop_stream stream) {
+  if (!r_tgt || !log_gamma || !t_bnd || !y || b <= 0 || H <= 0 || S <= 0 || n <= 0) {
+    set_last_error("kvpop_teacher_labels: bad arguments");
+    return KVPOP_ERR_INVALID_ARG;
+  }
+  if (bud.s < 0 || bud.w < 0 || bud.k < 0) {
+    set_last_error("kvpop_teacher_labels: invalid budget");
+    return KVPOP_ERR_INVALID_ARG;
+  }
+  if ((long long)b * H > 65535 || S > (1 << 30)) {
+    set_last_error("kvpop_teacher_labels: b*H must be <= 65535");
+    return KVPOP_ERR_UNSUPPORTED;
+  }
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const int cache = S <= kCacheFloats ? 1 : 0;
+  const int smem = cache ? S * 4 : 0;
+  kvpop_status st = cuda_check(
+      cudaFuncSetAttribute(teacher_labels_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kCacheFloats * 4),
+      "kvpop_teacher_labels: smem attribute");
+  if (st != KVPOP_OK) return st;
+  dim3 grid((S + kLabelRowsPerCta - 1) / kLabelRowsPerCta, b * H);
+  teacher_labels_kernel<<<grid, kLabelThreads, smem, cs>>>(r_tgt, H, S, bud.s, bud.w, bud.k, n, log_gamma, t_bnd,
+                                                            y, cache, device_status_ptr());
+  return cuda_check(cudaGetLastError(), "kvpop_teacher_labels: launch");
+}
+
+extern "C" kvpop_status kvpop_boundary_loss(const float* r_hat, const int32_t* t_bnd, const int32_t* y,
+                                            const float* omega, int b, int H, int S, int w, int n,
+                                            const float* log_gamma, float tau, float* loss, float* grad,
+                                            kvpop_stream stream) {
+  if (!r_hat || !t_bnd || !y || !log_gamma || !loss || !grad || b <= 0 || H <= 0 || S <= 0 || w < 0 || n <= 0 ||
+      !(tau > 0.0f)) {
+    set_last_error("kvpop_boundary_loss: bad arguments");
+    return KVPOP_ERR_INVALID_ARG;
+  }
+  const long long total = (long long)b * H * S;
+  if (total > (1LL << 24)) {  // the pair count is kept exactly in fp32
+    set_last_error("kvpop_boundary_loss: b*H*S must be <= 2^24");
+    return KVPOP_ERR_UNSUPPORTED;
+  }
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  kvpop_status st = cuda_check(cudaMemsetAsync(loss, 0, 2 * sizeof(float), cs), "kvpop_boundary_loss: clear");
+  if (st == KVPOP_OK) st = cuda_check(cudaMemsetAsync(grad, 0, total * sizeof(float), cs), "kvpop_boundary_loss: clear");
+  if (st != KVPOP_OK) return st;
+  boundary_loss_kernel<<<grid_for(total, 256), 256, 0, cs>>>(r_hat, t_bnd, y, omega, H, S, w, n, log_gamma,
+                                                              1.0f / tau, total, loss, grad);
+  st = cuda_check(cudaGetLastError(), "kvpop_boundary_loss: launch");
+  if (st != KVPOP_OK) return st;
+  boundary_loss_finalize<<<grid_for(total, 256), 256, 0, cs>>>(loss, grad, total);
+  st = cuda_check(cudaGetLastError(), "kvpop_boundary_loss: launch");
+  if (st != KVPOP_OK) return st;
+  boundary_loss_mean<<<1, 32, 0, cs>>>(loss);
+  return cuda_check(cudaGetLastError(), "kvpop_boundary_loss: launch");
+}

@@ -74,6 +74,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                  P], c_int),
         "kvpop_future_target_noalloc": ([P, P, P, c_int, c_int, c_int, c_int, c_int, c_float, c_int, P, P],
                                         c_int),
+        "kvpop_target_normalize": ([P, c_int, c_int, c_int, c_int, c_int, c_float, P, P], c_int),
+        "kvpop_teacher_labels": ([P, c_int, c_int, c_int, Budget, c_int, P, P, P, P], c_int),
+        "kvpop_boundary_loss": ([P, P, P, P, c_int, c_int, c_int, c_int, c_int, P, c_float, P, P, P], c_int),
         "kvpop_cache_create": ([c_int, c_int, c_int, c_int, Budget, P], c_int),
         "kvpop_cache_destroy": ([P], c_int),
         "kvpop_cache_prefill": ([P, P, P, P, c_int, P, P], c_int),
@@ -229,6 +232,50 @@ def future_target_noalloc(q, k, lse, w: int, scale: float = 0.0, out=None, strea
     _check(load().kvpop_future_target_noalloc(_p(q), _p(k), _p(lse), b, S, Hq, H, D, float(scale), int(w),
                                               _p(target), _stream(stream)), "kvpop_future_target_noalloc")
     return target
+
+
+# ----------------------------------------------------------------------------
+# training-side passes: normalised target, teacher labels, boundary loss
+# ----------------------------------------------------------------------------
+
+def target_normalize(target, G: int, w: int, eps: float, out=None, stream=None):
+    """r_tgt = log(eps + exp(target) / (G * N_t)), N_t = S - t - w, [b, H, S]."""
+    _need(target, torch.float32, "target")
+    b, H, S = target.shape
+    r = torch.empty_like(target) if out is None else out
+    _check(load().kvpop_target_normalize(_p(target), b, H, S, int(G), int(w), float(eps), _p(r), _stream(stream)),
+           "kvpop_target_normalize")
+    return r
+
+
+def teacher_labels(r_tgt, s: int, w: int, k: int, n: int, log_gamma, out=None, stream=None):
+    """(t_bnd, y) per row, int32 [b, H, S]; log_gamma: fp32 [H] on the device."""
+    _need(r_tgt, torch.float32, "r_tgt")
+    _need(log_gamma, torch.float32, "log_gamma")
+    b, H, S = r_tgt.shape
+    if out is None:
+        tb = torch.empty((b, H, S), dtype=torch.int32, device=r_tgt.device)
+        y = torch.empty_like(tb)
+    else:
+        tb, y = out
+    _check(load().kvpop_teacher_labels(_p(r_tgt), b, H, S, Budget(s, w, k), int(n), _p(log_gamma), _p(tb), _p(y),
+                                       _stream(stream)), "kvpop_teacher_labels")
+    return tb, y
+
+
+def boundary_loss(r_hat, t_bnd, y, w: int, n: int, log_gamma, tau: float, omega=None, out=None, stream=None):
+    """(loss[2] = (mean loss, pair count), grad [b, H, S]) of the pairwise boundary loss."""
+    _need(r_hat, torch.float32, "r_hat")
+    b, H, S = r_hat.shape
+    if out is None:
+        loss = torch.empty(2, dtype=torch.float32, device=r_hat.device)
+        grad = torch.empty_like(r_hat)
+    else:
+        loss, grad = out
+    _check(load().kvpop_boundary_loss(_p(r_hat), _p(t_bnd), _p(y), _p(omega), b, H, S, int(w), int(n),
+                                      _p(log_gamma), float(tau), _p(loss), _p(grad), _stream(stream)),
+           "kvpop_boundary_loss")
+    return loss, grad
 
 
 # ----------------------------------------------------------------------------

@@ -175,6 +175,54 @@ kvpop_status kvpop_future_target_noalloc(const void* q, const void* k, const flo
                                          float* target, kvpop_stream stream);
 
 /* ------------------------------------------------------------------------
+ * Training-side passes on the future-attention target ([notes] section 2.2).
+ *
+ * kvpop_target_normalize: r_tgt[b,h,t] = log(eps + (1/G) sum_g m_t^g) with
+ *   m_t^g = (1/N_t) sum_{d=t+w}^{S-1} A_{d,t}^g and N_t = S - t - w, from the
+ *   unnormalised target of kvpop_future_target (natural log) -- i.e.
+ *   log(eps + exp(target) / (G N_t)); a key with no future query (N_t <= 0)
+ *   has mass 0, so log(eps) (-inf when eps == 0).  target, r_tgt: [b, H, S]
+ *   fp32 device; r_tgt may equal target.  eps >= 0.  Errors: INVALID_ARG, CUDA.
+ *
+ * kvpop_teacher_labels: per row q, the token t_new = q - w leaves the window;
+ *   the teacher ranks E(q) = {s..q-w} by the decayed score
+ *     r_t(q) = r_tgt[t] + floor((q - t) / n) * log_gamma[h]
+ *   (fp32: rounded after the product and after the sum; NaN counts as -inf,
+ *   -0 as +0; ties go to the lower index) and keeps its top k.
+ *     t_bnd[b,h,q] = the k-th best token of E(q) other than t_new -- the
+ *                    cutoff t_new has to beat (when t_new is dropped it is the
+ *                    lowest-scoring member of the teacher top-k); -1 when
+ *                    fewer than k other tokens are eligible or k == 0;
+ *     y[b,h,q]     = +1 if t_new is in the teacher top-k, -1 if not, 0 when the
+ *                    row has no leaving token (q - w < s).
+ *   r_tgt [b, H, S] fp32, log_gamma [H] fp32 (log of the per-head decay factor,
+ *   <= 0), t_bnd and y [b, H, S] int32, all device.  n >= 1.  Cost: one
+ *   radix select over E(q) per row, O(S^2) per (batch, head).
+ *   Errors: INVALID_ARG, UNSUPPORTED (b*H > 65535), CUDA.
+ *
+ * kvpop_boundary_loss: the pairwise logistic loss over the rows with y != 0
+ *   and t_bnd >= 0:
+ *     loss[0] = mean of omega[q] * softplus(-y[q] (rh_new(q) - rh_bnd(q)) / tau),
+ *     rh_t(q) = r_hat[t] + floor((q - t) / n) * log_gamma[h]  (the same decay on
+ *     the predicted scores), t_new = q - w;
+ *     loss[1] = the number of such pairs (0 pairs: loss[0] = 0, grad = 0);
+ *     grad = d loss[0] / d r_hat, [b, H, S] fp32, overwritten.
+ *   r_hat [b, H, S] fp32; omega [b, H, S] fp32 or NULL (all 1); t_bnd, y as
+ *   from kvpop_teacher_labels; loss: 2 floats.  tau > 0.  b*H*S <= 2^24.  Sums
+ *   use fp32 atomics, so the last bits vary between runs.
+ *   Errors: INVALID_ARG, UNSUPPORTED, CUDA.
+ * ---------------------------------------------------------------------- */
+kvpop_status kvpop_target_normalize(const float* target, int b, int H, int S, int G, int w, float eps,
+                                    float* r_tgt, kvpop_stream stream);
+kvpop_status kvpop_teacher_labels(const float* r_tgt, int b, int H, int S, kvpop_budget budget, int n,
+                                  const float* log_gamma, int32_t* t_bnd, int32_t* y,
+                                  kvpop_stream stream);
+kvpop_status kvpop_boundary_loss(const float* r_hat, const int32_t* t_bnd, const int32_t* y,
+                                 const float* omega, int b, int H, int S, int w, int n,
+                                 const float* log_gamma, float tau, float* loss, float* grad,
+                                 kvpop_stream stream);
+
+/* ------------------------------------------------------------------------
  * Fixed-budget decode cache ([notes] section 2.4 and section 3.3: B slots
  * per KV head, the token u = q - w leaving the window is kept or evicted by
  * comparing its priority with the worst held long-range token; [summary]

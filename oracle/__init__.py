@@ -66,6 +66,7 @@ def _load():
         _lib.oracle_target_colsum.argtypes = [P, P, i32, i32, i32, i32, i32, f64, i32, P]
         _lib.oracle_target_normalize.argtypes = [P, i64, i32, i32, i32, f64, P]
         _lib.oracle_teacher_labels.argtypes = [P, i32, i32, i32, i32, i32, ctypes.c_float, P, P]
+        _lib.oracle_teacher_labels_rows.argtypes = [P, i32, i32, i32, i32, i32, ctypes.c_float, P, i32, P, P]
         _lib.oracle_boundary_loss.argtypes = [P, P, P, P, i64, i32, i32, i32, i32, P, f64, P, P]
         _lib.oracle_boundary_loss.restype = i64
         _lib.oracle_num_threads.restype = i32
@@ -354,3 +355,14 @@ def boundary_loss(r_hat: np.ndarray, t_bnd: np.ndarray, y: np.ndarray, w: int, n
     pairs = _load().oracle_boundary_loss(_p(rh), _p(tb), _p(yy), None if om is None else _p(om), b * H, S, H,
                                          w, n, _p(lg), float(tau), ctypes.byref(loss), _p(grad))
     return loss.value, grad, int(pairs)
+
+
+def teacher_labels_rows(r_1d: np.ndarray, s: int, w: int, k: int, n: int, log_gamma: float, rows):
+    """(t_bnd, y) of the listed rows only, for one (batch, head) row of targets."""
+    r = np.ascontiguousarray(r_1d, dtype=np.float32)
+    rows = np.ascontiguousarray(rows, dtype=np.int32)
+    tb = np.empty(len(rows), dtype=np.int32)
+    y = np.empty(len(rows), dtype=np.int32)
+    _load().oracle_teacher_labels_rows(_p(r), r.shape[-1], s, w, k, n, ctypes.c_float(np.float32(log_gamma)),
+                                       _p(rows), len(rows), _p(tb), _p(y))
+    return tb, y

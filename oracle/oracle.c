@@ -398,17 +398,18 @@ static int cmp_fkeyed(const void* a, const void* b) {
  *   rows without a leaving token (q - w < s) get y = 0, t_bnd = -1.
  * Sorting E(q) explicitly for every row: O(S^2 log S).
  */
-void oracle_teacher_labels(const float* r, int S, int s, int w, int k, int n, float lg, int32_t* t_bnd,
-                           int32_t* y) {
+void oracle_teacher_labels_rows(const float* r, int S, int s, int w, int k, int n, float lg,
+                                const int32_t* rows, int nrows, int32_t* t_bnd, int32_t* y) {
 #pragma omp parallel
     {
         fkeyed_t* buf = (fkeyed_t*)malloc(sizeof(fkeyed_t) * (size_t)(S > 0 ? S : 1));
 #pragma omp for schedule(dynamic, 16)
-        for (int q = 0; q < S; ++q) {
+        for (int i = 0; i < nrows; ++i) {
+            int q = rows[i];
             int tn = q - w;
             if (tn < s) {
-                t_bnd[q] = -1;
-                y[q] = 0;
+                t_bnd[i] = -1;
+                y[i] = 0;
                 continue;
             }
             int m = 0;
@@ -418,22 +419,31 @@ void oracle_teacher_labels(const float* r, int S, int s, int w, int k, int n, fl
                 ++m;
             }
             if (k == 0) {
-                t_bnd[q] = -1;
-                y[q] = -1;
+                t_bnd[i] = -1;
+                y[i] = -1;
                 continue;
             }
             if (m < k) {
-                t_bnd[q] = -1;
-                y[q] = 1;
+                t_bnd[i] = -1;
+                y[i] = 1;
                 continue;
             }
             qsort(buf, (size_t)m, sizeof(fkeyed_t), cmp_fkeyed);
             fkeyed_t me = {decayed(r[tn], q, tn, n, lg), tn};
-            t_bnd[q] = buf[k - 1].idx;
-            y[q] = cmp_fkeyed(&me, &buf[k - 1]) < 0 ? 1 : -1;
+            t_bnd[i] = buf[k - 1].idx;
+            y[i] = cmp_fkeyed(&me, &buf[k - 1]) < 0 ? 1 : -1;
         }
         free(buf);
     }
+}
+
+/* every row q = 0..S-1 */
+void oracle_teacher_labels(const float* r, int S, int s, int w, int k, int n, float lg, int32_t* t_bnd,
+                           int32_t* y) {
+    int32_t* rows = (int32_t*)malloc(sizeof(int32_t) * (size_t)(S > 0 ? S : 1));
+    for (int q = 0; q < S; ++q) rows[q] = q;
+    oracle_teacher_labels_rows(r, S, s, w, k, n, lg, rows, S, t_bnd, y);
+    free(rows);
 }
 
 static double softplus(double z) { return z > 0.0 ? z + log1p(exp(-z)) : log1p(exp(z)); }

@@ -75,3 +75,18 @@ def test_target_and_cache_validation(lib):
     # at most 65536 slots per head (the split merge holds 256 splits of 256 slots)
     assert lib.kvpop_cache_create(1, 1, 4, 64, kvpop.Budget(16, 1024, 65536 - 1040 + 1), ctypes.byref(h)) == 1
     assert lib.kvpop_decode_step(None, P, P, P, P, P, P, None, None) == 1
+
+
+def test_training_side_validation(lib):
+    """Argument checks of the normalised target, teacher labels and boundary loss
+    (host-side: nothing is launched on these paths)."""
+    P = ctypes.c_void_p(16)
+    bud = kvpop.Budget(1, 2, 3)
+    assert lib.kvpop_target_normalize(None, 1, 1, 8, 4, 2, 0.0, P, None) == 1
+    assert lib.kvpop_target_normalize(P, 1, 1, 8, 4, 2, -1.0, P, None) == 1        # eps < 0
+    assert lib.kvpop_teacher_labels(P, 1, 1, 8, bud, 0, P, P, P, None) == 1          # n = 0
+    assert lib.kvpop_teacher_labels(P, 1, 1, 8, kvpop.Budget(-1, 2, 3), 2, P, P, P, None) == 1
+    assert lib.kvpop_teacher_labels(P, 300, 300, 8, bud, 2, P, P, P, None) == 2      # b*H > 65535
+    assert lib.kvpop_boundary_loss(P, P, P, None, 1, 1, 8, 2, 2, P, 0.0, P, P, None) == 1   # tau = 0
+    assert lib.kvpop_boundary_loss(P, P, P, None, 1, 1, 8, 2, 2, None, 1.0, P, P, None) == 1
+    assert lib.kvpop_boundary_loss(P, P, P, None, 64, 64, 8192, 2, 2, P, 1.0, P, P, None) == 2  # > 2^24

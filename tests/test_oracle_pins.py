@@ -536,3 +536,13 @@ def test_boundary_loss_hand_example(oracle_mod):
                                                  float(f["loss_tau"][0]))
     assert pairs == 8
     assert abs(loss - float(f["loss_mean"][0])) < 1e-9
+
+
+def test_teacher_labels_rows_equal_full(oracle_mod):
+    """The sampled-row entry gives the full sweep's values on the rows it is asked for."""
+    rng = np.random.default_rng(21)
+    r = rng.standard_normal((1, 1, 400)).astype(np.float32)
+    tb, y = oracle_mod.teacher_labels(r, 3, 9, 11, 5, [-0.2])
+    rows = rng.choice(400, size=60, replace=False).astype(np.int32)
+    tbr, yr = oracle_mod.teacher_labels_rows(r[0, 0], 3, 9, 11, 5, -0.2, rows)
+    assert (tbr == tb[0, 0, rows]).all() and (yr == y[0, 0, rows]).all()
