@@ -66,7 +66,7 @@ def parse():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--only", choices=["mask", "sparse", "dense", "target", "decode"],
+    ap.add_argument("--only", choices=["mask", "sparse", "dense", "target", "decode", "labels"],
                     help="for a profiler: set up the workload, run that pass twice (decode: 24 steps), "
                          "print one status line and exit")
     return ap.parse_args()
@@ -252,7 +252,15 @@ def run_gpu(args, rank, world, local_rank):
         "gpu_launches": LAUNCHES_STEP * args.steps,
         "clocks": clk.summary(),
     }
+    # the sparse-LSE pipeline rate from the same per-pass times
+    sparse_step = times["mask"] + times["sparse_attn"] + times["future_target"]
+    result["sparse_lse_pipeline"] = {"ms_per_step": round(sparse_step, 4),
+                                     "value": round(job_throughput(b * S, world, max_over_ranks(sparse_step, world, dev)), 1),
+                                     "unit": "tokens/s",
+                                     "note": "mask + sparse forward + target on the sparse LSE; per-pass event times"}
 
+    result["training_side"] = training_side(args, wl, q, k, v, prio, ev_t, lists, lse_s, lse_d, target,
+                                            ws_tgt, dev, world)
     if not args.no_e2e:
         result["e2e"] = e2e(args, wl, q, k, v, prio, ws_mask, ws_tgt, dev, world)
     if not args.no_decode:
@@ -260,6 +268,63 @@ def run_gpu(args, rank, world, local_rank):
         result["gpu_launches"] += LAUNCHES_DECODE_STEP * result["decode"]["steps"]
     del q, k, v, O
     return result
+
+
+# decay of the teacher labels on the synthetic workload (the pages give no values)
+DECAY_STEP = 64
+DECAY_GAMMA = (0.90, 0.99)   # per KV head, spread linearly between these
+TARGET_EPS = 1e-6
+
+
+def training_side(args, wl, q, k, v, prio, ev_t, lists, lse_s, lse_d, target, ws_tgt, dev, world):
+    """The training-side passes on the same workload, each timed alone (CUDA events,
+    mean of `steps` launches): the normalised target, the teacher boundary labels,
+    the pairwise boundary loss with its gradient; and the sparse-LSE variant of the
+    pipeline (mask, sparse forward, target on the sparse LSE: no dense pass) with the
+    deviation of its target from the dense-LSE one."""
+    import torch
+    from fixed_budget_kv_gb300 import kvpop
+    b, S, H = wl.b, wl.S, wl.H
+    bud = (wl.s, wl.w, wl.k)
+    lg = torch.log(torch.linspace(DECAY_GAMMA[0], DECAY_GAMMA[1], H, device=dev, dtype=torch.float32))
+    r_tgt = torch.empty_like(target)
+    tb = torch.empty((b, H, S), dtype=torch.int32, device=dev)
+    y = torch.empty_like(tb)
+    r_hat = torch.randn((b, H, S), generator=torch.Generator(device=dev).manual_seed(1), device=dev)
+    loss = torch.empty(2, dtype=torch.float32, device=dev)
+    grad = torch.empty_like(r_hat)
+    t_sparse = torch.empty_like(target)
+    passes = {
+        "target_normalize": lambda: kvpop.target_normalize(target, wl.G, wl.w, TARGET_EPS, out=r_tgt),
+        "teacher_labels": lambda: kvpop.teacher_labels(r_tgt, *bud, DECAY_STEP, lg, out=(tb, y)),
+        "boundary_loss": lambda: kvpop.boundary_loss(r_hat, tb, y, wl.w, DECAY_STEP, lg, 1.0, out=(loss, grad)),
+        "sparse_lse_target": lambda: kvpop.future_target(q, k, lse_s, wl.w, workspace=ws_tgt, out=t_sparse),
+    }
+    out = {}
+    n = max(3, args.steps // 2)
+    for name, fn in passes.items():
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        out[name] = {"ms": round(max_over_ranks(e0.elapsed_time(e1) / n, world, dev), 4)}
+    st, words = kvpop.device_status(reset=True)
+    if st != 0:
+        raise RuntimeError(f"device status after the training-side passes: {words}")
+    out["teacher_labels"]["rows_per_s"] = round(job_throughput(b * H * S, world, out["teacher_labels"]["ms"]), 1)
+    out["boundary_loss"]["pairs"] = int(loss[1].item())
+    fin = torch.isfinite(target)
+    dev_abs = (t_sparse - target)[fin].abs()
+    out["sparse_lse_target"]["deviation_from_dense_lse_target"] = {
+        "max_abs": round(float(dev_abs.max()), 4), "mean_abs": round(float(dev_abs.mean()), 5),
+        "unit": "natural log of the future mass"}
+    out["settings"] = {"decay_step_n": DECAY_STEP, "gamma_range": list(DECAY_GAMMA), "eps": TARGET_EPS,
+                       "tau": 1.0, "r_hat": "N(0,1), torch generator seed 1"}
+    return out
 
 
 def e2e(args, wl, q, k, v, prio, ws_mask, ws_tgt, dev, world):
@@ -442,10 +507,15 @@ def run_only(args):
         bud = (wl.s, wl.w, wl.k)
         if args.only in ("sparse", "mask"):
             _, _, ev, lists = kvpop.mask(prio, *bud)
-        if args.only in ("dense", "target"):
+        if args.only in ("dense", "target", "labels"):
             _, lse_d = kvpop.attn_fwd(q, k, None, 0.0, want_o=False)
+        if args.only == "labels":
+            r_tgt = kvpop.target_normalize(kvpop.future_target(q, k, lse_d, wl.w), wl.G, wl.w, TARGET_EPS)
+            lg = torch.log(torch.linspace(DECAY_GAMMA[0], DECAY_GAMMA[1], wl.H, device=dev, dtype=torch.float32))
         for _ in range(2):
-            if args.only == "mask":
+            if args.only == "labels":
+                kvpop.teacher_labels(r_tgt, *bud, DECAY_STEP, lg)
+            elif args.only == "mask":
                 kvpop.mask(prio, *bud)
             elif args.only == "sparse":
                 kvpop.attn_fwd(q, k, v, 0.0, ev, lists, bud)

@@ -13,7 +13,9 @@
 // best "other" token is found by a radix select over a 64-bit key (decayed
 // score in order-preserving form, then the inverted index so that the lower
 // index wins ties), 8 bits per pass with a shared-memory histogram fed by
-// warp-aggregated increments, stopping as soon as one candidate is left.  The
+// warp-aggregated increments, stopping as soon as one candidate is left.  Up to
+// 16384 candidates per row the keys stay in registers across the passes and the
+// previous row's cutoff is tried first as a pivot.  The
 // decayed score is computed in fp32 with one rounding after the product and one
 // after the sum (no contraction), -0 read as +0 and NaN as -inf, so the integer
 // outputs are exactly those of that definition.
@@ -157,6 +159,162 @@ __global__ void __launch_bounds__(kLabelThreads)
   }
 }
 
+// floor(d / n) for 0 <= d < 2^24 through the fp32 reciprocal, corrected by one step
+__device__ __forceinline__ int div_floor(int d, int n, float inv_n) {
+  int m = __float2int_rz(__fmul_rn((float)d, inv_n));
+  if (m * n > d) --m;
+  else if ((m + 1) * n <= d) ++m;
+  return m;
+}
+
+__device__ __forceinline__ float decayed_score_m(float r, int m, float lg) {
+  float sc = __fadd_rn(r, __fmul_rn((float)m, lg));
+  if (sc != sc) sc = __int_as_float(0xff800000);
+  return sc == 0.0f ? 0.0f : sc;  // -0 == +0
+}
+
+// Same result as teacher_labels_kernel for rows with at most CPT * kLabelThreads
+// candidates: each thread keeps its candidates' keys in registers for all the
+// radix passes, and a row first tries the previous row's cutoff as a pivot (one
+// counting pass: it is still the cutoff when exactly k - 1 candidates beat it).
+template <int CPT>
+__global__ void __launch_bounds__(kLabelThreads)
+    teacher_labels_regs(const float* __restrict__ r_tgt, int H, int S, int s, int w, int k, int n, float inv_n,
+                        const float* __restrict__ log_gamma, int32_t* __restrict__ t_bnd,
+                        int32_t* __restrict__ y, int* status) {
+  static_assert(CPT <= 32, "validity bits");
+  __shared__ uint32_t hist[256];
+  __shared__ unsigned long long s_prefix;
+  __shared__ int s_need, s_left, s_found;
+  __shared__ int red[kLabelThreads / 32];
+  const int bh = blockIdx.y;
+  const float* r = r_tgt + (size_t)bh * S;
+  const float lg = log_gamma[bh % H];
+  const int q0 = blockIdx.x * kLabelRowsPerCta;
+  const int q1 = min(S, q0 + kLabelRowsPerCta);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // block-wide sum of one int per thread (every thread gets it)
+  auto block_sum = [&](int v) -> int {
+    v = __reduce_add_sync(0xffffffffu, v);
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    int tot = 0;
+#pragma unroll
+    for (int i = 0; i < kLabelThreads / 32; ++i) tot += red[i];
+    __syncthreads();
+    return tot;
+  };
+  int prev = -1;  // the previous row's cutoff
+  for (int q = q0; q < q1; ++q) {
+    const int tn = q - w;
+    const size_t out = (size_t)bh * S + q;
+    if (tn < s || k == 0 || tn - s < k) {  // uniform over the CTA
+      if (tid == 0) {
+        t_bnd[out] = -1;
+        y[out] = tn < s ? 0 : (k == 0 ? -1 : 1);
+      }
+      continue;
+    }
+    unsigned long long kc[CPT];
+    uint32_t valid = 0;
+#pragma unroll
+    for (int j = 0; j < CPT; ++j) {
+      const int t = s + tid + j * kLabelThreads;
+      kc[j] = 0;
+      if (t < tn) {
+        kc[j] = label_key(decayed_score_m(__ldg(r + t), div_floor(q - t, n, inv_n), lg), t);
+        valid |= 1u << j;
+      }
+    }
+    int found = -1;
+    if (prev >= 0) {  // uniform: prev is a candidate of this row too (prev < q - 1 - w < tn)
+      const unsigned long long pk =
+          label_key(decayed_score_m(__ldg(r + prev), div_floor(q - prev, n, inv_n), lg), prev);
+      int c = 0;
+#pragma unroll
+      for (int j = 0; j < CPT; ++j) c += ((valid >> j) & 1u) && kc[j] > pk;
+      if (block_sum(c) == k - 1) found = prev;
+    }
+    if (found < 0) {
+      unsigned long long prefix = 0, mask = 0;
+      int need = k;
+      for (int shift = 56; shift >= 0; shift -= 8) {
+        for (int i = tid; i < 256; i += kLabelThreads) hist[i] = 0;
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < CPT; ++j) {
+          const bool match = ((valid >> j) & 1u) && (kc[j] & mask) == prefix;
+          const uint32_t active = __ballot_sync(0xffffffffu, match);
+          if (match) {
+            const uint32_t bin = (uint32_t)(kc[j] >> shift) & 255u;
+            const uint32_t peers = __match_any_sync(active, bin);
+            if ((__ffs(peers) - 1) == lane) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
+          }
+        }
+        __syncthreads();
+        if (warp == 0) {
+          uint32_t c[8], tot = 0;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            c[i] = hist[255 - 8 * lane - i];
+            tot += c[i];
+          }
+          uint32_t incl = tot;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+          }
+          const uint32_t excl = incl - tot;
+          if (excl < (uint32_t)need && (uint32_t)need <= incl) {
+            uint32_t run = excl;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              if (run + c[i] >= (uint32_t)need) {
+                s_prefix = prefix | ((unsigned long long)(255 - 8 * lane - i) << shift);
+                s_need = need - (int)run;
+                s_left = (int)c[i];
+                break;
+              }
+              run += c[i];
+            }
+          }
+        }
+        __syncthreads();
+        prefix = s_prefix;
+        mask |= 255ull << shift;
+        need = s_need;
+        const int left = s_left;
+        __syncthreads();
+        if (left == 1 || shift == 0) {
+          if (tid == 0) s_found = -1;
+          __syncthreads();
+#pragma unroll
+          for (int j = 0; j < CPT; ++j)
+            if (((valid >> j) & 1u) && (kc[j] & mask) == prefix) atomicMax(&s_found, s + tid + j * kLabelThreads);
+          __syncthreads();
+          found = s_found;
+          __syncthreads();
+          break;
+        }
+      }
+    }
+    prev = found;
+    if (tid == 0) {
+      int yy = -1;
+      if (found >= 0) {
+        const float sb = decayed_score_m(__ldg(r + found), div_floor(q - found, n, inv_n), lg);
+        const float sn = decayed_score_m(__ldg(r + tn), div_floor(q - tn, n, inv_n), lg);
+        yy = sn > sb ? 1 : -1;  // t_new has the larger index: it loses ties
+      } else {
+        report_error(status, KVPOP_ERR_INTERNAL, SITE_INTERNAL_CHECK, 21);
+      }
+      t_bnd[out] = found;
+      y[out] = yy;
+    }
+  }
+}
+
 __global__ void target_normalize_kernel(const float* __restrict__ target, long long total, int S, int G, int w,
                                         float eps, float* __restrict__ r) {
   const float leps = eps > 0.0f ? logf(eps) : __int_as_float(0xff800000);
@@ -285,13 +443,26 @@ extern "C" kvpop_status kvpop_teacher_labels(const float* r_tgt, int b, int H, i
     return KVPOP_ERR_UNSUPPORTED;
   }
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  dim3 grid((S + kLabelRowsPerCta - 1) / kLabelRowsPerCta, b * H);
+  // candidates of the last row: S - 1 - w - s
+  const long long maxc = (long long)S - 1 - bud.w - bud.s;
+  const float inv_n = 1.0f / (float)n;
+  if (S < (1 << 24) && maxc <= 8LL * kLabelThreads) {
+    teacher_labels_regs<8><<<grid, kLabelThreads, 0, cs>>>(r_tgt, H, S, bud.s, bud.w, bud.k, n, inv_n, log_gamma,
+                                                           t_bnd, y, device_status_ptr());
+    return cuda_check(cudaGetLastError(), "kvpop_teacher_labels: launch");
+  }
+  if (S < (1 << 24) && maxc <= 32LL * kLabelThreads) {
+    teacher_labels_regs<32><<<grid, kLabelThreads, 0, cs>>>(r_tgt, H, S, bud.s, bud.w, bud.k, n, inv_n, log_gamma,
+                                                            t_bnd, y, device_status_ptr());
+    return cuda_check(cudaGetLastError(), "kvpop_teacher_labels: launch");
+  }
   const int cache = S <= kCacheFloats ? 1 : 0;
   const int smem = cache ? S * 4 : 0;
   kvpop_status st = cuda_check(
       cudaFuncSetAttribute(teacher_labels_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kCacheFloats * 4),
       "kvpop_teacher_labels: smem attribute");
   if (st != KVPOP_OK) return st;
-  dim3 grid((S + kLabelRowsPerCta - 1) / kLabelRowsPerCta, b * H);
   teacher_labels_kernel<<<grid, kLabelThreads, smem, cs>>>(r_tgt, H, S, bud.s, bud.w, bud.k, n, log_gamma, t_bnd,
                                                             y, cache, device_status_ptr());
   return cuda_check(cudaGetLastError(), "kvpop_teacher_labels: launch");
