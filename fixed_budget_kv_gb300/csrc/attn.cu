@@ -678,6 +678,8 @@ extern "C" kvpop_status kvpop_attn_fwd(const void* q, const void* k, const void*
   const float scale_log2 = sc * 1.4426950408889634f;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   if (!sparse && !O) return launch_dense_lse(q, k, b, S, Hq, H, D, scale_log2, lse, cs);
+  if (sparse && D == 128)
+    return launch_sparse_pair(q, k, v, b, S, Hq, H, scale_log2, evict_at, lists, bud, O, lse, cs);
 
   AttnParams prm;
   memset(&prm, 0, sizeof(prm));

@@ -468,6 +468,15 @@ __device__ __forceinline__ void tma_load_4d_pair(void* dst, const CUtensorMap* m
       : "memory");
 }
 
+__device__ __forceinline__ void tma_gather4_pair(void* dst, const CUtensorMap* map, uint32_t bar_cluster, int x,
+                                                 int r0, int r1, int r2, int r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+      : "memory");
+}
+
 // one warp of each CTA of the pair, together
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
@@ -489,6 +498,18 @@ __device__ __forceinline__ void mma_ss_pair(uint32_t d_tmem, uint64_t a_desc, ui
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// leader only: D (+)= A[tmem] * B[smem] over the pair (M = 256); A rows from each
+// CTA's tensor memory, B's N columns split between the CTAs' shared memory
+__device__ __forceinline__ void mma_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -518,6 +539,11 @@ bool make_tmap_rows(CUtensorMap* map, const void* base, uint64_t cols, uint64_t 
 
 int current_device();
 int num_sms();
+
+// Sparse forward on CTA pairs for D = 128 (csrc/attn_pair.cu); arguments already validated.
+kvpop_status launch_sparse_pair(const void* q, const void* k, const void* v, int b, int S, int Hq, int H,
+                                float scale_log2, const int32_t* evict_at, const int32_t* lists,
+                                kvpop_budget bud, void* O, float* lse, cudaStream_t cs);
 
 // Dense causal LSE-only pass (csrc/dense_lse.cu); arguments already validated.
 kvpop_status launch_dense_lse(const void* q, const void* k, int b, int S, int Hq, int H, int D,
