@@ -389,45 +389,71 @@ __global__ void evict_search(const int32_t* __restrict__ rank, const int32_t* __
 // Ordered compaction of candidates in [0, n) where `cand(i)` gives the
 // position: keeps those with lo < evict_at <= hi, calls emit(slot, pos, ev)
 // with slots counted from out_start (only below out_cap); returns the end.
+// Each thread takes kCompactItems consecutive candidates of a chunk (their
+// evict_at loads in flight together); one block-wide exclusive scan of the
+// per-thread counts per chunk keeps the order.  All threads of the block call it.
+constexpr int kCompactThreads = 1024;
+constexpr int kCompactItems = 4;
+
 template <typename Cand, typename Emit>
 __device__ int compact_alive(Cand cand, int n, int S, const int32_t* __restrict__ ev, int lo, int hi,
                              Emit emit, int out_cap, int out_start) {
-  __shared__ int wtot[32];
-  __shared__ int running;
+  __shared__ int wsum[kCompactThreads / 32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nw = blockDim.x >> 5;
-  if (tid == 0) running = out_start;
-  __syncthreads();
-  for (int c0 = 0; c0 < n; c0 += blockDim.x) {
-    int i = c0 + tid;
-    int pos = 0, e = 0;
-    bool keep = false;
-    if (i < n) {
-      pos = cand(i);
-      if (pos >= 0 && pos < S) {
-        e = ev[pos];
-        keep = e > lo && e <= hi;
+  constexpr int nw = kCompactThreads / 32;
+  int running = out_start;
+  for (int c0 = 0; c0 < n; c0 += kCompactThreads * kCompactItems) {
+    int pos[kCompactItems], e[kCompactItems];
+    int cnt = 0;
+#pragma unroll
+    for (int u = 0; u < kCompactItems; ++u) {
+      const int i = c0 + tid * kCompactItems + u;
+      pos[u] = -1;
+      e[u] = 0;
+      if (i < n) {
+        const int pp = cand(i);
+        if (pp >= 0 && pp < S) {
+          pos[u] = pp;
+          e[u] = ev[pp];
+        }
       }
     }
-    uint32_t bal = __ballot_sync(0xffffffffu, keep);
-    if (lane == 0) wtot[warp] = __popc(bal);
-    __syncthreads();
-    int before = running;
-    for (int w2 = 0; w2 < warp; ++w2) before += wtot[w2];
-    before += __popc(bal & ((1u << lane) - 1u));
-    if (keep && before < out_cap) emit(before, pos, e);
-    __syncthreads();
-    if (tid == 0) {
-      int tot = 0;
-      for (int w2 = 0; w2 < nw; ++w2) tot += wtot[w2];
-      running += tot;
+#pragma unroll
+    for (int u = 0; u < kCompactItems; ++u) {
+      const bool keep = pos[u] >= 0 && e[u] > lo && e[u] <= hi;
+      if (!keep) pos[u] = -1;
+      cnt += keep;
     }
+    // block exclusive scan of cnt
+    int x = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[warp] = x;
     __syncthreads();
+    int before = 0, total = 0;
+#pragma unroll 4
+    for (int w2 = 0; w2 < nw; ++w2) {
+      const int v = wsum[w2];
+      before += w2 < warp ? v : 0;
+      total += v;
+    }
+    int slot = running + before + x - cnt;
+#pragma unroll
+    for (int u = 0; u < kCompactItems; ++u)
+      if (pos[u] >= 0) {
+        if (slot < out_cap) emit(slot, pos[u], e[u]);
+        ++slot;
+      }
+    running += total;
+    __syncthreads();  // wsum is reused by the next chunk
   }
   return running;
 }
 
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kCompactThreads)
     lists_group_base(const int32_t* __restrict__ evict_at, int S, int s, int w, int k,
                      int ngroups, int32_t* __restrict__ gbase, int32_t* __restrict__ gcount,
                      int* status) {
@@ -448,7 +474,7 @@ __global__ void __launch_bounds__(256)
 // List j: keys of E(64 j) held at row 64 j as (position, evict_at) pairs --
 // first those held through row 64 j + 63, then those dropped inside the block,
 // each group in increasing position.
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kCompactThreads)
     lists_build(const int32_t* __restrict__ evict_at, int S, int s, int w, int k, int nL,
                 int ngroups, const int32_t* __restrict__ gbase, const int32_t* __restrict__ gcount,
                 int2* __restrict__ lists, int* status) {
@@ -650,9 +676,9 @@ extern "C" kvpop_status kvpop_mask(const float* prio, int b, int H, int S, kvpop
   evict_search<<<nb, tb, 0, cs>>>(rank, tau, S, bud.s, bud.w, p.nseg, evict_at);
   // 4. lists
   if (lists != nullptr && bud.k > 0) {
-    lists_group_base<<<dim3(p.ngroups, p.nseg), 256, 0, cs>>>(evict_at, S, bud.s, bud.w, bud.k,
+    lists_group_base<<<dim3(p.ngroups, p.nseg), kCompactThreads, 0, cs>>>(evict_at, S, bud.s, bud.w, bud.k,
                                                               p.ngroups, gbase, gcount, status);
-    lists_build<<<dim3(p.nL, p.nseg), 256, 0, cs>>>(evict_at, S, bud.s, bud.w, bud.k, p.nL,
+    lists_build<<<dim3(p.nL, p.nseg), kCompactThreads, 0, cs>>>(evict_at, S, bud.s, bud.w, bud.k, p.nL,
                                                     p.ngroups, gbase, gcount,
                                                     reinterpret_cast<int2*>(lists), status);
   }
