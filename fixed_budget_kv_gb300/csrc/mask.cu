@@ -392,17 +392,18 @@ __global__ void evict_search(const int32_t* __restrict__ rank, const int32_t* __
 // Each thread takes kCompactItems consecutive candidates of a chunk (their
 // evict_at loads in flight together); one block-wide exclusive scan of the
 // per-thread counts per chunk keeps the order.  All threads of the block call it.
-constexpr int kCompactThreads = 1024;
+constexpr int kGroupThreads = 1024;  // group bases: long scans (up to S candidates)
+constexpr int kListThreads = 256;    // lists: k + 1024 candidates at most, many blocks
 constexpr int kCompactItems = 4;
 
-template <typename Cand, typename Emit>
+template <int THREADS, typename Cand, typename Emit>
 __device__ int compact_alive(Cand cand, int n, int S, const int32_t* __restrict__ ev, int lo, int hi,
                              Emit emit, int out_cap, int out_start) {
-  __shared__ int wsum[kCompactThreads / 32];
+  __shared__ int wsum[THREADS / 32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  constexpr int nw = kCompactThreads / 32;
+  constexpr int nw = THREADS / 32;
   int running = out_start;
-  for (int c0 = 0; c0 < n; c0 += kCompactThreads * kCompactItems) {
+  for (int c0 = 0; c0 < n; c0 += THREADS * kCompactItems) {
     int pos[kCompactItems], e[kCompactItems];
     int cnt = 0;
 #pragma unroll
@@ -453,7 +454,7 @@ __device__ int compact_alive(Cand cand, int n, int S, const int32_t* __restrict_
   return running;
 }
 
-__global__ void __launch_bounds__(kCompactThreads)
+__global__ void __launch_bounds__(kGroupThreads)
     lists_group_base(const int32_t* __restrict__ evict_at, int S, int s, int w, int k,
                      int ngroups, int32_t* __restrict__ gbase, int32_t* __restrict__ gcount,
                      int* status) {
@@ -463,7 +464,7 @@ __global__ void __launch_bounds__(kCompactThreads)
   const int32_t* ev = evict_at + (size_t)seg * S;
   const int n = x0 >= s ? x0 - s + 1 : 0;
   int32_t* out = gbase + ((size_t)seg * ngroups + g) * k;
-  int cnt = compact_alive([=](int i) { return s + i; }, n, S, ev, q0, 0x7fffffff,
+  int cnt = compact_alive<kGroupThreads>([=](int i) { return s + i; }, n, S, ev, q0, 0x7fffffff,
                           [=](int slot, int pos, int) { out[slot] = pos; }, k, 0);
   if (threadIdx.x == 0) {
     gcount[(size_t)seg * ngroups + g] = cnt;
@@ -474,7 +475,7 @@ __global__ void __launch_bounds__(kCompactThreads)
 // List j: keys of E(64 j) held at row 64 j as (position, evict_at) pairs --
 // first those held through row 64 j + 63, then those dropped inside the block,
 // each group in increasing position.
-__global__ void __launch_bounds__(kCompactThreads)
+__global__ void __launch_bounds__(kListThreads)
     lists_build(const int32_t* __restrict__ evict_at, int S, int s, int w, int k, int nL,
                 int ngroups, const int32_t* __restrict__ gbase, const int32_t* __restrict__ gcount,
                 int2* __restrict__ lists, int* status) {
@@ -491,8 +492,8 @@ __global__ void __launch_bounds__(kCompactThreads)
   int2* out = lists + ((size_t)seg * nL + j) * k;
   auto cand = [=](int i) { return i < nb ? gb[i] : r0 + (i - nb); };
   auto emit = [=](int slot, int pos, int e) { out[slot] = make_int2(pos, e); };
-  const int na = compact_alive(cand, nb + nr, S, ev, q1, 0x7fffffff, emit, k, 0);
-  const int cnt = compact_alive(cand, nb + nr, S, ev, q0, q1, emit, k, na);
+  const int na = compact_alive<kListThreads>(cand, nb + nr, S, ev, q1, 0x7fffffff, emit, k, 0);
+  const int cnt = compact_alive<kListThreads>(cand, nb + nr, S, ev, q0, q1, emit, k, na);
   if (threadIdx.x == 0) {
     const int expect = min(k, x0 >= s ? x0 - s + 1 : 0);
     if (cnt != expect) report_error(status, KVPOP_ERR_INTERNAL, SITE_INTERNAL_CHECK, 2);
@@ -676,9 +677,9 @@ extern "C" kvpop_status kvpop_mask(const float* prio, int b, int H, int S, kvpop
   evict_search<<<nb, tb, 0, cs>>>(rank, tau, S, bud.s, bud.w, p.nseg, evict_at);
   // 4. lists
   if (lists != nullptr && bud.k > 0) {
-    lists_group_base<<<dim3(p.ngroups, p.nseg), kCompactThreads, 0, cs>>>(evict_at, S, bud.s, bud.w, bud.k,
+    lists_group_base<<<dim3(p.ngroups, p.nseg), kGroupThreads, 0, cs>>>(evict_at, S, bud.s, bud.w, bud.k,
                                                               p.ngroups, gbase, gcount, status);
-    lists_build<<<dim3(p.nL, p.nseg), kCompactThreads, 0, cs>>>(evict_at, S, bud.s, bud.w, bud.k, p.nL,
+    lists_build<<<dim3(p.nL, p.nseg), kListThreads, 0, cs>>>(evict_at, S, bud.s, bud.w, bud.k, p.nL,
                                                     p.ngroups, gbase, gcount,
                                                     reinterpret_cast<int2*>(lists), status);
   }
