@@ -29,8 +29,8 @@ namespace kvpop {
 namespace {
 
 constexpr int kSortThreads = 256;
-constexpr int kSortItems = 8;
-constexpr int kSortTile = kSortThreads * kSortItems;  // 2048
+constexpr int kSortItems = 4;
+constexpr int kSortTile = kSortThreads * kSortItems;  // 1024
 constexpr int kListGroup = 16;                         // lists per group base
 constexpr int kWmThreads = 1024;
 constexpr int kMaxClusterCtas = 8;
