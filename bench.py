@@ -58,7 +58,7 @@ def job_throughput(units_per_rank: float, world: int, step_ms_max: float) -> flo
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="kvpop", choices=["kvpop", "reference"])
     ap.add_argument("--workload", default="qwen3-4b-layer-prefill")
@@ -102,7 +102,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "10"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -426,11 +426,12 @@ def run_decode(args, dev, pk, world=1):
     if world > 1:
         torch.distributed.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for i in range(steps):
-        cache.step(qn[i], kn[i], vn[i], pn[i], out=(O, lse, evd))
-    e1.record()
-    torch.cuda.synchronize()
+    with ClockSampler(dev.index or 0) as clk:
+        e0.record()
+        for i in range(steps):
+            cache.step(qn[i], kn[i], vn[i], pn[i], out=(O, lse, evd))
+        e1.record()
+        torch.cuda.synchronize()
     ms = max_over_ranks(e0.elapsed_time(e1) / steps, world, dev)
     cache.close()
     bytes_step = n * H * wl.B * D * 2 * 2
@@ -441,7 +442,8 @@ def run_decode(args, dev, pk, world=1):
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                          "frac": round(gbs / pk["hbm_gbs"], 4), "traffic": TRAFFIC_BYTES["decode"],
                          "algorithmic_bytes_per_step": bytes_step,
-                         "note": "whole step (update + split attention + combine) timed with CUDA events"}}
+                         "note": "whole step (update + split attention + combine) timed with CUDA events"},
+            "clocks": clk.summary()}
 
 
 # ----------------------------------------------------------------------------
