@@ -1,7 +1,9 @@
 // kvpop_attn_fwd: causal GQA attention over the fixed-budget retained set
 // (sparse) or over all past tokens (dense), returning O and the log-sum-exp
-// ("KVpop ... 精读笔记", sections 2.1 and 2.3).  The dense LSE-only teacher pass
-// lives in dense_lse.cu.
+// ("KVpop ... 精读笔记", sections 2.1 and 2.3).  This file holds the entry point,
+// the sparse kernel for D = 64 and the dense kernel with O; the sparse kernel
+// for D = 128 (CTA pairs) is in attn_pair.cu and the dense LSE-only teacher pass
+// in dense_lse.cu.
 //
 // Persistent: one CTA per SM walks the work items with a stride of the grid
 // size.  An item is two 128-row query tiles of one (batch, KV head); a row is
@@ -721,6 +723,6 @@ extern "C" kvpop_status kvpop_attn_fwd(const void* q, const void* k, const void*
   prm.kk = bud.k;
   prm.nL = (S + KVPOP_LIST_QBLOCK - 1) / KVPOP_LIST_QBLOCK;
   prm.scale_log2 = scale_log2;
-  if (sparse) return D == 128 ? launch<128, true>(prm, cs) : launch<64, true>(prm, cs);
+  if (sparse) return launch<64, true>(prm, cs);  // D = 128 runs on CTA pairs (attn_pair.cu)
   return D == 128 ? launch<128, false>(prm, cs) : launch<64, false>(prm, cs);
 }
