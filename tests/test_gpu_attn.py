@@ -48,6 +48,8 @@ CASES = [
     (1, 1, 8, 128, 400, 2, 17, 33),       # G = 8
     (1, 1, 1, 128, 300, 1, 40, 60),       # G = 1
     (1, 1, 4, 128, 600, 8, 16, 2000),     # budget covers the sequence
+    (1, 1, 16, 128, 350, 3, 24, 40),      # G = 16: 8 positions per query tile
+    (2, 3, 2, 128, 520, 5, 40, 70),       # G = 2, three KV heads, two sequences
 ]
 
 
