@@ -1,6 +1,7 @@
 // Sparse attention forward on CTA pairs (tcgen05 cta_group::2), head dim 128:
 // the retained-set attention of "KVpop ... 精读笔记", sections 2.1 and 2.3, the same
-// computation as attn_kernel<128, true> in attn.cu, laid out for two SMs.
+// computation as the single-CTA attn_kernel in attn.cu (which serves D = 64),
+// laid out for two SMs.
 //
 // A cluster of two CTAs on one TPC is persistent and walks work items with a
 // stride of the number of clusters.  An item is two 256-row query tiles u of
@@ -505,19 +506,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float inv = l > 0.0f ? 1.0f / l : 0.0f;
       __nv_bfloat16* orow = p.O + (((size_t)x.b * S + q) * p.Hq + jh) * 128;
-      uint32_t pk[64];
+      // all 128 columns in flight at once; O's TMEM goes back before the conversion
+      uint32_t orr[4][32];
 #pragma unroll
-      for (int cd = 0; cd < 4; ++cd) {
-        uint32_t r[32];
-        tmem_ld32(tl + o_col + cd * 32, r);
-        tmem_wait_ld_dep(r);
+      for (int cd = 0; cd < 4; ++cd) tmem_ld32(tl + o_col + cd * 32, orr[cd]);
 #pragma unroll
-        for (int c = 0; c < 32; c += 2)
-          pk[cd * 16 + (c >> 1)] = pack_bf16x2(__uint_as_float(r[c]) * inv, __uint_as_float(r[c + 1]) * inv);
-      }
+      for (int cd = 0; cd < 4; ++cd) tmem_wait_ld_dep(orr[cd]);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(oe_bar);
+      uint32_t pk[64];
+#pragma unroll
+      for (int cd = 0; cd < 4; ++cd)
+#pragma unroll
+        for (int c = 0; c < 32; c += 2)
+          pk[cd * 16 + (c >> 1)] =
+              pack_bf16x2(__uint_as_float(orr[cd][c]) * inv, __uint_as_float(orr[cd][c + 1]) * inv);
       if (q <= x.qb1) {
         uint4* dst = reinterpret_cast<uint4*>(orow);
 #pragma unroll
