@@ -15,7 +15,9 @@
 // index wins ties), 8 bits per pass with a shared-memory histogram fed by
 // warp-aggregated increments, stopping as soon as one candidate is left.  Up to
 // 16384 candidates per row the keys stay in registers across the passes and the
-// previous row's cutoff is tried first as a pivot.  The
+// previous row's cutoff is tried first as a pivot: one counting pass tells how
+// far the cutoff moved, and a move of up to kWalk places is followed key by key
+// (block-wide minimum or maximum beyond the pivot) instead of a full select.  The
 // decayed score is computed in fp32 with one rounding after the product and one
 // after the sum (no contraction), -0 read as +0 and NaN as -inf, so the integer
 // outputs are exactly those of that definition.
@@ -29,6 +31,7 @@ namespace {
 constexpr int kLabelThreads = 512;
 constexpr int kLabelRowsPerCta = 64;
 constexpr int kCacheFloats = 32768;  // targets kept in shared memory when S fits (128 KB)
+constexpr int kWalk = 16;            // largest cutoff move followed key by key
 
 __device__ __forceinline__ float decayed_score(float r, int q, int t, int n, float lg) {
   const float m = (float)((q - t) / n);
@@ -204,6 +207,25 @@ __global__ void __launch_bounds__(kLabelThreads)
     __syncthreads();
     return tot;
   };
+  // block-wide minimum (up) or maximum of a 64-bit key
+  __shared__ unsigned long long red64[kLabelThreads / 32];
+  auto block_extreme = [&](unsigned long long v, bool up) -> unsigned long long {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long u = __shfl_xor_sync(0xffffffffu, v, o);
+      v = up ? (u < v ? u : v) : (u > v ? u : v);
+    }
+    if (lane == 0) red64[warp] = v;
+    __syncthreads();
+    unsigned long long r = red64[0];
+#pragma unroll
+    for (int i = 1; i < kLabelThreads / 32; ++i) {
+      const unsigned long long u = red64[i];
+      r = up ? (u < r ? u : r) : (u > r ? u : r);
+    }
+    __syncthreads();
+    return r;
+  };
   int prev = -1;  // the previous row's cutoff
   for (int q = q0; q < q1; ++q) {
     const int tn = q - w;
@@ -233,7 +255,26 @@ __global__ void __launch_bounds__(kLabelThreads)
       int c = 0;
 #pragma unroll
       for (int j = 0; j < CPT; ++j) c += ((valid >> j) & 1u) && kc[j] > pk;
-      if (block_sum(c) == k - 1) found = prev;
+      c = block_sum(c);  // keys above the previous cutoff
+      if (c == k - 1) {
+        found = prev;
+      } else if (c - (k - 1) <= kWalk && (k - 1) - c <= kWalk) {
+        // the cutoff moved by a few places: step key by key from the pivot --
+        // up through the (c - k + 1) smallest keys above it, or down through
+        // the (k - 1 - c) largest keys below it
+        const bool up = c > k - 1;
+        unsigned long long bound = pk;
+        for (int step = up ? c - (k - 1) : (k - 1) - c; step > 0; --step) {
+          unsigned long long best = up ? ~0ull : 0ull;
+#pragma unroll
+          for (int j = 0; j < CPT; ++j) {
+            if (!((valid >> j) & 1u)) continue;
+            if (up ? (kc[j] > bound && kc[j] < best) : (kc[j] < bound && kc[j] > best)) best = kc[j];
+          }
+          bound = block_extreme(best, up);
+        }
+        found = (int)(0xffffffffu - (uint32_t)bound);
+      }
     }
     if (found < 0) {
       unsigned long long prefix = 0, mask = 0;
