@@ -540,6 +540,25 @@ bool make_tmap_rows(CUtensorMap* map, const void* base, uint64_t cols, uint64_t 
 int current_device();
 int num_sms();
 
+// Launch with programmatic dependent launch: the kernel may be scheduled while
+// the previous kernel of the stream drains, and must call grid_dep_wait()
+// before it reads anything that kernel (or any earlier work) wrote.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t cs,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = cs;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // Sparse forward on CTA pairs for D = 128 (csrc/attn_pair.cu); arguments already validated.
 kvpop_status launch_sparse_pair(const void* q, const void* k, const void* v, int b, int S, int Hq, int H,
                                 float scale_log2, const int32_t* evict_at, const int32_t* lists,

@@ -55,6 +55,8 @@ template <bool FIRST>
 __global__ void __launch_bounds__(kSortThreads)
     radix_upsweep(const float* __restrict__ prio, const uint32_t* __restrict__ keys, int S,
                   int shift, int nblk, uint32_t* __restrict__ hist) {
+  grid_dep_wait();  // inputs of earlier kernels of the stream are complete
+  grid_dep_launch();
   __shared__ uint32_t h[256];
   const int seg = blockIdx.y, blk = blockIdx.x, tid = threadIdx.x;
   h[tid] = 0;
@@ -74,6 +76,8 @@ __global__ void __launch_bounds__(kSortThreads)
 
 // Exclusive scan of hist[seg][digit][blk] in (digit, blk) order.
 __global__ void __launch_bounds__(1024) radix_scan(uint32_t* __restrict__ hist, int nblk) {
+  grid_dep_wait();  // inputs of earlier kernels of the stream are complete
+  grid_dep_launch();
   __shared__ uint32_t wsum[32];
   const int seg = blockIdx.x, tid = threadIdx.x;
   const int n = 256 * nblk;
@@ -118,6 +122,8 @@ __global__ void __launch_bounds__(kSortThreads)
                     const int32_t* __restrict__ idx_in, int S, int shift, int nblk,
                     const uint32_t* __restrict__ hist, uint32_t* __restrict__ keys_out,
                     int32_t* __restrict__ idx_out, int32_t* __restrict__ rank_out, int* status) {
+  grid_dep_wait();  // inputs of earlier kernels of the stream are complete
+  grid_dep_launch();
   constexpr int W = kSortThreads / 32;
   __shared__ uint32_t wcnt[W][256];
   __shared__ uint32_t wpre[W][256];
@@ -186,6 +192,8 @@ __global__ void __launch_bounds__(kSortThreads)
 __global__ void __launch_bounds__(kWmThreads)
     wavelet_build(const int32_t* __restrict__ rank, int S, int L, int slice, int nwords,
                   uint2* __restrict__ wm, int32_t* __restrict__ zeros, int* status) {
+  grid_dep_wait();  // inputs of earlier kernels of the stream are complete
+  grid_dep_launch();
   cg::cluster_group cluster = cg::this_cluster();
   const int csize = (int)cluster.num_blocks();
   const int crank = (int)cluster.block_rank();
@@ -320,6 +328,8 @@ __device__ __forceinline__ int wm_rank1(const uint2* lvl, int i) {
 __global__ void tau_query(const uint2* __restrict__ wm, const int32_t* __restrict__ zeros, int S,
                           int L, int nwords, int s, int w, int k, int nseg,
                           int32_t* __restrict__ tau, int* status) {
+  grid_dep_wait();  // inputs of earlier kernels of the stream are complete
+  grid_dep_launch();
   const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (gid >= (long long)nseg * S) return;
   const int seg = (int)(gid / S), q = (int)(gid % S);
@@ -364,6 +374,8 @@ __global__ void tau_query(const uint2* __restrict__ wm, const int32_t* __restric
 
 __global__ void evict_search(const int32_t* __restrict__ rank, const int32_t* __restrict__ tau,
                              int S, int s, int w, int nseg, int32_t* __restrict__ ev) {
+  grid_dep_wait();  // inputs of earlier kernels of the stream are complete
+  grid_dep_launch();
   const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (gid >= (long long)nseg * S) return;
   const int seg = (int)(gid / S), t = (int)(gid % S);
@@ -458,6 +470,8 @@ __global__ void __launch_bounds__(kGroupThreads)
     lists_group_base(const int32_t* __restrict__ evict_at, int S, int s, int w, int k,
                      int ngroups, int32_t* __restrict__ gbase, int32_t* __restrict__ gcount,
                      int* status) {
+  grid_dep_wait();  // inputs of earlier kernels of the stream are complete
+  grid_dep_launch();
   const int g = blockIdx.x, seg = blockIdx.y;
   const int q0 = g * kListGroup * KVPOP_LIST_QBLOCK;
   const int x0 = q0 - w;
@@ -479,6 +493,8 @@ __global__ void __launch_bounds__(kListThreads)
     lists_build(const int32_t* __restrict__ evict_at, int S, int s, int w, int k, int nL,
                 int ngroups, const int32_t* __restrict__ gbase, const int32_t* __restrict__ gcount,
                 int2* __restrict__ lists, int* status) {
+  grid_dep_wait();  // inputs of earlier kernels of the stream are complete
+  grid_dep_launch();
   const int j = blockIdx.x, seg = blockIdx.y;
   const int g = j / kListGroup;
   const int q0 = j * KVPOP_LIST_QBLOCK, x0 = q0 - w;
@@ -628,19 +644,19 @@ extern "C" kvpop_status kvpop_mask(const float* prio, int b, int H, int S, kvpop
     uint32_t* kout = keys[pass & 1];
     int32_t* iout = idx[pass & 1];
     if (pass == 0)
-      radix_upsweep<true><<<sgrid, kSortThreads, 0, cs>>>(prio, nullptr, S, shift, p.nblk, hist);
+      launch_pdl(radix_upsweep<true>, sgrid, dim3(kSortThreads), 0, cs, prio, nullptr, S, shift, p.nblk, hist);
     else
-      radix_upsweep<false><<<sgrid, kSortThreads, 0, cs>>>(nullptr, kin, S, shift, p.nblk, hist);
-    radix_scan<<<p.nseg, 1024, 0, cs>>>(hist, p.nblk);
+      launch_pdl(radix_upsweep<false>, sgrid, dim3(kSortThreads), 0, cs, nullptr, kin, S, shift, p.nblk, hist);
+    launch_pdl(radix_scan, dim3(p.nseg), dim3(1024), 0, cs, hist, p.nblk);
     if (pass == 0)
-      radix_downsweep<true, false><<<sgrid, kSortThreads, 0, cs>>>(prio, nullptr, nullptr, S, shift,
-                                                                   p.nblk, hist, kout, iout, nullptr, status);
+      launch_pdl(radix_downsweep<true, false>, sgrid, dim3(kSortThreads), 0, cs, prio, nullptr, nullptr, S, shift,
+                 p.nblk, hist, kout, iout, nullptr, status);
     else if (pass < 3)
-      radix_downsweep<false, false><<<sgrid, kSortThreads, 0, cs>>>(nullptr, kin, iin, S, shift,
-                                                                    p.nblk, hist, kout, iout, nullptr, status);
+      launch_pdl(radix_downsweep<false, false>, sgrid, dim3(kSortThreads), 0, cs, nullptr, kin, iin, S, shift,
+                 p.nblk, hist, kout, iout, nullptr, status);
     else
-      radix_downsweep<false, true><<<sgrid, kSortThreads, 0, cs>>>(nullptr, kin, iin, S, shift,
-                                                                   p.nblk, hist, nullptr, nullptr, rank, status);
+      launch_pdl(radix_downsweep<false, true>, sgrid, dim3(kSortThreads), 0, cs, nullptr, kin, iin, S, shift,
+                 p.nblk, hist, nullptr, nullptr, rank, status);
   }
   st = cuda_check(cudaGetLastError(), "kvpop_mask: rank kernels");
   if (st != KVPOP_OK) return st;
@@ -657,13 +673,15 @@ extern "C" kvpop_status kvpop_mask(const float* prio, int b, int H, int S, kvpop
     cfg.blockDim = dim3(kWmThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = cs;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = p.csize;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     st = cuda_check(cudaLaunchKernelEx(&cfg, wavelet_build, (const int32_t*)rank, S, p.L, p.slice,
                                        p.nwords, wm, zeros, status),
                     "kvpop_mask: wavelet build");
@@ -672,16 +690,16 @@ extern "C" kvpop_status kvpop_mask(const float* prio, int b, int H, int S, kvpop
   const long long total = (long long)p.nseg * S;
   const int tb = 256;
   const unsigned nb = (unsigned)((total + tb - 1) / tb);
-  tau_query<<<nb, tb, 0, cs>>>(wm, zeros, S, p.L, p.nwords, bud.s, bud.w, bud.k, p.nseg, tau, status);
+  launch_pdl(tau_query, dim3(nb), dim3(tb), 0, cs, wm, zeros, S, p.L, p.nwords, bud.s, bud.w, bud.k, p.nseg, tau,
+             status);
   // 3. evict_at
-  evict_search<<<nb, tb, 0, cs>>>(rank, tau, S, bud.s, bud.w, p.nseg, evict_at);
+  launch_pdl(evict_search, dim3(nb), dim3(tb), 0, cs, rank, tau, S, bud.s, bud.w, p.nseg, evict_at);
   // 4. lists
   if (lists != nullptr && bud.k > 0) {
-    lists_group_base<<<dim3(p.ngroups, p.nseg), kGroupThreads, 0, cs>>>(evict_at, S, bud.s, bud.w, bud.k,
-                                                              p.ngroups, gbase, gcount, status);
-    lists_build<<<dim3(p.nL, p.nseg), kListThreads, 0, cs>>>(evict_at, S, bud.s, bud.w, bud.k, p.nL,
-                                                    p.ngroups, gbase, gcount,
-                                                    reinterpret_cast<int2*>(lists), status);
+    launch_pdl(lists_group_base, dim3(p.ngroups, p.nseg), dim3(kGroupThreads), 0, cs, evict_at, S, bud.s, bud.w,
+               bud.k, p.ngroups, gbase, gcount, status);
+    launch_pdl(lists_build, dim3(p.nL, p.nseg), dim3(kListThreads), 0, cs, evict_at, S, bud.s, bud.w, bud.k, p.nL,
+               p.ngroups, gbase, gcount, reinterpret_cast<int2*>(lists), status);
   }
   return cuda_check(cudaGetLastError(), "kvpop_mask: launch");
 }
