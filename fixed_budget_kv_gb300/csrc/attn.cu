@@ -184,6 +184,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  // the previous kernel of the stream may still be running (programmatic
+  // launch): wait for it before any global access; this CTA already holds its
+  // tensor memory, so the next kernel may be scheduled
+  grid_dep_wait();
+  grid_dep_launch();
 
   auto fail = [&](int site, int detail) {
     report_error(p.status, KVPOP_ERR_TIMEOUT, site, detail);
@@ -625,8 +630,7 @@ kvpop_status launch(const AttnParams& prm, cudaStream_t stream) {
   }
   // persistent: one CTA per SM walks the items with a stride of the grid size
   dim3 grid(min(prm.nitems, num_sms()));
-  kern<<<grid, kThreads, L::total, stream>>>(prm);
-  return cuda_check(cudaGetLastError(), "kvpop_attn_fwd: launch");
+  return cuda_check(launch_pdl(kern, grid, dim3(kThreads), L::total, stream, prm), "kvpop_attn_fwd: launch");
 }
 
 }  // namespace

@@ -153,6 +153,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_sync();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  // the previous kernel of the stream may still be running (programmatic
+  // launch): wait for it before any global access; this CTA already holds its
+  // tensor memory, so the next kernel may be scheduled
+  grid_dep_wait();
+  grid_dep_launch();
 
   auto fail = [&](int site, int detail) {
     report_error(p.status, KVPOP_ERR_TIMEOUT, site, detail);
@@ -603,8 +608,8 @@ kvpop_status launch_sparse_pair(const void* q, const void* k, const void* v, int
   }
   // persistent: one cluster per TPC walks the items with a stride of the cluster count
   const int clusters = min(prm.nitems, max(1, num_sms() / 2));
-  kern<<<2 * clusters, kThreads, PLayout::total, cs>>>(prm);
-  return cuda_check(cudaGetLastError(), "kvpop_attn_fwd: launch");
+  return cuda_check(launch_pdl(kern, dim3(2 * clusters), dim3(kThreads), PLayout::total, cs, prm),
+                    "kvpop_attn_fwd: launch");
 }
 
 }  // namespace kvpop

@@ -113,6 +113,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_sync();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  // the previous kernel of the stream may still be running (programmatic
+  // launch): wait for it before any global access; this CTA already holds its
+  // tensor memory, so the next kernel may be scheduled
+  grid_dep_wait();
+  grid_dep_launch();
   auto fail = [&](int site, int detail) {
     report_error(p.status, KVPOP_ERR_TIMEOUT, site, detail);
     *abort_flag = 1;
@@ -263,8 +268,8 @@ kvpop_status launch_d(const LseParams& prm, cudaStream_t cs) {
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::total),
       "dense LSE: smem attribute");
   if (st != KVPOP_OK) return st;
-  kern<<<2 * prm.npb * prm.nbh, kThreads, L::total, cs>>>(prm);
-  return cuda_check(cudaGetLastError(), "dense LSE: launch");
+  return cuda_check(launch_pdl(kern, dim3(2 * prm.npb * prm.nbh), dim3(kThreads), L::total, cs, prm),
+                    "dense LSE: launch");
 }
 
 }  // namespace

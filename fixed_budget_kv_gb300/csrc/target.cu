@@ -62,6 +62,8 @@ struct TBars {
 
 __global__ void lse_prep(const float* __restrict__ lse, int b, int H, int G, int S, int Spad,
                          float* __restrict__ lse2) {
+  grid_dep_wait();
+  grid_dep_launch();
   const long long n = (long long)b * H * Spad * G;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x) {
@@ -77,6 +79,8 @@ __global__ void lse_prep(const float* __restrict__ lse, int b, int H, int G, int
 }
 
 __global__ void target_finalize(float* __restrict__ t, long long n) {
+  grid_dep_wait();
+  grid_dep_launch();
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x) {
     const float s = t[i];
@@ -139,6 +143,11 @@ __global__ void __launch_bounds__(kThreads, 1) target_kernel(const __grid_consta
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  // the previous kernel of the stream may still be running (programmatic
+  // launch): wait for it before any global access; this CTA already holds its
+  // tensor memory, so the next kernel may be scheduled
+  grid_dep_wait();
+  grid_dep_launch();
   auto fail = [&](int site, int detail) {
     report_error(p.status, KVPOP_ERR_TIMEOUT, site, detail);
     *abort_flag = 1;
@@ -312,8 +321,7 @@ kvpop_status launch_target(const TargetParams& prm, int b, int H, cudaStream_t c
   if (st != KVPOP_OK) return st;
   const int nrb = (prm.S + 128 * kNR - 1) / (128 * kNR);
   dim3 grid(prm.nchunk, nrb, b * H);
-  kern<<<grid, kThreads, L::total, cs>>>(prm);
-  return cuda_check(cudaGetLastError(), "kvpop_future_target: launch");
+  return cuda_check(launch_pdl(kern, grid, dim3(kThreads), L::total, cs, prm), "kvpop_future_target: launch");
 }
 
 }  // namespace
@@ -405,13 +413,15 @@ extern "C" kvpop_status kvpop_future_target(const void* q, const void* k, const 
   if (st != KVPOP_OK) return st;
   const long long n = (long long)b * H * prm.Spad * G;
   const int blocks = (int)std::min<long long>((n + 255) / 256, 4096);
-  lse_prep<<<blocks, 256, 0, cs>>>(lse, b, H, G, S, prm.Spad, static_cast<float*>(workspace));
-  st = cuda_check(cudaGetLastError(), "kvpop_future_target: lse prep");
+  st = cuda_check(launch_pdl(lse_prep, dim3(blocks), dim3(256), 0, cs, lse, b, H, G, S, prm.Spad,
+                             static_cast<float*>(workspace)),
+                  "kvpop_future_target: lse prep");
   if (st != KVPOP_OK) return st;
   st = D == 128 ? launch_target<128>(prm, b, H, cs) : launch_target<64>(prm, b, H, cs);
   if (st != KVPOP_OK) return st;
-  target_finalize<<<(int)std::min<long long>((nout + 255) / 256, 4096), 256, 0, cs>>>(target, nout);
-  return cuda_check(cudaGetLastError(), "kvpop_future_target: finalize");
+  return cuda_check(launch_pdl(target_finalize, dim3((int)std::min<long long>((nout + 255) / 256, 4096)), dim3(256),
+                               0, cs, target, nout),
+                    "kvpop_future_target: finalize");
 }
 
 // ---------------------------------------------------------------------------
