@@ -11,6 +11,8 @@ Every function restates a definition from the KVpop pages:
   * running threshold with a Fenwick tree -- "KVpop — 基于预测性在线剪枝的键值缓存压缩",
     section 2.4;
   * softmax attention and its log-sum-exp -- "KVpop ... 精读笔记", section 2.3;
+  * the gradient of that attention (the student is trained through the
+    sparse attention) -- "KVpop ... 精读笔记", section 2.1, Figure 1;
   * future-attention mass and Eq. (8) -- "KVpop ... 精读笔记", sections 2.2-2.3;
   * decode-time eviction at the window boundary -- "KVpop ... 精读笔记",
     section 2.4 (token u = q - w leaves the window) and section 2.3;
@@ -62,6 +64,11 @@ def _load():
         _lib.oracle_evict_at_sweep.argtypes = [P, P, i32, i32, i32, i32, P]
         _lib.oracle_attn_rows.argtypes = [P, P, P, i32, i32, i32, i32, i32, f64, P, P, i32, i32,
                                           P, i64, P, P]
+        _lib.oracle_attn_bwd.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, f64, P, P, i32, i32, P, P, P]
+        _lib.oracle_attn_bwd_rows.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, f64, P, P, i32, i32,
+                                              P, i64, P]
+        _lib.oracle_attn_bwd_keys.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, f64, P, P, i32, i32,
+                                              P, i64, P, P]
         _lib.oracle_target_lse.argtypes = [P, P, P, i32, i32, i32, i32, i32, f64, i32, P, i64, P]
         _lib.oracle_target_colsum.argtypes = [P, P, i32, i32, i32, i32, i32, f64, i32, P]
         _lib.oracle_target_normalize.argtypes = [P, i64, i32, i32, i32, f64, P]
@@ -204,6 +211,64 @@ def attn(q, k, v, scale: float, rank_=None, tau_=None, s=0, w=0, want_o=True):
     if O is not None:
         O = np.transpose(O.reshape(b, Hq, S, D), (0, 2, 1, 3))
     return O, lse
+
+
+def _f32(a):
+    return np.ascontiguousarray(a, dtype=np.float32)
+
+
+def _i32_or_none(a):
+    return None if a is None else np.ascontiguousarray(a, dtype=np.int32)
+
+
+def attn_bwd(q, k, v, dO, scale: float, rank_=None, tau_=None, s=0, w=0):
+    """Gradient of sum(dO * O) through the attention of ``attn`` (sparse when
+    rank/tau are given, dense causal otherwise).  q, dO [b,S,Hq,D]; k, v
+    [b,S,H,D].  Returns dq [b,S,Hq,D], dk, dv [b,S,H,D], all fp64."""
+    lib = _load()
+    q, k, v, dO = _f32(q), _f32(k), _f32(v), _f32(dO)
+    b, S, Hq, D = q.shape
+    H = k.shape[2]
+    dq = np.empty((b, S, Hq, D), dtype=np.float64)
+    dk = np.empty((b, S, H, D), dtype=np.float64)
+    dv = np.empty((b, S, H, D), dtype=np.float64)
+    rk, tu = _i32_or_none(rank_), _i32_or_none(tau_)
+    lib.oracle_attn_bwd(_p(q), _p(k), _p(v), _p(dO), b, S, H, Hq // H, D, float(scale),
+                        None if rk is None else _p(rk), None if tu is None else _p(tu), int(s), int(w),
+                        _p(dq), _p(dk), _p(dv))
+    return dq, dk, dv
+
+
+def attn_bwd_rows(qvecs, dovecs, k, v, G: int, scale: float, rows, rank_=None, tau_=None, s=0, w=0):
+    """dq of explicit rows [n,3] = (batch, query head, position); qvecs/dovecs
+    [n,D] are those rows' query and upstream-gradient vectors.  Returns [n,D]."""
+    lib = _load()
+    qvecs, dovecs, k, v = _f32(qvecs), _f32(dovecs), _f32(k), _f32(v)
+    rows = np.ascontiguousarray(rows, dtype=np.int32).reshape(-1, 3)
+    b, S, H, D = k.shape
+    out = np.empty((rows.shape[0], D), dtype=np.float64)
+    rk, tu = _i32_or_none(rank_), _i32_or_none(tau_)
+    lib.oracle_attn_bwd_rows(_p(qvecs), _p(dovecs), _p(k), _p(v), b, S, H, G, D, float(scale),
+                             None if rk is None else _p(rk), None if tu is None else _p(tu), int(s), int(w),
+                             _p(rows), rows.shape[0], _p(out))
+    return out
+
+
+def attn_bwd_keys(q, k, v, dO, scale: float, keys, rank_=None, tau_=None, s=0, w=0):
+    """dk, dv of explicit keys [n,3] = (batch, KV head, position): each row that
+    retains the key is solved in full.  Returns two [n,D] arrays."""
+    lib = _load()
+    q, k, v, dO = _f32(q), _f32(k), _f32(v), _f32(dO)
+    keys = np.ascontiguousarray(keys, dtype=np.int32).reshape(-1, 3)
+    b, S, Hq, D = q.shape
+    H = k.shape[2]
+    dk = np.empty((keys.shape[0], D), dtype=np.float64)
+    dv = np.empty((keys.shape[0], D), dtype=np.float64)
+    rk, tu = _i32_or_none(rank_), _i32_or_none(tau_)
+    lib.oracle_attn_bwd_keys(_p(q), _p(k), _p(v), _p(dO), b, S, H, Hq // H, D, float(scale),
+                             None if rk is None else _p(rk), None if tu is None else _p(tu), int(s), int(w),
+                             _p(keys), keys.shape[0], _p(dk), _p(dv))
+    return dk, dv
 
 
 # ----------------------------------------------------------------------------

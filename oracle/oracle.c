@@ -276,6 +276,171 @@ void oracle_attn_rows(const float* qv, const float* k, const float* v, int b, in
 }
 
 /* ------------------------------------------------------------------------ */
+/* attention backward                                                        */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * [KVpop notes] 2.1 (Figure 1, training flow): the student runs attention over
+ * the retained set M_{q,.} and is trained through it, so the sparse attention
+ * needs its gradient.  For one row with logits l_t = scale * q.k_t over R_q,
+ * softmax P_t = exp(l_t - LSE) and output O = sum_t P_t v_t, the gradient of a
+ * loss L with upstream dO = dL/dO is the chain rule through the softmax:
+ *   dv_t += P_t dO
+ *   dP_t  = dO . v_t
+ *   dS_t  = P_t (dP_t - sum_u P_u dP_u)          (the softmax Jacobian)
+ *   dq    = scale * sum_t dS_t k_t
+ *   dk_t += scale * dS_t q
+ * This computes one row: idx[] receives the retained keys in position order,
+ * P[] and dS[] their probabilities and logit gradients.  Returns |R_q|.
+ */
+static int row_grad(const float* qrow, const float* dorow, const float* k, const float* v, int bi,
+                    int S, int H, int h, int D, double scale, const int32_t* rk, const int32_t* tu,
+                    int s, int w, int qp, int32_t* idx, double* P, double* dS) {
+    int n = 0;
+    double m = -INFINITY;
+    for (int t = 0; t <= qp; ++t) {
+        if (rk && !retained(rk, tu, s, w, qp, t)) continue;
+        idx[n] = t;
+        P[n] = scale * dot_f(qrow, k + (((size_t)bi * S + t) * H + h) * D, D);
+        if (P[n] > m) m = P[n];
+        ++n;
+    }
+    if (n == 0) return 0;
+    double sum = 0.0;
+    for (int i = 0; i < n; ++i) sum += exp(P[i] - m);
+    double L = m + log(sum);
+    double dsum = 0.0;
+    for (int i = 0; i < n; ++i) {
+        P[i] = exp(P[i] - L);
+        dS[i] = dot_f(dorow, v + (((size_t)bi * S + idx[i]) * H + h) * D, D);
+        dsum += P[i] * dS[i];
+    }
+    for (int i = 0; i < n; ++i) dS[i] = P[i] * (dS[i] - dsum);
+    return n;
+}
+
+/*
+ * Gradients of every row: q, dO [b,S,Hq,D]; k, v [b,S,H,D]; rank/tau [b,H,S]
+ * (NULL => dense causal).  dq [b,S,Hq,D], dk, dv [b,S,H,D] fp64, overwritten.
+ * One (batch, KV head) per thread, so its dk/dv rows have a single writer.
+ */
+void oracle_attn_bwd(const float* q, const float* k, const float* v, const float* dO, int b, int S,
+                     int H, int G, int D, double scale, const int32_t* rank, const int32_t* tau,
+                     int s, int w, double* dq, double* dk, double* dv) {
+    int Hq = H * G;
+    memset(dq, 0, sizeof(double) * (size_t)b * S * Hq * D);
+    memset(dk, 0, sizeof(double) * (size_t)b * S * H * D);
+    memset(dv, 0, sizeof(double) * (size_t)b * S * H * D);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int bh = 0; bh < b * H; ++bh) {
+        int bi = bh / H, h = bh % H;
+        const int32_t* rk = rank ? rank + ((size_t)bi * H + h) * S : NULL;
+        const int32_t* tu = tau ? tau + ((size_t)bi * H + h) * S : NULL;
+        int32_t* idx = (int32_t*)malloc(sizeof(int32_t) * (size_t)S);
+        double* P = (double*)malloc(sizeof(double) * (size_t)S);
+        double* dS = (double*)malloc(sizeof(double) * (size_t)S);
+        for (int g = 0; g < G; ++g) {
+            int j = h * G + g;
+            for (int qp = 0; qp < S; ++qp) {
+                size_t ro = (((size_t)bi * S + qp) * Hq + j) * D;
+                int n = row_grad(q + ro, dO + ro, k, v, bi, S, H, h, D, scale, rk, tu, s, w, qp, idx, P, dS);
+                for (int i = 0; i < n; ++i) {
+                    size_t ko = (((size_t)bi * S + idx[i]) * H + h) * D;
+                    for (int d = 0; d < D; ++d) {
+                        dq[ro + d] += scale * dS[i] * (double)k[ko + d];
+                        dk[ko + d] += scale * dS[i] * (double)q[ro + d];
+                        dv[ko + d] += P[i] * (double)dO[ro + d];
+                    }
+                }
+            }
+        }
+        free(idx);
+        free(P);
+        free(dS);
+    }
+}
+
+/*
+ * dq of explicit rows (batch, query head j, position): qv / dov [nrows, D] are
+ * the rows' query and upstream-gradient vectors.  dq [nrows, D].
+ */
+void oracle_attn_bwd_rows(const float* qv, const float* dov, const float* k, const float* v, int b,
+                          int S, int H, int G, int D, double scale, const int32_t* rank,
+                          const int32_t* tau, int s, int w, const int32_t* rows, int64_t nrows,
+                          double* dq) {
+    (void)b;
+#pragma omp parallel
+    {
+        int32_t* idx = (int32_t*)malloc(sizeof(int32_t) * (size_t)S);
+        double* P = (double*)malloc(sizeof(double) * (size_t)S);
+        double* dS = (double*)malloc(sizeof(double) * (size_t)S);
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t r = 0; r < nrows; ++r) {
+            int bi = rows[3 * r + 0], j = rows[3 * r + 1], qp = rows[3 * r + 2];
+            int h = j / G;
+            const int32_t* rk = rank ? rank + ((size_t)bi * H + h) * S : NULL;
+            const int32_t* tu = tau ? tau + ((size_t)bi * H + h) * S : NULL;
+            int n = row_grad(qv + (size_t)r * D, dov + (size_t)r * D, k, v, bi, S, H, h, D, scale, rk, tu,
+                             s, w, qp, idx, P, dS);
+            double* o = dq + (size_t)r * D;
+            for (int d = 0; d < D; ++d) o[d] = 0.0;
+            for (int i = 0; i < n; ++i) {
+                const float* krow = k + (((size_t)bi * S + idx[i]) * H + h) * D;
+                for (int d = 0; d < D; ++d) o[d] += scale * dS[i] * (double)krow[d];
+            }
+        }
+        free(idx);
+        free(P);
+        free(dS);
+    }
+}
+
+/*
+ * dk, dv of explicit keys (batch, KV head h, position t): every row q >= t of
+ * the G query heads that retains t contributes; each such row is solved in
+ * full.  q, dO [b,S,Hq,D].  dk, dv [nkeys, D].
+ */
+void oracle_attn_bwd_keys(const float* q, const float* k, const float* v, const float* dO, int b,
+                          int S, int H, int G, int D, double scale, const int32_t* rank,
+                          const int32_t* tau, int s, int w, const int32_t* keys, int64_t nkeys,
+                          double* dk, double* dv) {
+    (void)b;
+    int Hq = H * G;
+#pragma omp parallel
+    {
+        int32_t* idx = (int32_t*)malloc(sizeof(int32_t) * (size_t)S);
+        double* P = (double*)malloc(sizeof(double) * (size_t)S);
+        double* dS = (double*)malloc(sizeof(double) * (size_t)S);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t i = 0; i < nkeys; ++i) {
+            int bi = keys[3 * i + 0], h = keys[3 * i + 1], t = keys[3 * i + 2];
+            const int32_t* rk = rank ? rank + ((size_t)bi * H + h) * S : NULL;
+            const int32_t* tu = tau ? tau + ((size_t)bi * H + h) * S : NULL;
+            double* ok = dk + (size_t)i * D;
+            double* ov = dv + (size_t)i * D;
+            for (int d = 0; d < D; ++d) ok[d] = ov[d] = 0.0;
+            for (int qp = t; qp < S; ++qp) {
+                if (rk && !retained(rk, tu, s, w, qp, t)) continue;
+                for (int g = 0; g < G; ++g) {
+                    size_t ro = (((size_t)bi * S + qp) * Hq + h * G + g) * D;
+                    int n = row_grad(q + ro, dO + ro, k, v, bi, S, H, h, D, scale, rk, tu, s, w, qp, idx, P, dS);
+                    for (int u = 0; u < n; ++u) {
+                        if (idx[u] != t) continue;
+                        for (int d = 0; d < D; ++d) {
+                            ok[d] += scale * dS[u] * (double)q[ro + d];
+                            ov[d] += P[u] * (double)dO[ro + d];
+                        }
+                    }
+                }
+            }
+        }
+        free(idx);
+        free(P);
+        free(dS);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* future-attention target                                                   */
 /* ------------------------------------------------------------------------ */
 

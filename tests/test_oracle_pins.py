@@ -257,6 +257,105 @@ def test_attn_head_group_mapping(oracle_mod):
 
 
 # ----------------------------------------------------------------------------
+# attention backward
+# ----------------------------------------------------------------------------
+
+_BWD_BUDGETS = [(3, 8, 10), (0, 0, 12), (2, 6, 0), (1, 0, 5), (4, 200, 200)]
+
+
+@pytest.mark.parametrize("s,w,kk", _BWD_BUDGETS)
+def test_attn_bwd_matches_autograd(oracle_mod, s, w, kk):
+    """The hand-written chain rule against torch autograd (fp64, CPU) of the
+    masked softmax attention written with an explicit mask matrix."""
+    torch = pytest.importorskip("torch")
+    S, H, G, D = 72, 2, 3, 8
+    q, k, v, p = _tiny_inputs(S, H, G, D, seed=31 + kk)
+    p[..., ::7] = p[..., 3:4]                      # ties in the priority order
+    dO = np.random.default_rng(5 + w).standard_normal(q.shape).astype(np.float32)
+    scale = 1 / math.sqrt(D)
+    r, tau, _ = oracle_mod.mask(p, s, w, kk)
+    dq, dk, dv = oracle_mod.attn_bwd(q, k, v, dO, scale, r, tau, s, w)
+    tq = torch.tensor(q, dtype=torch.float64, requires_grad=True)
+    tk = torch.tensor(k, dtype=torch.float64, requires_grad=True)
+    tv = torch.tensor(v, dtype=torch.float64, requires_grad=True)
+    loss = 0
+    for j in range(H * G):
+        h = j // G
+        M = torch.tensor(oracle_mod.mask_dense(r[0, h], tau[0, h], s, w))
+        logits = scale * tq[0, :, j, :] @ tk[0, :, h, :].T
+        logits = logits.masked_fill(~M, float("-inf"))
+        O = torch.softmax(logits, dim=1) @ tv[0, :, h, :]
+        loss = loss + (O * torch.tensor(dO[0, :, j, :], dtype=torch.float64)).sum()
+    loss.backward()
+    assert np.allclose(dq, tq.grad.numpy(), atol=1e-12, rtol=0)
+    assert np.allclose(dk, tk.grad.numpy(), atol=1e-12, rtol=0)
+    assert np.allclose(dv, tv.grad.numpy(), atol=1e-12, rtol=0)
+
+
+def test_attn_bwd_finite_differences(oracle_mod):
+    """Central differences of L = sum(dO * O) through the oracle's forward pass
+    (itself pinned to the library softmax) at sampled input entries."""
+    S, H, G, D = 40, 1, 2, 8
+    s, w, kk = 2, 5, 6
+    q, k, v, p = _tiny_inputs(S, H, G, D, seed=13)
+    dO = np.random.default_rng(3).standard_normal(q.shape).astype(np.float32)
+    scale = 0.4
+    r, tau, _ = oracle_mod.mask(p, s, w, kk)
+    grads = dict(zip("qkv", oracle_mod.attn_bwd(q, k, v, dO, scale, r, tau, s, w)))
+    dO64 = dO.astype(np.float64)
+
+    def loss(qq, kk_, vv):
+        O, _ = oracle_mod.attn(qq, kk_, vv, scale, r, tau, s, w)
+        return float((O * dO64).sum())
+
+    rng = np.random.default_rng(8)
+    for name in "qkv":
+        for _ in range(6):
+            arrs = {"q": q, "k": k, "v": v}
+            idx = tuple(int(rng.integers(0, n)) for n in arrs[name].shape)
+            if name != "q":                        # a key that some row retains
+                idx = (0, int(rng.integers(0, 12)), 0, idx[3])
+            hi = {n: a.copy() for n, a in arrs.items()}
+            lo = {n: a.copy() for n, a in arrs.items()}
+            hi[name][idx] = np.float32(arrs[name][idx] + np.float32(2.0 ** -9))
+            lo[name][idx] = np.float32(arrs[name][idx] - np.float32(2.0 ** -9))
+            step = float(hi[name][idx]) - float(lo[name][idx])
+            fd = (loss(hi["q"], hi["k"], hi["v"]) - loss(lo["q"], lo["k"], lo["v"])) / step
+            assert abs(fd - grads[name][idx]) <= 1e-5 * max(1.0, abs(fd)), (name, idx, fd, grads[name][idx])
+
+
+def test_attn_bwd_invariants(oracle_mod):
+    """Each softmax row's logit gradients sum to zero, so sum_t dk_t = 0 per KV
+    head; each row's probabilities sum to one, so sum_t dv_t = sum over rows of dO."""
+    S, H, G, D = 90, 2, 4, 8
+    s, w, kk = 3, 9, 14
+    q, k, v, p = _tiny_inputs(S, H, G, D, seed=41)
+    dO = np.random.default_rng(6).standard_normal(q.shape).astype(np.float32)
+    r, tau, _ = oracle_mod.mask(p, s, w, kk)
+    _, dk, dv = oracle_mod.attn_bwd(q, k, v, dO, 0.3, r, tau, s, w)
+    assert np.abs(dk.sum(axis=1)).max() < 1e-12
+    ref = dO.astype(np.float64).reshape(1, S, H, G, D).sum(axis=(1, 3))
+    assert np.allclose(dv.sum(axis=1), ref, atol=1e-11, rtol=0)
+
+
+def test_attn_bwd_rows_and_keys_equal_full(oracle_mod):
+    S, H, G, D = 64, 2, 2, 8
+    s, w, kk = 2, 6, 9
+    q, k, v, p = _tiny_inputs(S, H, G, D, seed=2)
+    dO = np.random.default_rng(1).standard_normal(q.shape).astype(np.float32)
+    r, tau, _ = oracle_mod.mask(p, s, w, kk)
+    dq, dk, dv = oracle_mod.attn_bwd(q, k, v, dO, 0.5, r, tau, s, w)
+    rows = np.array([[0, j, t] for j in range(H * G) for t in (0, 1, 7, 30, S - 1)], np.int32)
+    got = oracle_mod.attn_bwd_rows(q[0, rows[:, 2], rows[:, 1]], dO[0, rows[:, 2], rows[:, 1]], k, v, G, 0.5,
+                                   rows, r, tau, s, w)
+    assert np.allclose(got, dq[0, rows[:, 2], rows[:, 1]], atol=1e-13, rtol=0)
+    keys = np.array([[0, h, t] for h in range(H) for t in (0, 1, 5, 20, S - 1)], np.int32)
+    gk, gv = oracle_mod.attn_bwd_keys(q, k, v, dO, 0.5, keys, r, tau, s, w)
+    assert np.allclose(gk, dk[0, keys[:, 2], keys[:, 1]], atol=1e-13, rtol=0)
+    assert np.allclose(gv, dv[0, keys[:, 2], keys[:, 1]], atol=1e-13, rtol=0)
+
+
+# ----------------------------------------------------------------------------
 # future-attention target
 # ----------------------------------------------------------------------------
 
