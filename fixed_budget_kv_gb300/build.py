@@ -16,7 +16,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libkvpop.so")
-SOURCES = ["runtime.cu", "mask.cu", "attn.cu", "attn_pair.cu", "dense_lse.cu", "target.cu", "decode.cu", "labels.cu"]
+SOURCES = ["runtime.cu", "mask.cu", "attn.cu", "attn_pair.cu", "attn_bwd.cu", "dense_lse.cu", "target.cu", "decode.cu",
+           "labels.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

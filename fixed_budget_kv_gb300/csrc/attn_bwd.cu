@@ -1,0 +1,1235 @@
+// kvpop_attn_bwd: gradient of the sparse attention of kvpop_attn_fwd with
+// respect to q, k and v ("KVpop ... 精读笔记", section 2.1 and Figure 1: the
+// student runs attention over the retained set and is trained through it).
+//
+// Per row (position q, query head j) with P_t = exp(scale q.k_t - LSE_q) over
+// the retained set and upstream gradient dO_q:
+//   dv_t += P_t dO_q,   dS_t = P_t (dO_q.v_t - dO_q.O_q),
+//   dq_q  = scale sum_t dS_t k_t,   dk_t += scale dS_t q_q.
+// Row q retains key t exactly when t <= q < evict_at[t].  That set splits
+// without overlap into the band pairs t <= q < t + w (the window; sinks
+// included) and the long pairs t + w <= q < evict_at[t].
+//
+// Four kernels:
+//   bwd_prep   Delta_q = dO_q.O_q and LSE_q in log2 units, in the order
+//              [b, H, Spad, G]: one 128-row query tile (128/G positions x G
+//              heads) is 512 contiguous bytes; padded rows get LSE = +inf.
+//   bwd_keys   per block of kRows query positions and KV head, the keys that
+//              hold a long pair with a row of the block: sinks, the long-range
+//              list at the block's first row, and the keys entering the top-k
+//              inside the block (evict_at[t] > t + w).
+//   bwd_dq     query-major, the forward's key plan (sinks, long-range list,
+//              span): S = Q K^T and dP = dO V^T in TMEM, dS in bf16 written
+//              over S, dQ += dS K accumulated in TMEM over the key tiles.
+//   bwd_dkdv   key-major: the 128 keys of an item are the TMEM lanes and the
+//              query rows stream by in 64-row halves: S^T = K Q^T and
+//              dP^T = V dO^T, P^T and dS^T in bf16 written over them,
+//              dV += P^T dO and dK += dS^T Q.  Launched twice: band items (128
+//              consecutive keys against rows t <= q < t + w) store dk and dv;
+//              long items (128 keys of a block's list against the block's
+//              rows, t + w <= q < evict_at[t]) add theirs with fp32 atomics.
+#include "common.cuh"
+
+namespace kvpop {
+namespace {
+
+constexpr int kThreads = 384;
+constexpr int kKeys = 128;
+constexpr int kRows = 256;  // query positions per long-pair block (a multiple of the list block)
+constexpr int kMetaStages = 4;
+constexpr int kBlockBytes = 128 * 128;  // 128 rows x 128 bytes (64 bf16)
+constexpr int kHalfBytes = 64 * 128;    // 64 rows of such a block
+constexpr int kRegsIo = 64;
+constexpr int kRegsEw = 216;
+constexpr int kRegsNeeded = (128 * kRegsIo + 256 * kRegsEw + kThreads - 1) / kThreads;
+static_assert(kRows % KVPOP_LIST_QBLOCK == 0 && kRows % 128 == 0, "block of rows");
+
+struct BwdParams {
+  CUtensorMap tq, tdo, tk, tv;  // 4-D tiles: q/dO box {64, G, P, 1}; k/v box {64, 1, 128, 1}
+  CUtensorMap tkr, tvr;         // K, V as [b*S*H rows, D] with one-row boxes (gather4)
+  const int32_t* evict_at;
+  const int2* lists;
+  const float* lse2;   // [b, H, Spad, G]
+  const float* delta;  // [b, H, Spad, G]
+  const int2* keys;    // [b, H, nblk, cap]
+  const int32_t* nkeys;  // [b, H, nblk]
+  float* dq;
+  float* dk;
+  float* dv;
+  int* status;
+  int S, Spad, Hq, H, G, gshift, P, nb;
+  int s, w, kk, nL;
+  int nqt, nblk, cap, ctiles;
+  int nitems;
+  float scale, scale_log2;
+};
+
+__device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
+__device__ __forceinline__ float pos_inf() { return __int_as_float(0x7f800000); }
+
+// ---------------------------------------------------------------------------
+// bwd_prep: Delta and LSE (log2 units) per row, in query-tile order
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void bwd_prep(const __nv_bfloat16* __restrict__ O, const __nv_bfloat16* __restrict__ dO,
+                         const float* __restrict__ lse, int b, int S, int Spad, int H, int G,
+                         float* __restrict__ lse2, float* __restrict__ delta) {
+  grid_dep_wait();
+  grid_dep_launch();
+  constexpr int TPR = D / 8;  // threads per row, 8 elements each
+  const int Hq = H * G;
+  const long long n = (long long)b * Spad * Hq * TPR;  // a multiple of 32 (Spad % 128 == 0)
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long r = i / TPR;
+    const int part = (int)(i - r * TPR);
+    const int j = (int)(r % Hq);
+    const long long bq = r / Hq;
+    const int qp = (int)(bq % Spad);
+    const int bi = (int)(bq / Spad);
+    float acc = 0.0f;
+    if (qp < S) {
+      const size_t off = (((size_t)bi * S + qp) * Hq + j) * D + part * 8;
+      const uint4 a = *reinterpret_cast<const uint4*>(O + off);
+      const uint4 c = *reinterpret_cast<const uint4*>(dO + off);
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+      const __nv_bfloat162* c2 = reinterpret_cast<const __nv_bfloat162*>(&c);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float2 fa = __bfloat1622float2(a2[u]), fc = __bfloat1622float2(c2[u]);
+        acc = fmaf(fa.x, fc.x, acc);
+        acc = fmaf(fa.y, fc.y, acc);
+      }
+    }
+#pragma unroll
+    for (int o = TPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (part == 0) {
+      const int h = j / G, g = j - h * G;
+      const size_t o = (((size_t)bi * H + h) * Spad + qp) * G + g;
+      float l2 = pos_inf();  // padded or empty rows: every probability is 0
+      if (qp < S) {
+        const float l = lse[((size_t)bi * Hq + j) * S + qp];
+        if (l != neg_inf()) l2 = l * 1.4426950408889634f;
+      }
+      lse2[o] = l2;
+      delta[o] = acc;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// bwd_keys: the keys holding a long pair with a row of each block
+// ---------------------------------------------------------------------------
+// One CTA of kRows threads per (block, batch x KV head): blockIdx.x = bh * nblk + block.  Order inside a list:
+// sinks, the long-range list at row r0, then the entering keys by position.
+__global__ void __launch_bounds__(kRows) bwd_keys(const int32_t* __restrict__ evict_at, const int2* __restrict__ lists,
+                                                  int S, int s, int w, int kk, int nL, int nblk, int cap,
+                                                  int2* __restrict__ keys, int32_t* __restrict__ nkeys) {
+  grid_dep_wait();
+  grid_dep_launch();
+  __shared__ int warp_tot[kRows / 32];
+  const int blk = (int)(blockIdx.x % (unsigned)nblk), bh = (int)(blockIdx.x / (unsigned)nblk);
+  const int r0 = blk * kRows;
+  const int r1 = min(r0 + kRows, S) - 1;
+  int2* out = keys + ((size_t)bh * nblk + blk) * cap;
+  const int32_t* ev = evict_at + (size_t)bh * S;
+  // sinks t with a row q >= t + w inside the block
+  const int n_sink = max(0, min(s, r1 - w + 1));
+  for (int i = threadIdx.x; i < n_sink; i += blockDim.x) out[i] = make_int2(i, S);
+  // keys retained at row r0 from E(r0): the forward's list (r0 is a list-block start)
+  const int n_list = kk > 0 ? min(kk, max(0, r0 - w - s + 1)) : 0;
+  if (n_list > 0) {
+    const int2* lst = lists + ((size_t)bh * nL + r0 / KVPOP_LIST_QBLOCK) * kk;
+    for (int i = threadIdx.x; i < n_list; i += blockDim.x) out[n_sink + i] = lst[i];
+  }
+  // keys entering E at a row of the block (t + w in (r0, r1]) and retained there
+  const int e0 = max(s, r0 - w + 1), e1 = r1 - w;  // at most kRows - 1 positions
+  const int t = e0 + (int)threadIdx.x;
+  int e = 0;
+  if (t <= e1) e = __ldg(ev + t);
+  const bool enter = t <= e1 && e > t + w;
+  const unsigned bal = __ballot_sync(0xffffffffu, enter);
+  const int lane = threadIdx.x & 31, wp = threadIdx.x >> 5;
+  if (lane == 0) warp_tot[wp] = __popc(bal);
+  __syncthreads();
+  int before = 0, total = 0;
+#pragma unroll
+  for (int u = 0; u < kRows / 32; ++u) {
+    before += u < wp ? warp_tot[u] : 0;
+    total += warp_tot[u];
+  }
+  if (enter) out[n_sink + n_list + before + __popc(bal & ((1u << lane) - 1))] = make_int2(t, e);
+  if (threadIdx.x == 0) nkeys[(size_t)bh * nblk + blk] = n_sink + n_list + total;
+}
+
+// ---------------------------------------------------------------------------
+// bwd_dq: query-major dQ
+// ---------------------------------------------------------------------------
+template <int NS>
+struct DqBars {
+  uint64_t q_full, q_empty;
+  uint64_t k_full[NS], k_empty[NS], v_full[NS], v_empty[NS];
+  uint64_t s_full[2], ds_full[2];
+  uint64_t dp_empty;
+  uint64_t o_full, o_empty;
+  uint64_t meta_full[kMetaStages], meta_empty[kMetaStages];
+  uint64_t drain;
+};
+
+template <int D>
+struct DqLayout {
+  static constexpr int DH = D / 64;
+  static constexpr int NS = D == 128 ? 2 : 4;
+  static constexpr int q_off = 0;
+  static constexpr int do_off = q_off + DH * kBlockBytes;
+  static constexpr int k_off = do_off + DH * kBlockBytes;
+  static constexpr int v_off = k_off + NS * DH * kBlockBytes;
+  static constexpr int meta_off = v_off + NS * DH * kBlockBytes;
+  static constexpr int meta_bytes = kMetaStages * (kKeys + 4) * 8;
+  static constexpr int bar_off = meta_off + meta_bytes;
+  static constexpr int misc_off = bar_off + (int)sizeof(DqBars<NS>);
+  static constexpr int total = misc_off + 64 + 1024;
+};
+
+// One query tile (P positions x G heads) of (batch b, KV head h) and its key
+// plan: [0, s) sinks, the list at row q0l = 64 floor(q0 / 64), then every
+// token in [max(s, q0l - w + 1), q1].
+struct DqItem {
+  int b, h, q0, q1;
+  int NT, NTg;
+  int n_sink, n_sl, sp0;
+  const int2* list;
+};
+
+__device__ __forceinline__ DqItem make_dq_item(const BwdParams& p, int it) {
+  DqItem x;
+  const int nbh = p.H * p.nb;
+  const int rank = it / nbh, rem = it - rank * nbh;
+  x.h = rem % p.H;
+  x.b = rem / p.H;
+  const int qt = p.nqt - 1 - rank;  // latest tiles first: they hold the full budget
+  x.q0 = qt * p.P;
+  x.q1 = min(x.q0 + p.P, p.S) - 1;
+  const int jl = x.q0 / KVPOP_LIST_QBLOCK;
+  const int q0l = jl * KVPOP_LIST_QBLOCK;
+  x.n_sink = min(p.s, x.q1 + 1);
+  const int n_list = p.kk > 0 ? min(p.kk, max(0, q0l - p.w - p.s + 1)) : 0;
+  x.list = p.lists ? p.lists + ((size_t)(x.b * p.H + x.h) * p.nL + jl) * (size_t)p.kk : nullptr;
+  x.n_sl = x.n_sink + n_list;
+  x.sp0 = max(p.s, q0l - p.w + 1);
+  const int n_span = max(0, x.q1 - x.sp0 + 1);
+  x.NTg = (x.n_sl + kKeys - 1) / kKeys;
+  x.NT = x.NTg + (n_span + kKeys - 1) / kKeys;
+  return x;
+}
+
+// Warp roles (384 threads):
+//   warp 0      key metadata of each K/V tile: (position, eviction row) per key
+//               and per 32-key chunk the latest position and earliest
+//               eviction row (rows inside that range skip masking)
+//   warp 1      TMEM allocation and the single-thread tcgen05.mma issuer
+//   warp 2      Q tile of each item and the K tiles (gather4 for sinks and
+//               long-range keys, one TMA box per span tile)
+//   warp 3      dO tile of each item and the V tiles
+//   warps 4-11  elementwise: warpgroup 0 takes keys 0-63 of each tile,
+//               warpgroup 1 keys 64-127, one query row per thread; then the
+//               dQ epilogue (warpgroup 0 the low half of the columns)
+// TMEM columns: S of key tile t at 128 (t & 1) (two buffers), dP at 256, dQ at
+// 384.  Each warpgroup packs its 64 dS values (bf16 pairs) over the first 32
+// of its own 64 S columns, so neither overwrites S the other has not read.
+// MMA order: S_{t+1}, dP_{t+1} (once dP_t has been read), then dQ += dS_t K_t,
+// so the tensor core computes the next tile while the elementwise warps work.
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdParams p) {
+  using L = DqLayout<D>;
+  constexpr int DH = L::DH;
+  constexpr int NS = L::NS;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  DqBars<NS>* bars = reinterpret_cast<DqBars<NS>*>(smem + L::bar_off);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::misc_off);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::misc_off + 4);
+  int2* meta = reinterpret_cast<int2*>(smem + L::meta_off);
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = warp_id(), lane = lane_id();
+  const int S = p.S, G = p.G;
+  const int it0 = blockIdx.x, dit = gridDim.x;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 2);  // Q (warp 2) and dO (warp 3)
+    mbar_init(&bars->q_empty, 1);
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&bars->k_full[i], 1);
+      mbar_init(&bars->k_empty[i], 1);
+      mbar_init(&bars->v_full[i], 1);
+      mbar_init(&bars->v_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->s_full[i], 1);
+      mbar_init(&bars->ds_full[i], 8);
+    }
+    mbar_init(&bars->dp_empty, 8);
+    mbar_init(&bars->o_full, 1);
+    mbar_init(&bars->o_empty, 8);
+    for (int i = 0; i < kMetaStages; ++i) {
+      mbar_init(&bars->meta_full[i], 1);
+      mbar_init(&bars->meta_empty[i], 10);  // 8 elementwise warps + 2 loader warps
+    }
+    mbar_init(&bars->drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  grid_dep_wait();
+  grid_dep_launch();
+
+  auto fail = [&](int site, int detail) {
+    report_error(p.status, KVPOP_ERR_TIMEOUT, site, detail);
+    *abort_flag = 1;
+  };
+  const uint32_t q_addr = sbase + L::q_off;
+  const uint32_t do_addr = sbase + L::do_off;
+  const uint32_t k_addr = sbase + L::k_off;
+  const uint32_t v_addr = sbase + L::v_off;
+
+  if (warp < 4) {
+    setmaxnreg_dec<kRegsIo>();
+    if (warp == 0) {
+      // ---------------------------------------------------------- key metadata
+      bool ok = true;
+      int t = 0;
+      for (int it = it0; ok && it < p.nitems; it += dit) {
+        const DqItem x = make_dq_item(p, it);
+        const int32_t* ev = p.evict_at + (size_t)(x.b * p.H + x.h) * S;
+        auto load_tile = [&](int j, int2 (&e)[4]) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int r = lane + 32 * c;
+            e[c] = make_int2(0x7fffffff, 0);  // padding: never visible
+            if (j < x.NTg) {
+              const int i = j * kKeys + r;
+              if (i < x.n_sink) e[c] = make_int2(i, S);
+              else if (i < x.n_sl) e[c] = __ldg(x.list + (i - x.n_sink));
+            } else {
+              const int pos = x.sp0 + (j - x.NTg) * kKeys + r;
+              if (pos <= x.q1) e[c] = make_int2(pos, __ldg(ev + pos));
+            }
+          }
+        };
+        int2 cur_e[4], nxt_e[4];
+        load_tile(0, cur_e);
+        for (int j = 0; j < x.NT; ++j, ++t) {
+          const int ms = t % kMetaStages;
+          if (j + 1 < x.NT) load_tile(j + 1, nxt_e);
+          if (!warp_wait(&bars->meta_empty[ms], ((t / kMetaStages) & 1) ^ 1, abort_flag)) {
+            if (lane == 0) fail(SITE_ATTN_PRODUCER, 31);
+            ok = false;
+            break;
+          }
+          int2* m = meta + ms * (kKeys + 4);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int r = lane + 32 * c;
+            int2 e = cur_e[c];
+            if (e.x != 0x7fffffff && (e.x < 0 || e.x >= S)) {  // a corrupt list entry: never gathered
+              report_error(p.status, KVPOP_ERR_INTERNAL, SITE_INTERNAL_CHECK, 11);
+              e = make_int2(0x7fffffff, 0);
+            }
+            m[r] = e;
+            int lo = e.x, hi = e.y;  // rows in [lo, hi) see every key of the chunk
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+              lo = max(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+              hi = min(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+            }
+            if (lane == 0) m[kKeys + c] = make_int2(lo, hi);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->meta_full[ms]);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) cur_e[c] = nxt_e[c];
+        }
+      }
+    } else if (warp == 1) {
+      // ---------------------------------------------------------- MMA issuer
+      if (lane == 0 && it0 < p.nitems) {
+        constexpr uint32_t idesc_s = idesc_bf16(128, 128, 0);
+        constexpr uint32_t idesc_dq = idesc_bf16(128, D, 1);
+        auto issue_nt = [&](uint32_t a_base, uint32_t b_base, uint32_t dcol) {  // A B^T over D
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const int dh = ks >> 2;
+            const uint32_t w32 = (uint32_t)(ks & 3) * 32;
+            const uint64_t a = smem_desc_sw128(a_base + dh * kBlockBytes + w32, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(b_base + dh * kBlockBytes + w32, 16, 1024);
+            mma_ss(tbase + dcol, a, bd, idesc_s, ks > 0 ? 1u : 0u);
+          }
+        };
+        auto wait_bar = [&](uint64_t* bar, uint32_t ph, int detail) -> bool {
+          if (!mbar_wait(bar, ph, abort_flag)) {
+            fail(SITE_ATTN_MMA, detail);
+            return false;
+          }
+          tc_fence_after();
+          return true;
+        };
+        // S_t and dP_t of global tile t (ring stage st, phase ph); item counter n
+        auto issue_sdp = [&](int t, int st, uint32_t ph, bool first_of_item, int n) -> bool {
+          if (first_of_item && !wait_bar(&bars->q_full, n & 1, 31)) return false;
+          if (!wait_bar(&bars->k_full[st], ph, 32)) return false;
+          issue_nt(q_addr, k_addr + st * DH * kBlockBytes, 128u * (uint32_t)(t & 1));
+          if (t > 0 && !wait_bar(&bars->dp_empty, (t - 1) & 1, 33)) return false;
+          if (!wait_bar(&bars->v_full[st], ph, 34)) return false;
+          issue_nt(do_addr, v_addr + st * DH * kBlockBytes, 256u);
+          mma_commit(&bars->s_full[t & 1]);
+          mma_commit(&bars->v_empty[st]);
+          return true;
+        };
+        DqItem x = make_dq_item(p, it0);
+        bool ok = issue_sdp(0, 0, 0, true, 0);
+        if (ok && x.NT == 1) mma_commit(&bars->q_empty);
+        int t = 0, n = 0;
+        for (int it = it0; ok;) {
+          for (int j = 0; ok && j < x.NT; ++j, ++t) {
+            const int st = t % NS;
+            const bool last = j + 1 == x.NT;
+            const int it1 = last ? it + dit : it;
+            if (it1 < p.nitems) {
+              const int NT1 = last ? make_dq_item(p, it1).NT : x.NT;
+              const int j1 = last ? 0 : j + 1;
+              if (!(ok = issue_sdp(t + 1, (t + 1) % NS, ((t + 1) / NS) & 1, j1 == 0, last ? n + 1 : n))) break;
+              if (j1 == NT1 - 1) mma_commit(&bars->q_empty);  // every S and dP of that item issued
+            }
+            if (!(ok = wait_bar(&bars->ds_full[t & 1], (t >> 1) & 1, 35))) break;
+            if (j == 0 && !(ok = wait_bar(&bars->o_empty, (n & 1) ^ 1, 36))) break;
+#pragma unroll
+            for (int ks = 0; ks < kKeys / 16; ++ks) {
+              const uint64_t bd = smem_desc_sw128(k_addr + st * DH * kBlockBytes + ks * 2048,
+                                                  DH > 1 ? kBlockBytes : 16, 1024);
+              // dS of keys 16 ks .. 16 ks + 15: warpgroup ks / 4 packed them over its own S columns
+              const uint32_t a_col = 128u * (uint32_t)(t & 1) + 64u * (uint32_t)(ks >> 2) + 8u * (uint32_t)(ks & 3);
+              mma_ts(tbase + 384, tbase + a_col, bd, idesc_dq, (j > 0 || ks > 0) ? 1u : 0u);
+            }
+            mma_commit(&bars->k_empty[st]);
+            if (last) mma_commit(&bars->o_full);
+          }
+          if (!ok) break;
+          it += dit;
+          ++n;
+          if (it >= p.nitems) break;
+          x = make_dq_item(p, it);
+        }
+        mma_commit(&bars->drain);
+        mbar_wait(&bars->drain, 0, nullptr);
+      }
+    } else {
+      // ---------------------------------------------------------- loaders: warp 2 Q and K, warp 3 dO and V
+      const bool is_v = warp == 3;
+      const CUtensorMap* rmap = is_v ? &p.tvr : &p.tkr;
+      const CUtensorMap* tmap = is_v ? &p.tv : &p.tk;
+      const CUtensorMap* qmap = is_v ? &p.tdo : &p.tq;
+      uint64_t* full = is_v ? bars->v_full : bars->k_full;
+      uint64_t* empty = is_v ? bars->v_empty : bars->k_empty;
+      const int off = is_v ? L::v_off : L::k_off;
+      const int qoff = is_v ? L::do_off : L::q_off;
+      if (lane == 0) tma_prefetch_desc(qmap);
+      bool ok = true;
+      int t = 0, n = 0;
+      for (int it = it0; ok && it < p.nitems; it += dit, ++n) {
+        const DqItem x = make_dq_item(p, it);
+        if (lane == 0) {
+          ok = mbar_wait(&bars->q_empty, (n & 1) ^ 1, abort_flag);
+          if (!ok) {
+            fail(SITE_ATTN_PRODUCER, 37);
+          } else {
+            mbar_arrive_expect_tx(&bars->q_full, DH * kBlockBytes);
+            for (int dh = 0; dh < DH; ++dh)
+              tma_load_4d(smem + qoff + dh * kBlockBytes, qmap, &bars->q_full, dh * 64, x.h * G, x.q0, x.b);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        const int row_base = x.b * S * p.H + x.h;  // row of position t is row_base + t * H
+        for (int j = 0; j < x.NT; ++j, ++t) {
+          const int st = t % NS;
+          const uint32_t ph = (t / NS) & 1;
+          const int ms = t % kMetaStages;
+          if (!warp_wait(&bars->meta_full[ms], (t / kMetaStages) & 1, abort_flag)) {
+            if (lane == 0) fail(SITE_ATTN_PRODUCER, 38);
+            ok = false;
+            break;
+          }
+          if (!warp_wait(&empty[st], ph ^ 1, abort_flag)) {
+            if (lane == 0) fail(SITE_ATTN_PRODUCER, 39);
+            ok = false;
+            break;
+          }
+          if (lane == 0) mbar_arrive_expect_tx(&full[st], DH * kBlockBytes);
+          __syncwarp();
+          if (j < x.NTg) {
+            const int2* km = meta + ms * (kKeys + 4);
+            int rows[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int pos = km[4 * lane + u].x;
+              rows[u] = pos != 0x7fffffff ? row_base + pos * p.H : row_base;  // padding: any row, masked
+            }
+#pragma unroll
+            for (int d2 = 0; d2 < DH; ++d2)
+              tma_gather4(smem + off + (st * DH + d2) * kBlockBytes + lane * 512, rmap, &full[st], d2 * 64,
+                          rows[0], rows[1], rows[2], rows[3]);
+          } else if (lane == 0) {
+            const int span_row = x.sp0 + (j - x.NTg) * kKeys;
+            for (int d2 = 0; d2 < DH; ++d2)
+              tma_load_4d(smem + off + (st * DH + d2) * kBlockBytes, tmap, &full[st], d2 * 64, x.h, span_row, x.b);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->meta_empty[ms]);
+        }
+      }
+    }
+  } else {
+    setmaxnreg_inc<kRegsEw>();
+    // ------------------------------------------------------------ elementwise
+    const int wg = (warp - 4) >> 2;  // key half of each tile
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const int p_row = row >> p.gshift, g = row - (p_row << p.gshift);
+    const uint32_t tl = tbase + ((uint32_t)(quarter * 32) << 16);
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    int t = 0, n = 0;
+    for (int it = it0; ok && it < p.nitems; it += dit, ++n) {
+      const DqItem x = make_dq_item(p, it);
+      const int q = x.q0 + p_row;
+      const size_t ro = ((size_t)(x.b * p.H + x.h) * p.Spad + x.q0) * G + row;
+      const float l2 = __ldg(p.lse2 + ro);
+      const float dl = __ldg(p.delta + ro);
+      for (int j = 0; j < x.NT; ++j, ++t) {
+        const int sb = t & 1;
+        if (!warp_wait(&bars->s_full[sb], (t >> 1) & 1, abort_flag)) {
+          if (lane == 0) fail(SITE_ATTN_SOFTMAX, 31);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int ms = t % kMetaStages;
+        if (!warp_wait(&bars->meta_full[ms], (t / kMetaStages) & 1, abort_flag)) {
+          if (lane == 0) fail(SITE_ATTN_SOFTMAX, 32);
+          ok = false;
+          break;
+        }
+        const int2* km = meta + ms * (kKeys + 4);
+        uint32_t sr[2][32], dr[2][32];
+        tmem_ld32(tl + 128 * sb + 64 * wg, sr[0]);
+        tmem_ld32(tl + 128 * sb + 64 * wg + 32, sr[1]);
+        tmem_ld32(tl + 256 + 64 * wg, dr[0]);
+        tmem_ld32(tl + 256 + 64 * wg + 32, dr[1]);
+        tmem_wait_ld_dep(sr[0]);
+        tmem_wait_ld_dep(sr[1]);
+        tmem_wait_ld_dep(dr[0]);
+        tmem_wait_ld_dep(dr[1]);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->dp_empty);  // the next dP may overwrite its columns
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {
+          const int c32 = 2 * wg + ch;
+          const int2 sum = km[kKeys + c32];
+          const bool fast = q >= sum.x && q < sum.y;
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            float ds[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int2 e = km[c32 * 32 + c + u];
+              const bool vis = fast || (e.x <= q && q < e.y);
+              const float pr = vis ? ex2_approx(fmaf(__uint_as_float(sr[ch][c + u]), sl2, -l2)) : 0.0f;
+              ds[u] = pr * (__uint_as_float(dr[ch][c + u]) - dl);
+            }
+            pk[c >> 1] = pack_bf16x2(ds[0], ds[1]);
+          }
+          tmem_st16(tl + 128 * sb + 64 * wg + 16 * ch, pk);  // over this warpgroup's own S columns
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&bars->ds_full[sb]);
+          mbar_arrive(&bars->meta_empty[ms]);
+        }
+      }
+      if (!ok) break;
+      // epilogue: this warpgroup's half of the dQ columns, scaled
+      if (!warp_wait(&bars->o_full, n & 1, abort_flag)) {
+        if (lane == 0) fail(SITE_ATTN_EPILOGUE, 31);
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      constexpr int HC = D / 2;  // columns per warpgroup
+      uint32_t acc[HC];
+#pragma unroll
+      for (int cc = 0; cc < HC / 32; ++cc) {
+        uint32_t r[32];
+        tmem_ld32(tl + 384 + HC * wg + 32 * cc, r);
+        tmem_wait_ld_dep(r);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) acc[32 * cc + c] = r[c];
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->o_empty);
+      if (q <= x.q1) {
+        float4* dst = reinterpret_cast<float4*>(p.dq + (((size_t)x.b * S + q) * p.Hq + x.h * G + g) * D + HC * wg);
+#pragma unroll
+        for (int u = 0; u < HC / 4; ++u)
+          dst[u] = make_float4(__uint_as_float(acc[4 * u]) * p.scale, __uint_as_float(acc[4 * u + 1]) * p.scale,
+                               __uint_as_float(acc[4 * u + 2]) * p.scale, __uint_as_float(acc[4 * u + 3]) * p.scale);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// bwd_dkdv: key-major dK, dV
+// ---------------------------------------------------------------------------
+template <int NQS>
+struct KvBars {
+  uint64_t kv_full, kv_empty;
+  uint64_t q_full[NQS], q_empty[NQS];
+  uint64_t s_full[2], p_full[2];
+  uint64_t acc_full, acc_empty;
+  uint64_t drain;
+};
+
+template <int D>
+struct KvLayout {
+  static constexpr int DH = D / 64;
+  static constexpr int NQS = D == 128 ? 2 : 4;  // Q/dO stages
+  static constexpr int k_off = 0;
+  static constexpr int v_off = k_off + DH * kBlockBytes;
+  static constexpr int q_off = v_off + DH * kBlockBytes;           // stage i: Q at q_off + 2 i DH blocks
+  static constexpr int stage_bytes = 2 * DH * kBlockBytes;         // Q then dO
+  static constexpr int row_off = q_off + NQS * stage_bytes;        // stage i: 128 LSE2 then 128 Delta floats
+  static constexpr int kmeta_off = row_off + NQS * 1024;
+  static constexpr int bar_off = kmeta_off + kKeys * 8;
+  static constexpr int misc_off = bar_off + (int)sizeof(KvBars<NQS>);
+  static constexpr int total = misc_off + 64 + 1024;
+};
+
+// Band item: keys [t0, t0 + 128) against rows t0 .. t0 + 126 + w.
+// Long item: keys [128 c, 128 c + 128) of block blk's list against the rows of the block.
+struct KvItem {
+  int b, h, n;    // n: keys in the item (0: nothing to do)
+  int t0;         // band: first key position
+  const int2* keys;  // long: the item's list entries
+  int qt0, NQ;    // first query tile and number of query tiles
+};
+
+template <bool LONG>
+__device__ __forceinline__ KvItem make_kv_item(const BwdParams& p, int it) {
+  KvItem x;
+  const int nbh = p.H * p.nb;
+  const int rank = it / nbh, rem = it - rank * nbh;
+  x.h = rem % p.H;
+  x.b = rem / p.H;
+  x.keys = nullptr;
+  x.t0 = 0;
+  if (!LONG) {
+    x.t0 = rank * kKeys;
+    x.n = min(kKeys, p.S - x.t0);
+    const int q_hi = min(p.S - 1, x.t0 + kKeys - 2 + p.w);
+    x.qt0 = x.t0 / p.P;
+    x.NQ = q_hi / p.P - x.qt0 + 1;
+  } else {
+    const int blk = p.nblk - 1 - rank / p.ctiles, c = rank % p.ctiles;
+    const size_t bb = (size_t)(x.b * p.H + x.h) * p.nblk + blk;
+    const int cnt = __ldg(p.nkeys + bb);
+    x.n = min(kKeys, cnt - c * kKeys);
+    x.keys = p.keys + bb * p.cap + c * kKeys;
+    const int r0 = blk * kRows, r1 = min(r0 + kRows, p.S) - 1;
+    x.qt0 = r0 / p.P;
+    x.NQ = r1 / p.P - x.qt0 + 1;
+  }
+  if (x.n <= 0) x.n = 0;
+  return x;
+}
+
+// Warp roles (384 threads):
+//   warp 0      per query tile: Q and dO (TMA boxes) with the tile's LSE2 and
+//               Delta rows (bulk copies) into a ring of NQS stages
+//   warp 1      TMEM allocation and the single-thread tcgen05.mma issuer
+//   warp 2      the item's K tile (one TMA box, or gather4 from its list) and
+//               the keys' (position, eviction row)
+//   warp 3      the item's V tile
+//   warps 4-11  elementwise: warpgroup h takes rows 64h .. 64h + 63 of each
+//               query tile, one key per thread (TMEM lane); then the epilogue:
+//               warpgroup 0 writes dv, warpgroup 1 dk
+// TMEM columns: dV at 0, dK at D; half h of a query tile: S^T at 256 + 128 h,
+// dP^T at 256 + 128 h + 64 (P^T and dS^T in bf16 over them).
+// MMA order per query tile u: dV, dK of half 0; S^T, dP^T of half 0 of tile
+// u + 1; dV, dK of half 1; S^T, dP^T of half 1 of tile u + 1.
+template <int D, bool LONG>
+__global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
+  using L = KvLayout<D>;
+  constexpr int DH = L::DH;
+  constexpr int NQS = L::NQS;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  KvBars<NQS>* bars = reinterpret_cast<KvBars<NQS>*>(smem + L::bar_off);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::misc_off);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::misc_off + 4);
+  int2* kmeta = reinterpret_cast<int2*>(smem + L::kmeta_off);
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = warp_id(), lane = lane_id();
+  const int S = p.S, G = p.G, P = p.P;
+  const int it0 = blockIdx.x, dit = gridDim.x;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->kv_full, 2);  // K (warp 2) and V (warp 3)
+    mbar_init(&bars->kv_empty, 1);
+    for (int i = 0; i < NQS; ++i) {
+      mbar_init(&bars->q_full[i], 1);
+      mbar_init(&bars->q_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->s_full[i], 1);
+      mbar_init(&bars->p_full[i], 4);
+    }
+    mbar_init(&bars->acc_full, 1);
+    mbar_init(&bars->acc_empty, 8);
+    mbar_init(&bars->drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  grid_dep_wait();
+  grid_dep_launch();
+
+  auto fail = [&](int site, int detail) {
+    report_error(p.status, KVPOP_ERR_TIMEOUT, site, detail);
+    *abort_flag = 1;
+  };
+  const uint32_t k_addr = sbase + L::k_off;
+  const uint32_t v_addr = sbase + L::v_off;
+  auto q_stage = [&](int stg) { return sbase + L::q_off + stg * L::stage_bytes; };
+  auto do_stage = [&](int stg) { return sbase + L::q_off + stg * L::stage_bytes + DH * kBlockBytes; };
+
+  if (warp < 4) {
+    setmaxnreg_dec<kRegsIo>();
+    if (warp == 0) {
+      // ---------------------------------------------------------- Q / dO / row constants
+      if (lane == 0) {
+        tma_prefetch_desc(&p.tq);
+        tma_prefetch_desc(&p.tdo);
+        bool ok = true;
+        int u = 0;
+        for (int it = it0; ok && it < p.nitems; it += dit) {
+          const KvItem x = make_kv_item<LONG>(p, it);
+          if (x.n == 0) continue;
+          const size_t rbase = (size_t)(x.b * p.H + x.h) * p.Spad * G;
+          for (int i = 0; i < x.NQ; ++i, ++u) {
+            const int stg = u % NQS;
+            if (!mbar_wait(&bars->q_empty[stg], ((u / NQS) & 1) ^ 1, abort_flag)) {
+              fail(SITE_ATTN_PRODUCER, 41);
+              ok = false;
+              break;
+            }
+            const int qt = x.qt0 + i;
+            uint64_t* bar = &bars->q_full[stg];
+            mbar_arrive_expect_tx(bar, 2 * DH * kBlockBytes + 1024);
+            uint8_t* qs = smem + L::q_off + stg * L::stage_bytes;
+            for (int dh = 0; dh < DH; ++dh) {
+              tma_load_4d(qs + dh * kBlockBytes, &p.tq, bar, dh * 64, x.h * G, qt * P, x.b);
+              tma_load_4d(qs + (DH + dh) * kBlockBytes, &p.tdo, bar, dh * 64, x.h * G, qt * P, x.b);
+            }
+            uint8_t* rs = smem + L::row_off + stg * 1024;
+            bulk_load(rs, p.lse2 + rbase + (size_t)qt * 128, 512, bar);
+            bulk_load(rs + 512, p.delta + rbase + (size_t)qt * 128, 512, bar);
+          }
+        }
+      }
+    } else if (warp == 1) {
+      // ---------------------------------------------------------- MMA issuer
+      if (lane == 0) {
+        constexpr uint32_t idesc_s = idesc_bf16(128, 64, 0);
+        constexpr uint32_t idesc_acc = idesc_bf16(128, D, 1);
+        auto wait_bar = [&](uint64_t* bar, uint32_t ph, int detail) -> bool {
+          if (!mbar_wait(bar, ph, abort_flag)) {
+            fail(SITE_ATTN_MMA, detail);
+            return false;
+          }
+          tc_fence_after();
+          return true;
+        };
+        // S^T_h = K Q_h^T and dP^T_h = V dO_h^T for half h of the tile in stage stg
+        auto issue_sdp = [&](int stg, int h) {
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const int dh = ks >> 2;
+            const uint32_t w32 = (uint32_t)(ks & 3) * 32;
+            const uint64_t a = smem_desc_sw128(k_addr + dh * kBlockBytes + w32, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(q_stage(stg) + dh * kBlockBytes + h * kHalfBytes + w32, 16, 1024);
+            mma_ss(tbase + 256 + 128 * h, a, bd, idesc_s, ks > 0 ? 1u : 0u);
+          }
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const int dh = ks >> 2;
+            const uint32_t w32 = (uint32_t)(ks & 3) * 32;
+            const uint64_t a = smem_desc_sw128(v_addr + dh * kBlockBytes + w32, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(do_stage(stg) + dh * kBlockBytes + h * kHalfBytes + w32, 16, 1024);
+            mma_ss(tbase + 256 + 128 * h + 64, a, bd, idesc_s, ks > 0 ? 1u : 0u);
+          }
+          mma_commit(&bars->s_full[h]);
+        };
+        // dV += P^T_h dO_h and dK += dS^T_h Q_h
+        auto issue_acc = [&](int stg, int h, bool first) {
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint64_t bd = smem_desc_sw128(do_stage(stg) + h * kHalfBytes + ks * 2048, DH > 1 ? kBlockBytes : 16, 1024);
+            mma_ts(tbase, tbase + 256 + 128 * h + ks * 8, bd, idesc_acc, (first && ks == 0) ? 0u : 1u);
+          }
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint64_t bd = smem_desc_sw128(q_stage(stg) + h * kHalfBytes + ks * 2048, DH > 1 ? kBlockBytes : 16, 1024);
+            mma_ts(tbase + D, tbase + 256 + 128 * h + 64 + ks * 8, bd, idesc_acc, (first && ks == 0) ? 0u : 1u);
+          }
+        };
+        bool ok = true;
+        int u = 0, n = 0;
+        for (int it = it0; ok && it < p.nitems; it += dit) {
+          const KvItem x = make_kv_item<LONG>(p, it);
+          if (x.n == 0) continue;
+          if (!(ok = wait_bar(&bars->kv_full, n & 1, 41))) break;
+          if (!(ok = wait_bar(&bars->q_full[u % NQS], (u / NQS) & 1, 42))) break;
+          issue_sdp(u % NQS, 0);
+          issue_sdp(u % NQS, 1);
+          for (int i = 0; ok && i < x.NQ; ++i, ++u) {
+            const int stg = u % NQS;
+            const bool more = i + 1 < x.NQ;
+            const int stg1 = (u + 1) % NQS;
+            if (!(ok = wait_bar(&bars->p_full[0], u & 1, 43))) break;
+            if (i == 0 && !(ok = wait_bar(&bars->acc_empty, (n & 1) ^ 1, 44))) break;
+            issue_acc(stg, 0, i == 0);
+            if (more) {
+              if (!(ok = wait_bar(&bars->q_full[stg1], ((u + 1) / NQS) & 1, 45))) break;
+              issue_sdp(stg1, 0);
+            }
+            if (!(ok = wait_bar(&bars->p_full[1], u & 1, 46))) break;
+            issue_acc(stg, 1, false);
+            mma_commit(&bars->q_empty[stg]);
+            if (more) issue_sdp(stg1, 1);
+          }
+          if (!ok) break;
+          mma_commit(&bars->acc_full);
+          mma_commit(&bars->kv_empty);
+          ++n;
+        }
+        mma_commit(&bars->drain);
+        mbar_wait(&bars->drain, 0, nullptr);
+      }
+    } else {
+      // ---------------------------------------------------------- K (warp 2) and V (warp 3) of each item
+      const bool is_v = warp == 3;
+      const CUtensorMap* rmap = is_v ? &p.tvr : &p.tkr;
+      const CUtensorMap* tmap = is_v ? &p.tv : &p.tk;
+      const int off = is_v ? L::v_off : L::k_off;
+      bool ok = true;
+      int n = 0;
+      for (int it = it0; ok && it < p.nitems; it += dit) {
+        const KvItem x = make_kv_item<LONG>(p, it);
+        if (x.n == 0) continue;
+        if (!warp_wait(&bars->kv_empty, (n & 1) ^ 1, abort_flag)) {
+          if (lane == 0) fail(SITE_ATTN_PRODUCER, 42);
+          ok = false;
+          break;
+        }
+        if (!LONG) {
+          if (!is_v) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) kmeta[lane + 32 * c] = make_int2(x.t0 + lane + 32 * c, S);
+          }
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&bars->kv_full, DH * kBlockBytes);
+            for (int dh = 0; dh < DH; ++dh)
+              tma_load_4d(smem + off + dh * kBlockBytes, tmap, &bars->kv_full, dh * 64, x.h, x.t0, x.b);
+          }
+        } else {
+          const int row_base = x.b * S * p.H + x.h;
+          int rows[4];
+#pragma unroll
+          for (int u2 = 0; u2 < 4; ++u2) {
+            const int r = 4 * lane + u2;
+            int2 e = r < x.n ? __ldg(x.keys + r) : make_int2(0x7fffffff, 0);
+            if (e.x != 0x7fffffff && (e.x < 0 || e.x >= S)) {  // a corrupt entry: never gathered
+              report_error(p.status, KVPOP_ERR_INTERNAL, SITE_INTERNAL_CHECK, 12);
+              e = make_int2(0x7fffffff, 0);
+            }
+            rows[u2] = e.x != 0x7fffffff ? row_base + e.x * p.H : row_base;  // padding: any row, masked
+            if (!is_v) kmeta[r] = e;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive_expect_tx(&bars->kv_full, DH * kBlockBytes);
+          __syncwarp();
+#pragma unroll
+          for (int dh = 0; dh < DH; ++dh)
+            tma_gather4(smem + off + dh * kBlockBytes + lane * 512, rmap, &bars->kv_full, dh * 64, rows[0], rows[1],
+                        rows[2], rows[3]);
+        }
+        ++n;
+      }
+    }
+  } else {
+    setmaxnreg_inc<kRegsEw>();
+    // ------------------------------------------------------------ elementwise
+    const int hh = (warp - 4) >> 2;  // row half of each query tile
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;  // this thread's key (TMEM lane)
+    const uint32_t tl = tbase + ((uint32_t)(quarter * 32) << 16);
+    const float sl2 = p.scale_log2;
+    const int w = p.w;
+    bool ok = true;
+    int u = 0, n = 0;
+    for (int it = it0; ok && it < p.nitems; it += dit) {
+      const KvItem x = make_kv_item<LONG>(p, it);
+      if (x.n == 0) continue;
+      if (!warp_wait(&bars->kv_full, n & 1, abort_flag)) {
+        if (lane == 0) fail(SITE_ATTN_SOFTMAX, 41);
+        ok = false;
+        break;
+      }
+      const int2 me = kmeta[r];
+      // band: rows [t, t + w) (and < S); long: rows [t + w, evict_at[t])
+      const int lo = LONG ? (me.x == 0x7fffffff ? 0x7fffffff : me.x + w) : me.x;
+      const int hi = LONG ? me.y : min(me.x + w, S);
+      for (int i = 0; i < x.NQ; ++i, ++u) {
+        const int stg = u % NQS;
+        if (!warp_wait(&bars->s_full[hh], u & 1, abort_flag)) {
+          if (lane == 0) fail(SITE_ATTN_SOFTMAX, 42);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t sr[2][32], dr[2][32];
+        const uint32_t col = 256 + 128 * hh;
+        tmem_ld32(tl + col, sr[0]);
+        tmem_ld32(tl + col + 32, sr[1]);
+        tmem_ld32(tl + col + 64, dr[0]);
+        tmem_ld32(tl + col + 96, dr[1]);
+        tmem_wait_ld_dep(sr[0]);
+        tmem_wait_ld_dep(sr[1]);
+        tmem_wait_ld_dep(dr[0]);
+        tmem_wait_ld_dep(dr[1]);
+        const float* rl2 = reinterpret_cast<const float*>(smem + L::row_off + stg * 1024) + 64 * hh;
+        const float* rdl = rl2 + 128;
+        const int pos0 = (x.qt0 + i) * P;  // position of row 0 of the tile
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {
+          uint32_t pk[16], dk[16];
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            float pr[2], ds[2];
+#pragma unroll
+            for (int v2 = 0; v2 < 2; ++v2) {
+              const int cr = 64 * hh + 32 * ch + c + v2;  // row of the tile
+              const int qp = pos0 + (cr >> p.gshift);
+              const bool vis = qp >= lo && qp < hi;
+              const float e = vis ? ex2_approx(fmaf(__uint_as_float(sr[ch][c + v2]), sl2, -rl2[32 * ch + c + v2])) : 0.0f;
+              pr[v2] = e;
+              ds[v2] = e * (__uint_as_float(dr[ch][c + v2]) - rdl[32 * ch + c + v2]);
+            }
+            pk[c >> 1] = pack_bf16x2(pr[0], pr[1]);
+            dk[c >> 1] = pack_bf16x2(ds[0], ds[1]);
+          }
+          tmem_st16(tl + col + 16 * ch, pk);
+          tmem_st16(tl + col + 64 + 16 * ch, dk);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->p_full[hh]);
+      }
+      if (!ok) break;
+      // epilogue: warpgroup 0 dV, warpgroup 1 dK (scaled)
+      if (!warp_wait(&bars->acc_full, n & 1, abort_flag)) {
+        if (lane == 0) fail(SITE_ATTN_EPILOGUE, 41);
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t acc[D];
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t rr[32];
+        tmem_ld32(tl + D * hh + 32 * cc, rr);
+        tmem_wait_ld_dep(rr);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) acc[32 * cc + c] = rr[c];
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->acc_empty);
+      const bool valid = me.x >= 0 && me.x < S;  // padding and rejected entries hold 0x7fffffff
+      if (valid) {
+        const float sc = hh == 1 ? p.scale : 1.0f;
+        float* base = hh == 1 ? p.dk : p.dv;
+        float4* dst = reinterpret_cast<float4*>(base + (((size_t)x.b * S + me.x) * p.H + x.h) * D);
+#pragma unroll
+        for (int c4 = 0; c4 < D / 4; ++c4) {
+          const float4 val = make_float4(__uint_as_float(acc[4 * c4]) * sc, __uint_as_float(acc[4 * c4 + 1]) * sc,
+                                         __uint_as_float(acc[4 * c4 + 2]) * sc, __uint_as_float(acc[4 * c4 + 3]) * sc);
+          if (LONG) atomicAdd(dst + c4, val);
+          else dst[c4] = val;
+        }
+      }
+      ++n;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+template <typename K>
+kvpop_status prepare(K kern, int smem_bytes, const char* what) {
+  kvpop_status st = cuda_check(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes), what);
+  if (st != KVPOP_OK) return st;
+  cudaFuncAttributes fa;
+  st = cuda_check(cudaFuncGetAttributes(&fa, kern), what);
+  if (st != KVPOP_OK) return st;
+  if (((fa.numRegs + 7) / 8) * 8 < kRegsNeeded) {
+    set_last_error("%s: kernel built with %d registers per thread, %d needed", what, fa.numRegs, kRegsNeeded);
+    return KVPOP_ERR_INTERNAL;
+  }
+  return KVPOP_OK;
+}
+
+template <int D>
+kvpop_status launch_bwd(BwdParams prm, const void* O, const void* dO, const float* lse, float* lse2, float* delta,
+                        int2* keys, int32_t* nkeys, cudaStream_t cs) {
+  const int b = prm.nb, S = prm.S, H = prm.H, G = prm.G;
+  const int nbh = b * H;
+  kvpop_status st;
+  {
+    const long long n = (long long)b * prm.Spad * prm.Hq * (D / 8);
+    const int blocks = (int)std::min<long long>((n + 255) / 256, 8LL * num_sms());
+    st = cuda_check(launch_pdl(bwd_prep<D>, dim3(blocks), dim3(256), 0, cs,
+                               static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), lse, b,
+                               S, prm.Spad, H, G, lse2, delta),
+                    "kvpop_attn_bwd: prep");
+    if (st != KVPOP_OK) return st;
+  }
+  st = cuda_check(launch_pdl(bwd_keys, dim3(prm.nblk * nbh), dim3(kRows), 0, cs, prm.evict_at, prm.lists, S, prm.s,
+                             prm.w, prm.kk, prm.nL, prm.nblk, prm.cap, keys, nkeys),
+                  "kvpop_attn_bwd: key lists");
+  if (st != KVPOP_OK) return st;
+  // dQ
+  {
+    using L = DqLayout<D>;
+    auto kern = bwd_dq_kernel<D>;
+    if ((st = prepare(kern, L::total, "kvpop_attn_bwd: dq")) != KVPOP_OK) return st;
+    BwdParams pq = prm;
+    pq.nitems = prm.nqt * nbh;
+    st = cuda_check(launch_pdl(kern, dim3(std::min(pq.nitems, num_sms())), dim3(kThreads), L::total, cs, pq),
+                    "kvpop_attn_bwd: dq launch");
+    if (st != KVPOP_OK) return st;
+  }
+  // dK, dV: band items store, long items add
+  using KL = KvLayout<D>;
+  if (prm.w > 0) {
+    auto kern = bwd_dkdv_kernel<D, false>;
+    if ((st = prepare(kern, KL::total, "kvpop_attn_bwd: dkdv")) != KVPOP_OK) return st;
+    BwdParams pb = prm;
+    pb.nitems = ((S + kKeys - 1) / kKeys) * nbh;
+    st = cuda_check(launch_pdl(kern, dim3(std::min(pb.nitems, num_sms())), dim3(kThreads), KL::total, cs, pb),
+                    "kvpop_attn_bwd: band launch");
+    if (st != KVPOP_OK) return st;
+  } else {
+    const size_t bytes = (size_t)b * S * H * D * sizeof(float);
+    if ((st = cuda_check(cudaMemsetAsync(prm.dk, 0, bytes, cs), "kvpop_attn_bwd: zero dk")) != KVPOP_OK) return st;
+    if ((st = cuda_check(cudaMemsetAsync(prm.dv, 0, bytes, cs), "kvpop_attn_bwd: zero dv")) != KVPOP_OK) return st;
+  }
+  {
+    auto kern = bwd_dkdv_kernel<D, true>;
+    if ((st = prepare(kern, KL::total, "kvpop_attn_bwd: dkdv")) != KVPOP_OK) return st;
+    BwdParams pl = prm;
+    pl.nitems = prm.nblk * prm.ctiles * nbh;
+    st = cuda_check(launch_pdl(kern, dim3(std::min(pl.nitems, num_sms())), dim3(kThreads), KL::total, cs, pl),
+                    "kvpop_attn_bwd: long launch");
+  }
+  return st;
+}
+
+struct BwdSizes {
+  int G, P, Spad, nblk, cap, ctiles;
+  size_t rows_bytes, keys_bytes, counts_bytes, total;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+kvpop_status bwd_sizes(int b, int S, int Hq, int H, kvpop_budget bud, BwdSizes* z, const char* who) {
+  if (b <= 0 || S <= 0 || H <= 0 || Hq <= 0 || Hq % H != 0) {
+    set_last_error("%s: bad shape b=%d S=%d Hq=%d H=%d", who, b, S, Hq, H);
+    return KVPOP_ERR_INVALID_ARG;
+  }
+  if (bud.s < 0 || bud.w < 0 || bud.k < 0 || (long long)bud.s + bud.w + bud.k < 1) {
+    set_last_error("%s: invalid budget", who);
+    return KVPOP_ERR_INVALID_ARG;
+  }
+  z->G = Hq / H;
+  if (128 % z->G != 0) {
+    set_last_error("%s: G=%d must divide 128", who, z->G);
+    return KVPOP_ERR_UNSUPPORTED;
+  }
+  if (b > 65535 || H > 65535 || S > (1 << 24)) {
+    set_last_error("%s: b and H must be <= 65535, S <= 2^24", who);
+    return KVPOP_ERR_UNSUPPORTED;
+  }
+  z->P = 128 / z->G;
+  z->Spad = (S + 127) / 128 * 128;
+  z->nblk = (S + kRows - 1) / kRows;
+  z->cap = bud.s + bud.k + kRows;
+  z->ctiles = (z->cap + kKeys - 1) / kKeys;
+  const long long items = (long long)z->nblk * z->ctiles * b * H;
+  const long long qitems = (long long)(S + z->P - 1) / z->P * b * H;
+  if (items > (1LL << 30) || qitems > (1LL << 30) || (long long)bud.s + bud.k > (1LL << 28)) {
+    set_last_error("%s: problem too large for the work-item indexing", who);
+    return KVPOP_ERR_UNSUPPORTED;
+  }
+  z->rows_bytes = align256((size_t)b * H * z->Spad * z->G * sizeof(float));
+  z->keys_bytes = align256((size_t)b * H * z->nblk * z->cap * sizeof(int2));
+  z->counts_bytes = align256((size_t)b * H * z->nblk * sizeof(int32_t));
+  z->total = 2 * z->rows_bytes + z->keys_bytes + z->counts_bytes;
+  return KVPOP_OK;
+}
+
+}  // namespace
+}  // namespace kvpop
+
+using namespace kvpop;
+
+extern "C" kvpop_status kvpop_attn_bwd_workspace_size(int b, int S, int Hq, int H, kvpop_budget bud,
+                                                      size_t* bytes) {
+  if (!bytes) {
+    set_last_error("kvpop_attn_bwd_workspace_size: bytes is NULL");
+    return KVPOP_ERR_INVALID_ARG;
+  }
+  BwdSizes z;
+  kvpop_status st = bwd_sizes(b, S, Hq, H, bud, &z, "kvpop_attn_bwd_workspace_size");
+  if (st != KVPOP_OK) return st;
+  *bytes = z.total;
+  return KVPOP_OK;
+}
+
+extern "C" kvpop_status kvpop_attn_bwd(const void* q, const void* k, const void* v, const void* O, const void* dO,
+                                       const float* lse, int b, int S, int Hq, int H, int D, float scale,
+                                       const int32_t* evict_at, const int32_t* lists, kvpop_budget bud, float* dq,
+                                       float* dk, float* dv, void* workspace, size_t workspace_bytes,
+                                       kvpop_stream stream) {
+  if (!q || !k || !v || !O || !dO || !lse || !evict_at || (!lists && bud.k > 0) || !dq || !dk || !dv) {
+    set_last_error("kvpop_attn_bwd: q, k, v, O, dO, lse, evict_at, lists (k > 0), dq, dk, dv must be non-NULL");
+    return KVPOP_ERR_INVALID_ARG;
+  }
+  BwdSizes z;
+  kvpop_status st = bwd_sizes(b, S, Hq, H, bud, &z, "kvpop_attn_bwd");
+  if (st != KVPOP_OK) return st;
+  if (D != 64 && D != 128) {
+    set_last_error("kvpop_attn_bwd: D=%d unsupported (64 or 128)", D);
+    return KVPOP_ERR_UNSUPPORTED;
+  }
+  if (!workspace || workspace_bytes < z.total) {
+    set_last_error("kvpop_attn_bwd: workspace of %zu bytes needed", z.total);
+    return KVPOP_ERR_INVALID_ARG;
+  }
+  const uintptr_t am = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                       reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(O) |
+                       reinterpret_cast<uintptr_t>(dO) | reinterpret_cast<uintptr_t>(dq) |
+                       reinterpret_cast<uintptr_t>(dk) | reinterpret_cast<uintptr_t>(dv);
+  if ((am & 15) || (reinterpret_cast<uintptr_t>(workspace) & 255)) {
+    set_last_error("kvpop_attn_bwd: tensors must be 16-byte aligned, the workspace 256-byte aligned");
+    return KVPOP_ERR_UNSUPPORTED;
+  }
+  const int G = z.G, P = z.P;
+  BwdParams prm;
+  memset(&prm, 0, sizeof(prm));
+  {
+    uint64_t dq4[4] = {(uint64_t)D, (uint64_t)Hq, (uint64_t)S, (uint64_t)b};
+    uint64_t sq[3] = {(uint64_t)D * 2, (uint64_t)Hq * D * 2, (uint64_t)S * Hq * D * 2};
+    uint32_t bq[4] = {64, (uint32_t)G, (uint32_t)P, 1};
+    uint64_t dk4[4] = {(uint64_t)D, (uint64_t)H, (uint64_t)S, (uint64_t)b};
+    uint64_t sk[3] = {(uint64_t)D * 2, (uint64_t)H * D * 2, (uint64_t)S * H * D * 2};
+    uint32_t bk[4] = {64, 1, 128, 1};
+    if (!make_tmap_4d(&prm.tq, q, dq4, sq, bq) || !make_tmap_4d(&prm.tdo, dO, dq4, sq, bq) ||
+        !make_tmap_4d(&prm.tk, k, dk4, sk, bk) || !make_tmap_4d(&prm.tv, v, dk4, sk, bk) ||
+        !make_tmap_rows(&prm.tkr, k, (uint64_t)D, (uint64_t)b * S * H, 64) ||
+        !make_tmap_rows(&prm.tvr, v, (uint64_t)D, (uint64_t)b * S * H, 64))
+      return KVPOP_ERR_CUDA;
+  }
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* lse2 = reinterpret_cast<float*>(ws);
+  float* delta = reinterpret_cast<float*>(ws + z.rows_bytes);
+  int2* keys = reinterpret_cast<int2*>(ws + 2 * z.rows_bytes);
+  int32_t* nkeys = reinterpret_cast<int32_t*>(ws + 2 * z.rows_bytes + z.keys_bytes);
+  prm.evict_at = evict_at;
+  prm.lists = reinterpret_cast<const int2*>(lists);
+  prm.lse2 = lse2;
+  prm.delta = delta;
+  prm.keys = keys;
+  prm.nkeys = nkeys;
+  prm.dq = dq;
+  prm.dk = dk;
+  prm.dv = dv;
+  prm.status = device_status_ptr();
+  prm.S = S;
+  prm.Spad = z.Spad;
+  prm.Hq = Hq;
+  prm.H = H;
+  prm.G = G;
+  prm.gshift = __builtin_ctz((unsigned)G);
+  prm.P = P;
+  prm.nb = b;
+  prm.s = bud.s;
+  prm.w = bud.w;
+  prm.kk = bud.k;
+  prm.nL = (S + KVPOP_LIST_QBLOCK - 1) / KVPOP_LIST_QBLOCK;
+  prm.nqt = (S + P - 1) / P;
+  prm.nblk = z.nblk;
+  prm.cap = z.cap;
+  prm.ctiles = z.ctiles;
+  const float sc = scale > 0.0f ? scale : 1.0f / sqrtf((float)D);
+  prm.scale = sc;
+  prm.scale_log2 = sc * 1.4426950408889634f;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  return D == 128 ? launch_bwd<128>(prm, O, dO, lse, lse2, delta, keys, nkeys, cs)
+                  : launch_bwd<64>(prm, O, dO, lse, lse2, delta, keys, nkeys, cs);
+}

@@ -69,6 +69,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "kvpop_mask": ([P, c_int, c_int, c_int, Budget, P, P, P, P, P, c_size, P], c_int),
         "kvpop_attn_fwd": ([P, P, P, c_int, c_int, c_int, c_int, c_int, c_float, P, P, Budget, P, P, P],
                            c_int),
+        "kvpop_attn_bwd_workspace_size": ([c_int, c_int, c_int, c_int, Budget, P], c_int),
+        "kvpop_attn_bwd": ([P, P, P, P, P, P, c_int, c_int, c_int, c_int, c_int, c_float, P, P, Budget, P, P, P,
+                            P, c_size, P], c_int),
         "kvpop_future_target_workspace_size": ([c_int, c_int, c_int, c_int, P], c_int),
         "kvpop_future_target": ([P, P, P, c_int, c_int, c_int, c_int, c_int, c_float, c_int, P, P, c_size,
                                  P], c_int),
@@ -193,6 +196,38 @@ def attn_fwd(q, k, v, scale: float = 0.0, evict_at=None, lists=None, budget=(0, 
                                  _p(lists), Budget(*budget), _p(O), _p(lse), _stream(stream)),
            "kvpop_attn_fwd")
     return O, lse
+
+
+def attn_bwd_workspace_size(b, S, Hq, H, budget) -> int:
+    n = c_size()
+    _check(load().kvpop_attn_bwd_workspace_size(b, S, Hq, H, Budget(*budget), ctypes.byref(n)),
+           "attn_bwd_workspace_size")
+    return n.value
+
+
+def attn_bwd(q, k, v, O, dO, lse, evict_at, lists, budget, scale: float = 0.0, workspace=None, out=None,
+             stream=None):
+    """Gradient of the sparse attention: (dq [b,S,Hq,D], dk, dv [b,S,H,D]), fp32.
+
+    O and lse are the forward's outputs for the same inputs; dO is the upstream
+    gradient (bf16, the shape of q)."""
+    for t, name in ((q, "q"), (k, "k"), (v, "v"), (O, "O"), (dO, "dO")):
+        _need(t, torch.bfloat16, name)
+    _need(lse, torch.float32, "lse")
+    b, S, Hq, D = q.shape
+    H = k.shape[2]
+    if workspace is None:
+        workspace = torch.empty(attn_bwd_workspace_size(b, S, Hq, H, budget), dtype=torch.uint8, device=q.device)
+    if out is None:
+        dq = torch.empty((b, S, Hq, D), dtype=torch.float32, device=q.device)
+        dk = torch.empty((b, S, H, D), dtype=torch.float32, device=q.device)
+        dv = torch.empty_like(dk)
+    else:
+        dq, dk, dv = out
+    _check(load().kvpop_attn_bwd(_p(q), _p(k), _p(v), _p(O), _p(dO), _p(lse), b, S, Hq, H, D, float(scale),
+                                 _p(evict_at), _p(lists), Budget(*budget), _p(dq), _p(dk), _p(dv), _p(workspace),
+                                 workspace.numel(), _stream(stream)), "kvpop_attn_bwd")
+    return dq, dk, dv
 
 
 def target_workspace_size(b, S, Hq, H) -> int:

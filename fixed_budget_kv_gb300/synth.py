@@ -36,6 +36,7 @@ _CHUNK = 1 << 21
 
 # stream ids
 Q, K, V, PRIO, SPIKE = 1, 2, 3, 4, 5
+DO = 6  # upstream gradient dL/dO of the attention output (training path)
 QN, KN, VN, PRION = 11, 12, 13, 14
 
 
@@ -296,6 +297,11 @@ def normal_bf16_torch(seed: int, stream: int, shape, device, scale: float = 1.0,
         out[c0:c1] = x.to(torch.bfloat16)
         del z, u1, u2, x
     return out.view(*shape)
+
+
+def upstream_grad(wl: Workload) -> np.ndarray:
+    """dO for the attention backward: bf16 bits [b,S,Hq,D], N(0,1) draws of stream DO."""
+    return _bf16_tensor(wl.seed, DO, (wl.b, wl.S, wl.Hq, wl.D))
 
 
 def make_prefill_device(wl: Workload, device):

@@ -132,6 +132,37 @@ kvpop_status kvpop_attn_fwd(const void* q, const void* k, const void* v, int b, 
                             kvpop_stream stream);
 
 /* ------------------------------------------------------------------------
+ * kvpop_attn_bwd -- gradient of the sparse attention (the training path).
+ *
+ * [notes] section 2.1 (Figure 1 and the training flow: the student runs the
+ * sparse attention over the retained set and the backbone is trained through
+ * it).  For the sparse rows of kvpop_attn_fwd -- same q, k, v, evict_at, lists,
+ * budget and scale -- and an upstream gradient dO = dL/dO, with
+ * P_{q,t} = exp(scale * q.k_t - lse_q) over {t <= q : q < evict_at[t]}:
+ *   dv_t     = sum_q P_{q,t} dO_q
+ *   dS_{q,t} = P_{q,t} (dO_q . v_t - dO_q . O_q)
+ *   dq_q     = scale * sum_t dS_{q,t} k_t
+ *   dk_t     = scale * sum_q dS_{q,t} q_q
+ * where the sums over q run over the G query heads of the KV head too.
+ *   O, lse     the forward's outputs for these inputs: [b, S, Hq, D] bf16 and
+ *              [b, Hq, S] fp32 (dO . O stands in for sum_t P dP)
+ *   dO         [b, S, Hq, D] bf16
+ *   dq         [b, S, Hq, D] fp32; dk, dv [b, S, H, D] fp32; all overwritten
+ * workspace: kvpop_attn_bwd_workspace_size() bytes, 256-byte aligned (row
+ * constants and per-block key lists; contents undefined between calls).
+ * D 64 or 128, G dividing 128, tensors 16-byte aligned.  bf16 operands (P and
+ * dS rounded to bf16 before their products), fp32 accumulation; dk and dv
+ * take fp32 atomic additions, so their last bits vary from run to run.
+ * Errors: INVALID_ARG, UNSUPPORTED, CUDA.
+ * ---------------------------------------------------------------------- */
+kvpop_status kvpop_attn_bwd_workspace_size(int b, int S, int Hq, int H, kvpop_budget budget, size_t* bytes);
+kvpop_status kvpop_attn_bwd(const void* q, const void* k, const void* v, const void* O, const void* dO,
+                            const float* lse, int b, int S, int Hq, int H, int D, float scale,
+                            const int32_t* evict_at, const int32_t* lists, kvpop_budget budget, float* dq,
+                            float* dk, float* dv, void* workspace, size_t workspace_bytes,
+                            kvpop_stream stream);
+
+/* ------------------------------------------------------------------------
  * kvpop_future_target -- transposed-attention pass for the future mass.
  *
  * [notes] section 2.2 (m_t = (1/N_t) sum_{d=t+w}^{S-1} A_{d,t}) and section

@@ -1,0 +1,146 @@
+"""kvpop_attn_bwd on the GPU against the fp64 oracle's gradient of the sparse
+attention ("KVpop ... 精读笔记", section 2.1, Figure 1: the student is trained
+through the sparse attention).
+
+The GPU path runs mask -> sparse forward -> backward on the same seeded bf16
+inputs the oracle reads (q, k, v, the upstream gradient dO); the oracle
+recomputes everything in fp64 from those inputs.  Tolerance per tensor:
+max |gpu - oracle| <= 1e-2 * max |oracle|.  Derivation: the kernels round the
+softmax probabilities P and the logit gradients dS to bf16 (relative error up
+to 2^-9, about 1.1e-3 RMS for round-to-nearest) before the products whose
+fp32 sums give dv, dq and dk; each output is a random-sign sum of such terms,
+so its error is about that relative RMS of the sum's own scale, and the bound
+leaves a factor of about ten for the largest of many elements.  dO . O with
+the bf16 forward output stands in for sum_t P dP, an error of the same order."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fixed_budget_kv_gb300 import kvpop, synth
+from gpu_util import dev, dev_bf16, host
+
+pytestmark = pytest.mark.gpu
+
+TOL_GRAD = 1e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    kvpop.device_status(reset=True)
+    yield
+    st, words = kvpop.device_status(reset=True)
+    assert st == 0, f"device status {words}"
+
+
+def gpu_grads(wl, inp, dO_bits):
+    bud = (wl.s, wl.w, wl.k)
+    q, k, v = dev_bf16(inp.q), dev_bf16(inp.k), dev_bf16(inp.v)
+    dO = dev_bf16(dO_bits)
+    _, _, ev, lists = kvpop.mask(dev(inp.prio), *bud)
+    O, lse = kvpop.attn_fwd(q, k, v, 0.0, ev, lists, bud)
+    dq, dk, dv = kvpop.attn_bwd(q, k, v, O, dO, lse, ev, lists, bud)
+    return host(dq), host(dk), host(dv)
+
+
+def check(got, ref, what):
+    scale = float(np.abs(ref).max())
+    err = float(np.abs(got - ref).max())
+    assert np.isfinite(got).all(), f"{what}: non-finite values"
+    assert err <= TOL_GRAD * scale, f"{what}: max abs error {err:.3e} > {TOL_GRAD:.0e} * {scale:.3e}"
+    return err / scale
+
+
+CASES = [
+    # b, H, G, D, S, s, w, k
+    (1, 1, 2, 64, 256, 4, 32, 32),        # the tiny workload's shape
+    (1, 2, 4, 128, 700, 4, 48, 64),       # several tiles, ragged tail
+    (2, 2, 4, 128, 1000, 16, 100, 200),
+    (1, 1, 4, 128, 1000, 0, 0, 50),       # w = 0, s = 0: no band pass
+    (1, 2, 4, 64, 513, 3, 100, 0),        # k = 0 (sinks + window, no lists)
+    (1, 1, 8, 128, 400, 2, 17, 33),       # G = 8
+    (1, 2, 1, 64, 400, 2, 30, 60),        # G = 1: 128 positions per query tile
+    (1, 1, 4, 128, 600, 8, 16, 2000),     # budget covers the sequence
+    (1, 1, 16, 128, 350, 3, 24, 40),      # G = 16: 8 positions per query tile
+    (2, 3, 2, 128, 520, 5, 40, 70),       # G = 2, three KV heads, two sequences
+    (1, 1, 4, 128, 2100, 600, 300, 400),  # more sinks than a key tile, blocks of sinks only
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "b{}H{}G{}D{}S{}_s{}w{}k{}".format(*c))
+def test_attn_bwd_matches_oracle(case):
+    b, H, G, D, S, s, w, k = case
+    wl = synth.Workload("case", b=b, H=H, G=G, D=D, S=S, s=s, w=w, k=k, prio="uniform", seed=sum(case) + 7)
+    inp = synth.make_prefill(wl)
+    dO_bits = synth.upstream_grad(wl)
+    dq, dk, dv = gpu_grads(wl, inp, dO_bits)
+    rank, tau, _ = oracle.mask(inp.prio, s, w, k)
+    rq, rk, rv = oracle.attn_bwd(inp.f32("q"), inp.f32("k"), inp.f32("v"), synth.bf16_bits_to_f32(dO_bits),
+                                 1 / math.sqrt(D), rank, tau, s, w)
+    check(dq, rq, "dq")
+    check(dk, rk, "dk")
+    check(dv, rv, "dv")
+
+
+def test_attn_bwd_repeatable_and_workspace_reuse():
+    """A second call with the same workspace gives the same dq bit for bit (dq
+    has one writer per element) and dk/dv equal up to the atomics' order."""
+    wl = synth.Workload("case", b=1, H=2, G=4, D=128, S=900, s=4, w=64, k=96, prio="normal", seed=3)
+    inp = synth.make_prefill(wl)
+    bud = (wl.s, wl.w, wl.k)
+    q, k, v = dev_bf16(inp.q), dev_bf16(inp.k), dev_bf16(inp.v)
+    dO = dev_bf16(synth.upstream_grad(wl))
+    _, _, ev, lists = kvpop.mask(dev(inp.prio), *bud)
+    O, lse = kvpop.attn_fwd(q, k, v, 0.0, ev, lists, bud)
+    ws = torch.empty(kvpop.attn_bwd_workspace_size(1, wl.S, wl.Hq, wl.H, bud), dtype=torch.uint8, device="cuda")
+    a = [host(t) for t in kvpop.attn_bwd(q, k, v, O, dO, lse, ev, lists, bud, workspace=ws)]
+    c = [host(t) for t in kvpop.attn_bwd(q, k, v, O, dO, lse, ev, lists, bud, workspace=ws)]
+    assert np.array_equal(a[0], c[0])
+    for x, y in zip(a[1:], c[1:]):
+        assert np.abs(x - y).max() <= 1e-5 * np.abs(x).max()
+
+
+def test_attn_bwd_full_size_sampled():
+    """The 4B-like layer (b1 H8 G4 D128 S16384, s16 w512 k1520) in the launch the
+    benchmark times: dq of sampled rows and dk/dv of sampled keys (keys whose
+    rows the oracle can afford: window-only keys and keys held up to ~1500 rows
+    past the window) against the oracle; over all keys, the softmax-row
+    invariants sum_t dk_t = 0 and sum_t dv_t = sum over rows of dO."""
+    wl = synth.QWEN3_4B
+    bud = (wl.s, wl.w, wl.k)
+    q, k, v, prio = synth.make_prefill_device(wl, "cuda")
+    dO = synth.normal_bf16_torch(wl.seed, synth.DO, (wl.b, wl.S, wl.Hq, wl.D), "cuda")
+    _, _, ev, lists = kvpop.mask(prio, *bud)
+    O, lse = kvpop.attn_fwd(q, k, v, 0.0, ev, lists, bud)
+    dq, dk, dv = kvpop.attn_bwd(q, k, v, O, dO, lse, ev, lists, bud)
+    torch.cuda.synchronize()
+    # invariants over all keys of every head
+    dkh, dvh, dOh = host(dk).astype(np.float64), host(dv).astype(np.float64), host(dO).astype(np.float64)
+    assert np.abs(dkh.sum(axis=1)).max() <= 1e-3 * np.abs(dkh).sum(axis=1).max()
+    ref_v = dOh.reshape(wl.b, wl.S, wl.H, wl.G, wl.D).sum(axis=(1, 3))
+    assert np.abs(dvh.sum(axis=1) - ref_v).max() <= 1e-2 * np.abs(ref_v).max() + 1e-2
+    # sampled rows and keys against the oracle
+    qf, kf, vf, dOf = host(q), host(k), host(v), dOh.astype(np.float32)
+    rank, tau, _ = oracle.mask(host(prio), *bud)
+    evh = host(ev)
+    rng = np.random.default_rng(17)
+    pos = np.concatenate([rng.integers(0, wl.S, 40), [0, 1, 600, 4095, wl.S - 1]])
+    rows = np.stack([np.zeros_like(pos), rng.integers(0, wl.Hq, len(pos)), pos], axis=1).astype(np.int32)
+    rq = oracle.attn_bwd_rows(qf[0, rows[:, 2], rows[:, 1]], dOf[0, rows[:, 2], rows[:, 1]], kf, vf, wl.G,
+                              1 / math.sqrt(wl.D), rows, rank, tau, wl.s, wl.w)
+    check(host(dq)[0, rows[:, 2], rows[:, 1]], rq, "dq rows")
+    keys = []
+    for h in (0, 5):
+        life = evh[0, h] - np.arange(wl.S)
+        short = np.nonzero((life == wl.w) & (np.arange(wl.S) >= wl.s))[0]
+        mid = np.nonzero((life > wl.w + 200) & (life < wl.w + 1500))[0]
+        keys += [[0, h, t] for t in rng.choice(short, 3, replace=False)]
+        keys += [[0, h, t] for t in rng.choice(mid, 2, replace=False)]
+    keys = np.array(keys, np.int32)
+    rk, rv = oracle.attn_bwd_keys(qf, kf, vf, dOf, 1 / math.sqrt(wl.D), keys, rank, tau, wl.s, wl.w)
+    check(dkh[0, keys[:, 2], keys[:, 1]], rk, "dk keys")
+    check(dvh[0, keys[:, 2], keys[:, 1]], rv, "dv keys")
