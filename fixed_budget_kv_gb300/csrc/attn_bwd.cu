@@ -11,9 +11,11 @@
 // included) and the long pairs t + w <= q < evict_at[t].
 //
 // Four kernels:
-//   bwd_prep   Delta_q = dO_q.O_q and LSE_q in log2 units, in the order
+//   bwd_prep   -Delta_q = -dO_q.O_q and -LSE_q in log2 units, in the order
 //              [b, H, Spad, G]: one 128-row query tile (128/G positions x G
-//              heads) is 512 contiguous bytes; padded rows get LSE = +inf.
+//              heads) is 512 contiguous bytes; padded rows get -LSE = -inf.
+//              Negated so that the elementwise steps are one packed FMA
+//              (scale s - LSE) and one packed add (dP - Delta) per pair.
 //   bwd_keys   per block of kRows query positions and KV head, the keys that
 //              hold a long pair with a row of the block: sinks, the long-range
 //              list at the block's first row, and the keys entering the top-k
@@ -35,12 +37,12 @@ namespace {
 
 constexpr int kThreads = 384;
 constexpr int kKeys = 128;
-constexpr int kRows = 256;  // query positions per long-pair block (a multiple of the list block)
+constexpr int kRows = 512;  // query positions per long-pair block (a multiple of the list block)
 constexpr int kMetaStages = 4;
 constexpr int kBlockBytes = 128 * 128;  // 128 rows x 128 bytes (64 bf16)
 constexpr int kHalfBytes = 64 * 128;    // 64 rows of such a block
-constexpr int kRegsIo = 64;
-constexpr int kRegsEw = 216;
+constexpr int kRegsIo = 80;
+constexpr int kRegsEw = 208;
 constexpr int kRegsNeeded = (128 * kRegsIo + 256 * kRegsEw + kThreads - 1) / kThreads;
 static_assert(kRows % KVPOP_LIST_QBLOCK == 0 && kRows % 128 == 0, "block of rows");
 
@@ -49,8 +51,8 @@ struct BwdParams {
   CUtensorMap tkr, tvr;         // K, V as [b*S*H rows, D] with one-row boxes (gather4)
   const int32_t* evict_at;
   const int2* lists;
-  const float* lse2;   // [b, H, Spad, G]
-  const float* delta;  // [b, H, Spad, G]
+  const float* nlse2;   // [b, H, Spad, G]: -LSE * log2(e)
+  const float* ndelta;  // [b, H, Spad, G]: -dO . O
   const int2* keys;    // [b, H, nblk, cap]
   const int32_t* nkeys;  // [b, H, nblk]
   float* dq;
@@ -65,15 +67,14 @@ struct BwdParams {
 };
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
-__device__ __forceinline__ float pos_inf() { return __int_as_float(0x7f800000); }
 
 // ---------------------------------------------------------------------------
-// bwd_prep: Delta and LSE (log2 units) per row, in query-tile order
+// bwd_prep: -Delta and -LSE (log2 units) per row, in query-tile order
 // ---------------------------------------------------------------------------
 template <int D>
 __global__ void bwd_prep(const __nv_bfloat16* __restrict__ O, const __nv_bfloat16* __restrict__ dO,
                          const float* __restrict__ lse, int b, int S, int Spad, int H, int G,
-                         float* __restrict__ lse2, float* __restrict__ delta) {
+                         float* __restrict__ nlse2, float* __restrict__ ndelta) {
   grid_dep_wait();
   grid_dep_launch();
   constexpr int TPR = D / 8;  // threads per row, 8 elements each
@@ -106,13 +107,13 @@ __global__ void bwd_prep(const __nv_bfloat16* __restrict__ O, const __nv_bfloat1
     if (part == 0) {
       const int h = j / G, g = j - h * G;
       const size_t o = (((size_t)bi * H + h) * Spad + qp) * G + g;
-      float l2 = pos_inf();  // padded or empty rows: every probability is 0
+      float nl2 = neg_inf();  // padded or empty rows: every probability is 0
       if (qp < S) {
         const float l = lse[((size_t)bi * Hq + j) * S + qp];
-        if (l != neg_inf()) l2 = l * 1.4426950408889634f;
+        if (l != neg_inf()) nl2 = -l * 1.4426950408889634f;
       }
-      lse2[o] = l2;
-      delta[o] = acc;
+      nlse2[o] = nl2;
+      ndelta[o] = -acc;
     }
   }
 }
@@ -510,8 +511,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
       const DqItem x = make_dq_item(p, it);
       const int q = x.q0 + p_row;
       const size_t ro = ((size_t)(x.b * p.H + x.h) * p.Spad + x.q0) * G + row;
-      const float l2 = __ldg(p.lse2 + ro);
-      const float dl = __ldg(p.delta + ro);
+      const float nl2 = __ldg(p.nlse2 + ro);
+      const float nd = __ldg(p.ndelta + ro);
+      const uint64_t s2 = pack2(sl2, sl2), n2 = pack2(nl2, nl2), nd2 = pack2(nd, nd), zero2 = pack2(0.0f, 0.0f);
       for (int j = 0; j < x.NT; ++j, ++t) {
         const int sb = t & 1;
         if (!warp_wait(&bars->s_full[sb], (t >> 1) & 1, abort_flag)) {
@@ -543,19 +545,24 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
         for (int ch = 0; ch < 2; ++ch) {
           const int c32 = 2 * wg + ch;
           const int2 sum = km[kKeys + c32];
-          const bool fast = q >= sum.x && q < sum.y;
+          if (!(q >= sum.x && q < sum.y)) {  // some key of the chunk is not visible from this row
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              const int2 e = km[c32 * 32 + c];
+              if (!(e.x <= q && q < e.y)) sr[ch][c] = 0xff800000u;
+            }
+          }
+          // P = exp2(s scale_log2 - LSE2), dS = P (dP - Delta), packed in pairs
           uint32_t pk[16];
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {
-            float ds[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int2 e = km[c32 * 32 + c + u];
-              const bool vis = fast || (e.x <= q && q < e.y);
-              const float pr = vis ? ex2_approx(fmaf(__uint_as_float(sr[ch][c + u]), sl2, -l2)) : 0.0f;
-              ds[u] = pr * (__uint_as_float(dr[ch][c + u]) - dl);
-            }
-            pk[c >> 1] = pack_bf16x2(ds[0], ds[1]);
+            float e0, e1;
+            unpack2(fma2(pack2(__uint_as_float(sr[ch][c]), __uint_as_float(sr[ch][c + 1])), s2, n2), e0, e1);
+            const uint64_t pp = pack2(ex2_approx(e0), ex2_approx(e1));
+            const uint64_t dd = add2(pack2(__uint_as_float(dr[ch][c]), __uint_as_float(dr[ch][c + 1])), nd2);
+            float d0, d1;
+            unpack2(fma2(pp, dd, zero2), d0, d1);
+            pk[c >> 1] = pack_bf16x2(d0, d1);
           }
           tmem_st16(tl + 128 * sb + 64 * wg + 16 * ch, pk);  // over this warpgroup's own S columns
         }
@@ -627,7 +634,7 @@ struct KvLayout {
   static constexpr int v_off = k_off + DH * kBlockBytes;
   static constexpr int q_off = v_off + DH * kBlockBytes;           // stage i: Q at q_off + 2 i DH blocks
   static constexpr int stage_bytes = 2 * DH * kBlockBytes;         // Q then dO
-  static constexpr int row_off = q_off + NQS * stage_bytes;        // stage i: 128 LSE2 then 128 Delta floats
+  static constexpr int row_off = q_off + NQS * stage_bytes;        // stage i: 128 -LSE2 then 128 -Delta floats
   static constexpr int kmeta_off = row_off + NQS * 1024;
   static constexpr int bar_off = kmeta_off + kKeys * 8;
   static constexpr int misc_off = bar_off + (int)sizeof(KvBars<NQS>);
@@ -768,8 +775,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
               tma_load_4d(qs + (DH + dh) * kBlockBytes, &p.tdo, bar, dh * 64, x.h * G, qt * P, x.b);
             }
             uint8_t* rs = smem + L::row_off + stg * 1024;
-            bulk_load(rs, p.lse2 + rbase + (size_t)qt * 128, 512, bar);
-            bulk_load(rs + 512, p.delta + rbase + (size_t)qt * 128, 512, bar);
+            bulk_load(rs, p.nlse2 + rbase + (size_t)qt * 128, 512, bar);
+            bulk_load(rs + 512, p.ndelta + rbase + (size_t)qt * 128, 512, bar);
           }
         }
       }
@@ -912,7 +919,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
     const int r = quarter * 32 + lane;  // this thread's key (TMEM lane)
     const uint32_t tl = tbase + ((uint32_t)(quarter * 32) << 16);
     const float sl2 = p.scale_log2;
-    const int w = p.w;
+    const uint64_t s2 = pack2(sl2, sl2), zero2 = pack2(0.0f, 0.0f);
+    const int w = p.w, gs = p.gshift;
     bool ok = true;
     int u = 0, n = 0;
     for (int it = it0; ok && it < p.nitems; it += dit) {
@@ -945,26 +953,41 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
         tmem_wait_ld_dep(sr[1]);
         tmem_wait_ld_dep(dr[0]);
         tmem_wait_ld_dep(dr[1]);
-        const float* rl2 = reinterpret_cast<const float*>(smem + L::row_off + stg * 1024) + 64 * hh;
-        const float* rdl = rl2 + 128;
-        const int pos0 = (x.qt0 + i) * P;  // position of row 0 of the tile
+        // this half's rows: row 64 hh + c is at position pos_h + (c >> gshift);
+        // the key sees the columns [clo, chi)
+        const int pos_h = (x.qt0 + i) * P + ((64 * hh) >> gs);
+        const int a = lo - pos_h, bnd = hi - pos_h;
+        const int clo = a <= 0 ? 0 : min(64, min(a, 64) << gs);
+        const int chi = bnd <= 0 ? 0 : min(64, min(bnd, 64) << gs);
+        if (clo > 0 || chi < 64) {
+#pragma unroll
+          for (int ch = 0; ch < 2; ++ch)
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+              if (32 * ch + c < clo || 32 * ch + c >= chi) sr[ch][c] = 0xff800000u;
+        }
+        const float4* rl2 = reinterpret_cast<const float4*>(smem + L::row_off + stg * 1024) + 16 * hh;
+        const float4* rdl = rl2 + 32;
 #pragma unroll
         for (int ch = 0; ch < 2; ++ch) {
           uint32_t pk[16], dk[16];
 #pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            float pr[2], ds[2];
+          for (int c = 0; c < 32; c += 4) {
+            const float4 nl = rl2[(32 * ch + c) >> 2];  // -LSE2 of four rows (a broadcast read)
+            const float4 nd = rdl[(32 * ch + c) >> 2];  // -Delta of the same rows
 #pragma unroll
-            for (int v2 = 0; v2 < 2; ++v2) {
-              const int cr = 64 * hh + 32 * ch + c + v2;  // row of the tile
-              const int qp = pos0 + (cr >> p.gshift);
-              const bool vis = qp >= lo && qp < hi;
-              const float e = vis ? ex2_approx(fmaf(__uint_as_float(sr[ch][c + v2]), sl2, -rl2[32 * ch + c + v2])) : 0.0f;
-              pr[v2] = e;
-              ds[v2] = e * (__uint_as_float(dr[ch][c + v2]) - rdl[32 * ch + c + v2]);
+            for (int v2 = 0; v2 < 4; v2 += 2) {
+              const uint64_t n2 = v2 == 0 ? pack2(nl.x, nl.y) : pack2(nl.z, nl.w);
+              const uint64_t d2 = v2 == 0 ? pack2(nd.x, nd.y) : pack2(nd.z, nd.w);
+              float e0, e1;
+              unpack2(fma2(pack2(__uint_as_float(sr[ch][c + v2]), __uint_as_float(sr[ch][c + v2 + 1])), s2, n2), e0, e1);
+              const float p0 = ex2_approx(e0), p1 = ex2_approx(e1);
+              const uint64_t dd = add2(pack2(__uint_as_float(dr[ch][c + v2]), __uint_as_float(dr[ch][c + v2 + 1])), d2);
+              float d0, d1;
+              unpack2(fma2(pack2(p0, p1), dd, zero2), d0, d1);
+              pk[(c + v2) >> 1] = pack_bf16x2(p0, p1);
+              dk[(c + v2) >> 1] = pack_bf16x2(d0, d1);
             }
-            pk[c >> 1] = pack_bf16x2(pr[0], pr[1]);
-            dk[c >> 1] = pack_bf16x2(ds[0], ds[1]);
           }
           tmem_st16(tl + col + 16 * ch, pk);
           tmem_st16(tl + col + 64 + 16 * ch, dk);
@@ -1035,7 +1058,7 @@ kvpop_status prepare(K kern, int smem_bytes, const char* what) {
 }
 
 template <int D>
-kvpop_status launch_bwd(BwdParams prm, const void* O, const void* dO, const float* lse, float* lse2, float* delta,
+kvpop_status launch_bwd(BwdParams prm, const void* O, const void* dO, const float* lse, float* nlse2, float* ndelta,
                         int2* keys, int32_t* nkeys, cudaStream_t cs) {
   const int b = prm.nb, S = prm.S, H = prm.H, G = prm.G;
   const int nbh = b * H;
@@ -1045,7 +1068,7 @@ kvpop_status launch_bwd(BwdParams prm, const void* O, const void* dO, const floa
     const int blocks = (int)std::min<long long>((n + 255) / 256, 8LL * num_sms());
     st = cuda_check(launch_pdl(bwd_prep<D>, dim3(blocks), dim3(256), 0, cs,
                                static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), lse, b,
-                               S, prm.Spad, H, G, lse2, delta),
+                               S, prm.Spad, H, G, nlse2, ndelta),
                     "kvpop_attn_bwd: prep");
     if (st != KVPOP_OK) return st;
   }
@@ -1196,14 +1219,14 @@ extern "C" kvpop_status kvpop_attn_bwd(const void* q, const void* k, const void*
       return KVPOP_ERR_CUDA;
   }
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  float* lse2 = reinterpret_cast<float*>(ws);
-  float* delta = reinterpret_cast<float*>(ws + z.rows_bytes);
+  float* nlse2 = reinterpret_cast<float*>(ws);
+  float* ndelta = reinterpret_cast<float*>(ws + z.rows_bytes);
   int2* keys = reinterpret_cast<int2*>(ws + 2 * z.rows_bytes);
   int32_t* nkeys = reinterpret_cast<int32_t*>(ws + 2 * z.rows_bytes + z.keys_bytes);
   prm.evict_at = evict_at;
   prm.lists = reinterpret_cast<const int2*>(lists);
-  prm.lse2 = lse2;
-  prm.delta = delta;
+  prm.nlse2 = nlse2;
+  prm.ndelta = ndelta;
   prm.keys = keys;
   prm.nkeys = nkeys;
   prm.dq = dq;
@@ -1230,6 +1253,6 @@ extern "C" kvpop_status kvpop_attn_bwd(const void* q, const void* k, const void*
   prm.scale = sc;
   prm.scale_log2 = sc * 1.4426950408889634f;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  return D == 128 ? launch_bwd<128>(prm, O, dO, lse, lse2, delta, keys, nkeys, cs)
-                  : launch_bwd<64>(prm, O, dO, lse, lse2, delta, keys, nkeys, cs);
+  return D == 128 ? launch_bwd<128>(prm, O, dO, lse, nlse2, ndelta, keys, nkeys, cs)
+                  : launch_bwd<64>(prm, O, dO, lse, nlse2, ndelta, keys, nkeys, cs);
 }
