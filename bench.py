@@ -66,7 +66,7 @@ def parse():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--only", choices=["mask", "sparse", "dense", "target", "decode", "labels"],
+    ap.add_argument("--only", choices=["mask", "sparse", "dense", "target", "decode", "labels", "bwd"],
                     help="for a profiler: set up the workload, run that pass twice (decode: 24 steps), "
                          "print one status line and exit")
     return ap.parse_args()
@@ -259,8 +259,8 @@ def run_gpu(args, rank, world, local_rank):
                                      "unit": "tokens/s",
                                      "note": "mask + sparse forward + target on the sparse LSE; per-pass event times"}
 
-    result["training_side"] = training_side(args, wl, q, k, v, prio, ev_t, lists, lse_s, lse_d, target,
-                                            ws_tgt, dev, world)
+    result["training_side"] = training_side(args, wl, q, k, v, prio, ev_t, lists, O, lse_s, lse_d, target,
+                                            ws_tgt, dev, world, pk, flops)
     if not args.no_e2e:
         result["e2e"] = e2e(args, wl, q, k, v, prio, ws_mask, ws_tgt, dev, world)
     if not args.no_decode:
@@ -276,14 +276,15 @@ DECAY_GAMMA = (0.90, 0.99)   # per KV head, spread linearly between these
 TARGET_EPS = 1e-6
 
 
-def training_side(args, wl, q, k, v, prio, ev_t, lists, lse_s, lse_d, target, ws_tgt, dev, world):
+def training_side(args, wl, q, k, v, prio, ev_t, lists, O, lse_s, lse_d, target, ws_tgt, dev, world, pk, flops):
     """The training-side passes on the same workload, each timed alone (CUDA events,
     mean of `steps` launches): the normalised target, the teacher boundary labels,
-    the pairwise boundary loss with its gradient; and the sparse-LSE variant of the
-    pipeline (mask, sparse forward, target on the sparse LSE: no dense pass) with the
-    deviation of its target from the dense-LSE one."""
+    the pairwise boundary loss with its gradient, the gradient of the sparse
+    attention (upstream gradient dO: N(0,1) draws of its own stream); and the
+    sparse-LSE variant of the pipeline (mask, sparse forward, target on the sparse
+    LSE: no dense pass) with the deviation of its target from the dense-LSE one."""
     import torch
-    from fixed_budget_kv_gb300 import kvpop
+    from fixed_budget_kv_gb300 import kvpop, synth
     b, S, H = wl.b, wl.S, wl.H
     bud = (wl.s, wl.w, wl.k)
     lg = torch.log(torch.linspace(DECAY_GAMMA[0], DECAY_GAMMA[1], H, device=dev, dtype=torch.float32))
@@ -294,11 +295,16 @@ def training_side(args, wl, q, k, v, prio, ev_t, lists, lse_s, lse_d, target, ws
     loss = torch.empty(2, dtype=torch.float32, device=dev)
     grad = torch.empty_like(r_hat)
     t_sparse = torch.empty_like(target)
+    dO = synth.normal_bf16_torch(wl.seed, synth.DO, tuple(q.shape), dev)
+    ws_bwd = torch.empty(kvpop.attn_bwd_workspace_size(b, S, wl.Hq, H, bud), dtype=torch.uint8, device=dev)
+    grads = (torch.empty(q.shape, dtype=torch.float32, device=dev), torch.empty(k.shape, dtype=torch.float32, device=dev),
+             torch.empty(k.shape, dtype=torch.float32, device=dev))
     passes = {
         "target_normalize": lambda: kvpop.target_normalize(target, wl.G, wl.w, TARGET_EPS, out=r_tgt),
         "teacher_labels": lambda: kvpop.teacher_labels(r_tgt, *bud, DECAY_STEP, lg, out=(tb, y)),
         "boundary_loss": lambda: kvpop.boundary_loss(r_hat, tb, y, wl.w, DECAY_STEP, lg, 1.0, out=(loss, grad)),
         "sparse_lse_target": lambda: kvpop.future_target(q, k, lse_s, wl.w, workspace=ws_tgt, out=t_sparse),
+        "sparse_attn_bwd": lambda: kvpop.attn_bwd(q, k, v, O, dO, lse_s, ev_t, lists, bud, workspace=ws_bwd, out=grads),
     }
     out = {}
     n = max(3, args.steps // 2)
@@ -317,6 +323,14 @@ def training_side(args, wl, q, k, v, prio, ev_t, lists, lse_s, lse_d, target, ws
         raise RuntimeError(f"device status after the training-side passes: {words}")
     out["teacher_labels"]["rows_per_s"] = round(job_throughput(b * H * S, world, out["teacher_labels"]["ms"]), 1)
     out["boundary_loss"]["pairs"] = int(loss[1].item())
+    # useful work of the backward: five products of 2 D flops per retained (row, key) pair
+    # (S = Q K^T, dP = dO V^T, dV, dQ, dK), i.e. 2.5 x the forward's useful flops
+    bwd_flops = 2.5 * flops["sparse_attn"]
+    bwd_tf = bwd_flops / (out["sparse_attn_bwd"]["ms"] / 1e3) / 1e12
+    out["sparse_attn_bwd"].update({"tflops": round(bwd_tf, 1),
+                                   "frac_of_sustained_bf16": round(bwd_tf / pk["bf16_tflops_sustained"], 3),
+                                   "tokens_per_s": round(job_throughput(b * S, world, out["sparse_attn_bwd"]["ms"]), 1),
+                                   "useful_flops": bwd_flops})
     fin = torch.isfinite(target)
     dev_abs = (t_sparse - target)[fin].abs()
     out["sparse_lse_target"]["deviation_from_dense_lse_target"] = {
@@ -536,8 +550,11 @@ def run_only(args):
         wl = synth.PREFILL_WORKLOADS[args.workload]
         q, k, v, prio = synth.make_prefill_device(wl, dev)
         bud = (wl.s, wl.w, wl.k)
-        if args.only in ("sparse", "mask"):
+        if args.only in ("sparse", "mask", "bwd"):
             _, _, ev, lists = kvpop.mask(prio, *bud)
+        if args.only == "bwd":
+            O, lse_s = kvpop.attn_fwd(q, k, v, 0.0, ev, lists, bud)
+            dO = synth.normal_bf16_torch(wl.seed, synth.DO, tuple(q.shape), dev)
         if args.only in ("dense", "target", "labels"):
             _, lse_d = kvpop.attn_fwd(q, k, None, 0.0, want_o=False)
         if args.only == "labels":
@@ -550,6 +567,8 @@ def run_only(args):
                 kvpop.mask(prio, *bud)
             elif args.only == "sparse":
                 kvpop.attn_fwd(q, k, v, 0.0, ev, lists, bud)
+            elif args.only == "bwd":
+                kvpop.attn_bwd(q, k, v, O, dO, lse_s, ev, lists, bud)
             elif args.only == "dense":
                 kvpop.attn_fwd(q, k, None, 0.0, want_o=False)
             else:
