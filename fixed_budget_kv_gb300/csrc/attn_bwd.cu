@@ -44,6 +44,16 @@ constexpr int kHalfBytes = 64 * 128;    // 64 rows of such a block
 constexpr int kRegsIo = 80;
 constexpr int kRegsEw = 208;
 constexpr int kRegsNeeded = (128 * kRegsIo + 256 * kRegsEw + kThreads - 1) / kThreads;
+// The dQ kernel adds a fourth warpgroup of gather issuers: tile::gather4 from one
+// warp moves only about 8 B/clk/SM, and its K and V tiles (64 KB per 128 query
+// rows) are spread over three issuing warps each.
+constexpr int kDqThreads = 512;
+constexpr int kDqRegsIo = 64;
+constexpr int kDqRegsHelp = 48;
+constexpr int kDqRegsEw = 200;
+constexpr int kDqRegsNeeded = (128 * kDqRegsIo + 128 * kDqRegsHelp + 256 * kDqRegsEw + kDqThreads - 1) / kDqThreads;
+constexpr int kGatherOps = 2 * (kKeys / 4);  // gather4 ops per 128-key tile: two 64-dim halves
+constexpr int kOpsPerIssuer = (kGatherOps + 2) / 3;
 static_assert(kRows % KVPOP_LIST_QBLOCK == 0 && kRows % 128 == 0, "block of rows");
 
 struct BwdParams {
@@ -224,7 +234,7 @@ __device__ __forceinline__ DqItem make_dq_item(const BwdParams& p, int it) {
   return x;
 }
 
-// Warp roles (384 threads):
+// Warp roles (512 threads):
 //   warp 0      key metadata of each K/V tile: (position, eviction row) per key
 //               and per 32-key chunk the latest position and earliest
 //               eviction row (rows inside that range skip masking)
@@ -235,13 +245,15 @@ __device__ __forceinline__ DqItem make_dq_item(const BwdParams& p, int it) {
 //   warps 4-11  elementwise: warpgroup 0 takes keys 0-63 of each tile,
 //               warpgroup 1 keys 64-127, one query row per thread; then the
 //               dQ epilogue (warpgroup 0 the low half of the columns)
+//   warps 12-15 gather helpers: 12 and 13 issue two thirds of each gathered K
+//               tile's ops with warp 2, 14 and 15 of each V tile's with warp 3
 // TMEM columns: S of key tile t at 128 (t & 1) (two buffers), dP at 256, dQ at
 // 384.  Each warpgroup packs its 64 dS values (bf16 pairs) over the first 32
 // of its own 64 S columns, so neither overwrites S the other has not read.
 // MMA order: S_{t+1}, dP_{t+1} (once dP_t has been read), then dQ += dS_t K_t,
 // so the tensor core computes the next tile while the elementwise warps work.
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(kDqThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdParams p) {
   using L = DqLayout<D>;
   constexpr int DH = L::DH;
   constexpr int NS = L::NS;
@@ -274,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
     mbar_init(&bars->o_empty, 8);
     for (int i = 0; i < kMetaStages; ++i) {
       mbar_init(&bars->meta_full[i], 1);
-      mbar_init(&bars->meta_empty[i], 10);  // 8 elementwise warps + 2 loader warps
+      mbar_init(&bars->meta_empty[i], 14);  // 8 elementwise warps + 2 loader warps + 4 helpers
     }
     mbar_init(&bars->drain, 1);
     *abort_flag = 0;
@@ -299,9 +311,61 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
   const uint32_t do_addr = sbase + L::do_off;
   const uint32_t k_addr = sbase + L::k_off;
   const uint32_t v_addr = sbase + L::v_off;
+  // gather4 op `o` of a gathered tile (o < kGatherOps): keys 4 (o % 32) .. + 3, dims 64 (o / 32) ..
+  auto issue_gather_ops = [&](int first, int count, const int2* km, int row_base, int off, int st,
+                              const CUtensorMap* rmap, uint64_t* bar) {
+    if (lane < count) {
+      const int o = first + lane;
+      const int q4 = o & 31, d2 = o >> 5;
+      int rows[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int pos = km[4 * q4 + u].x;
+        rows[u] = pos != 0x7fffffff ? row_base + pos * p.H : row_base;  // padding: any row, masked
+      }
+      tma_gather4(smem + off + (st * DH + d2) * kBlockBytes + q4 * 512, rmap, bar, d2 * 64, rows[0], rows[1],
+                  rows[2], rows[3]);
+    }
+  };
 
-  if (warp < 4) {
-    setmaxnreg_dec<kRegsIo>();
+  if (warp >= 12) {
+    setmaxnreg_dec<kDqRegsHelp>();
+    // ---------------------------------------------------------- gather helpers
+    const bool is_v = warp >= 14;
+    const int part = 1 + (warp & 1);  // issuer 0 is the loader warp itself
+    const CUtensorMap* rmap = is_v ? &p.tvr : &p.tkr;
+    uint64_t* full = is_v ? bars->v_full : bars->k_full;
+    uint64_t* empty = is_v ? bars->v_empty : bars->k_empty;
+    const int off = is_v ? L::v_off : L::k_off;
+    const int first = part * kOpsPerIssuer;
+    const int count = min(kOpsPerIssuer, (DH * kKeys / 4) - first);
+    bool ok = true;
+    int t = 0;
+    for (int it = it0; ok && it < p.nitems; it += dit) {
+      const DqItem x = make_dq_item(p, it);
+      const int row_base = x.b * S * p.H + x.h;
+      for (int j = 0; j < x.NT; ++j, ++t) {
+        const int st = t % NS;
+        const int ms = t % kMetaStages;
+        if (!warp_wait(&bars->meta_full[ms], (t / kMetaStages) & 1, abort_flag)) {
+          if (lane == 0) fail(SITE_ATTN_PRODUCER, 40);
+          ok = false;
+          break;
+        }
+        // every tile, gathered or not: a parity wait is only exact while the
+        // waiter is at most one phase ahead of the barrier
+        if (!warp_wait(&empty[st], ((t / NS) & 1) ^ 1, abort_flag)) {
+          if (lane == 0) fail(SITE_ATTN_PRODUCER, 43);
+          ok = false;
+          break;
+        }
+        if (j < x.NTg) issue_gather_ops(first, count, meta + ms * (kKeys + 4), row_base, off, st, rmap, &full[st]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->meta_empty[ms]);
+      }
+    }
+  } else if (warp < 4) {
+    setmaxnreg_dec<kDqRegsIo>();
     if (warp == 0) {
       // ---------------------------------------------------------- key metadata
       bool ok = true;
@@ -475,17 +539,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
           if (lane == 0) mbar_arrive_expect_tx(&full[st], DH * kBlockBytes);
           __syncwarp();
           if (j < x.NTg) {
-            const int2* km = meta + ms * (kKeys + 4);
-            int rows[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int pos = km[4 * lane + u].x;
-              rows[u] = pos != 0x7fffffff ? row_base + pos * p.H : row_base;  // padding: any row, masked
-            }
-#pragma unroll
-            for (int d2 = 0; d2 < DH; ++d2)
-              tma_gather4(smem + off + (st * DH + d2) * kBlockBytes + lane * 512, rmap, &full[st], d2 * 64,
-                          rows[0], rows[1], rows[2], rows[3]);
+            // the first third of the tile's gather4 ops; warps 12-15 issue the rest
+            issue_gather_ops(0, min(kOpsPerIssuer, DH * kKeys / 4), meta + ms * (kKeys + 4), row_base, off, st,
+                             rmap, &full[st]);
           } else if (lane == 0) {
             const int span_row = x.sp0 + (j - x.NTg) * kKeys;
             for (int d2 = 0; d2 < DH; ++d2)
@@ -497,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
       }
     }
   } else {
-    setmaxnreg_inc<kRegsEw>();
+    setmaxnreg_inc<kDqRegsEw>();
     // ------------------------------------------------------------ elementwise
     const int wg = (warp - 4) >> 2;  // key half of each tile
     const int quarter = warp & 3;
@@ -1044,14 +1100,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
 }
 
 template <typename K>
-kvpop_status prepare(K kern, int smem_bytes, const char* what) {
+kvpop_status prepare(K kern, int smem_bytes, const char* what, int regs_needed = kRegsNeeded) {
   kvpop_status st = cuda_check(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes), what);
   if (st != KVPOP_OK) return st;
   cudaFuncAttributes fa;
   st = cuda_check(cudaFuncGetAttributes(&fa, kern), what);
   if (st != KVPOP_OK) return st;
-  if (((fa.numRegs + 7) / 8) * 8 < kRegsNeeded) {
-    set_last_error("%s: kernel built with %d registers per thread, %d needed", what, fa.numRegs, kRegsNeeded);
+  if (((fa.numRegs + 7) / 8) * 8 < regs_needed) {
+    set_last_error("%s: kernel built with %d registers per thread, %d needed", what, fa.numRegs, regs_needed);
     return KVPOP_ERR_INTERNAL;
   }
   return KVPOP_OK;
@@ -1080,10 +1136,10 @@ kvpop_status launch_bwd(BwdParams prm, const void* O, const void* dO, const floa
   {
     using L = DqLayout<D>;
     auto kern = bwd_dq_kernel<D>;
-    if ((st = prepare(kern, L::total, "kvpop_attn_bwd: dq")) != KVPOP_OK) return st;
+    if ((st = prepare(kern, L::total, "kvpop_attn_bwd: dq", kDqRegsNeeded)) != KVPOP_OK) return st;
     BwdParams pq = prm;
     pq.nitems = prm.nqt * nbh;
-    st = cuda_check(launch_pdl(kern, dim3(std::min(pq.nitems, num_sms())), dim3(kThreads), L::total, cs, pq),
+    st = cuda_check(launch_pdl(kern, dim3(std::min(pq.nitems, num_sms())), dim3(kDqThreads), L::total, cs, pq),
                     "kvpop_attn_bwd: dq launch");
     if (st != KVPOP_OK) return st;
   }
