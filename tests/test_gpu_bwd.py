@@ -144,3 +144,40 @@ def test_attn_bwd_full_size_sampled():
     rk, rv = oracle.attn_bwd_keys(qf, kf, vf, dOf, 1 / math.sqrt(wl.D), keys, rank, tau, wl.s, wl.w)
     check(dkh[0, keys[:, 2], keys[:, 1]], rk, "dk keys")
     check(dvh[0, keys[:, 2], keys[:, 1]], rv, "dv keys")
+
+
+def test_attn_bwd_long_context_sampled():
+    """The long-context workload (b1 H8 G4 D128 S131072, s16 w1024 k3056): dq of sampled
+    rows and dk/dv of window-only keys against the oracle; the softmax-row invariants
+    over all keys."""
+    wl = synth.LONG
+    bud = (wl.s, wl.w, wl.k)
+    q, k, v, prio = synth.make_prefill_device(wl, "cuda")
+    dO = synth.normal_bf16_torch(wl.seed, synth.DO, (wl.b, wl.S, wl.Hq, wl.D), "cuda")
+    _, _, ev, lists = kvpop.mask(prio, *bud)
+    O, lse = kvpop.attn_fwd(q, k, v, 0.0, ev, lists, bud)
+    dq, dk, dv = kvpop.attn_bwd(q, k, v, O, dO, lse, ev, lists, bud)
+    torch.cuda.synchronize()
+    # invariants, summed on the device in fp64
+    dks = dk.double().sum(dim=1)
+    assert float(dks.abs().max()) <= 1e-3 * float(dk.double().abs().sum(dim=1).max())
+    ref_v = dO.double().view(wl.b, wl.S, wl.H, wl.G, wl.D).sum(dim=(1, 3))
+    assert float((dv.double().sum(dim=1) - ref_v).abs().max()) <= 1e-2 * float(ref_v.abs().max()) + 1e-2
+    qf, kf, vf = host(q), host(k), host(v)
+    rank, tau, _ = oracle.mask(host(prio), *bud)
+    evh = host(ev)
+    rng = np.random.default_rng(23)
+    pos = np.concatenate([rng.integers(0, wl.S, 24), [0, 4095, 65536, wl.S - 1]])
+    rows = np.stack([np.zeros_like(pos), rng.integers(0, wl.Hq, len(pos)), pos], axis=1).astype(np.int32)
+    qi, ji = torch.from_numpy(rows[:, 2]).long().cuda(), torch.from_numpy(rows[:, 1]).long().cuda()
+    rq = oracle.attn_bwd_rows(host(q[0, qi, ji]), host(dO[0, qi, ji]), kf, vf, wl.G, 1 / math.sqrt(wl.D), rows,
+                              rank, tau, wl.s, wl.w)
+    check(host(dq[0, qi, ji]), rq, "dq rows")
+    h = 3
+    life = evh[0, h] - np.arange(wl.S)
+    short = np.nonzero((life == wl.w) & (np.arange(wl.S) >= wl.s) & (np.arange(wl.S) < wl.S - wl.w))[0]
+    keys = np.array([[0, h, t] for t in rng.choice(short, 3, replace=False)], np.int32)
+    # the oracle only needs the rows these keys reach: positions [t, t + w) of KV head h
+    rk, rv = oracle.attn_bwd_keys(qf, kf, vf, host(dO), 1 / math.sqrt(wl.D), keys, rank, tau, wl.s, wl.w)
+    check(host(dk[0, torch.from_numpy(keys[:, 2]).long().cuda(), h]), rk, "dk keys")
+    check(host(dv[0, torch.from_numpy(keys[:, 2]).long().cuda(), h]), rv, "dv keys")
