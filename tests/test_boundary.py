@@ -90,3 +90,35 @@ def test_training_side_validation(lib):
     assert lib.kvpop_boundary_loss(P, P, P, None, 1, 1, 8, 2, 2, P, 0.0, P, P, None) == 1   # tau = 0
     assert lib.kvpop_boundary_loss(P, P, P, None, 1, 1, 8, 2, 2, None, 1.0, P, P, None) == 1
     assert lib.kvpop_boundary_loss(P, P, P, None, 64, 64, 8192, 2, 2, P, 1.0, P, P, None) == 2  # > 2^24
+
+
+def test_attn_bwd_sizes_and_validation(lib):
+    # workspace: two fp32 row arrays [b,H,S rounded up to 128,G], per 512-row block a key
+    # list of s + k + 512 pairs, and one count per block (each part 256-byte aligned)
+    def up(x):
+        return (x + 255) // 256 * 256
+    b, S, Hq, H, bud = 1, 1000, 8, 2, (3, 40, 60)
+    nblk = (S + 511) // 512
+    want = 2 * up(b * H * 1024 * 4 * 4) + up(b * H * nblk * (3 + 60 + 512) * 8) + up(b * H * nblk * 4)
+    assert kvpop.attn_bwd_workspace_size(b, S, Hq, H, bud) == want
+    n = ctypes.c_size_t()
+    assert lib.kvpop_attn_bwd_workspace_size(1, 0, 8, 2, kvpop.Budget(1, 1, 1), ctypes.byref(n)) == 1
+    assert lib.kvpop_attn_bwd_workspace_size(1, 10, 8, 2, kvpop.Budget(0, 0, 0), ctypes.byref(n)) == 1
+    assert lib.kvpop_attn_bwd_workspace_size(1, 10, 6, 2, kvpop.Budget(1, 1, 1), ctypes.byref(n)) == 2  # G = 3
+    assert lib.kvpop_attn_bwd_workspace_size(1, 10, 8, 2, kvpop.Budget(1, 1, 1), None) == 1
+    P = ctypes.c_void_p(256)
+    ok = kvpop.Budget(1, 2, 3)
+    ws = ctypes.c_size_t(1 << 30)
+
+    def call(q=P, O=P, D=64, ev=P, lists=P, bud=ok, dq=P, wsp=P, wsn=ws, Hq=8, H=2):
+        return lib.kvpop_attn_bwd(q, P, P, O, P, P, 1, 100, Hq, H, D, 0.0, ev, lists, bud, dq, P, P, wsp, wsn, None)
+    assert call(O=None) == 1                        # O missing
+    assert call(ev=None) == 1                       # not sparse
+    assert call(lists=None) == 1                    # k > 0 needs lists
+    assert call(dq=None) == 1                       # output missing
+    assert call(D=96) == 2                          # head dim
+    assert call(Hq=6, H=2) == 2                     # G = 3 does not divide 128
+    assert call(wsn=ctypes.c_size_t(16)) == 1       # workspace too small
+    assert call(wsp=ctypes.c_void_p(272)) == 2      # workspace not 256-byte aligned
+    assert call(q=ctypes.c_void_p(264)) == 2        # tensor not 16-byte aligned
+    assert lib.kvpop_last_error()
