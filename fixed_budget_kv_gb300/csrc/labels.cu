@@ -56,6 +56,8 @@ __global__ void __launch_bounds__(kLabelThreads)
   __shared__ uint32_t hist[256];
   __shared__ unsigned long long s_prefix;
   __shared__ int s_need, s_left, s_found;
+  __shared__ int red[kLabelThreads / 32];
+  __shared__ unsigned long long red64[kLabelThreads / 32];
   const int bh = blockIdx.y;
   const int h = bh % H;
   const float* r = r_tgt + (size_t)bh * S;
@@ -67,6 +69,37 @@ __global__ void __launch_bounds__(kLabelThreads)
   if (cache)
     for (int t = tid; t < tmax; t += kLabelThreads) rs[t] = r[t];
   __syncthreads();
+  auto key_of = [&](int q, int t) -> unsigned long long {
+    return label_key(decayed_score(cache ? rs[t] : __ldg(r + t), q, t, n, lg), t);
+  };
+  auto block_sum = [&](int v) -> int {
+    v = __reduce_add_sync(0xffffffffu, v);
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    int tot = 0;
+#pragma unroll
+    for (int i = 0; i < kLabelThreads / 32; ++i) tot += red[i];
+    __syncthreads();
+    return tot;
+  };
+  auto block_extreme = [&](unsigned long long v, bool up) -> unsigned long long {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long u = __shfl_xor_sync(0xffffffffu, v, o);
+      v = up ? (u < v ? u : v) : (u > v ? u : v);
+    }
+    if (lane == 0) red64[warp] = v;
+    __syncthreads();
+    unsigned long long m = red64[0];
+#pragma unroll
+    for (int i = 1; i < kLabelThreads / 32; ++i) {
+      const unsigned long long u = red64[i];
+      m = up ? (u < m ? u : m) : (u > m ? u : m);
+    }
+    __syncthreads();
+    return m;
+  };
+  int prev = -1;  // the previous row's cutoff
   for (int q = q0; q < q1; ++q) {
     const int tn = q - w;
     const size_t out = (size_t)bh * S + q;
@@ -77,11 +110,35 @@ __global__ void __launch_bounds__(kLabelThreads)
       }
       continue;
     }
-    // radix select of the k-th largest key among t in [s, tn)
+    int found = -1;
+    if (prev >= 0) {
+      // the previous row's cutoff as pivot: still the cutoff when exactly k - 1
+      // candidates beat it; a move of a few places is followed key by key (each
+      // step one pass: the smallest key above the bound, or the largest below)
+      const unsigned long long pk = key_of(q, prev);
+      int c = 0;
+      for (int t = s + tid; t < tn; t += kLabelThreads) c += key_of(q, t) > pk;
+      c = block_sum(c);
+      if (c == k - 1) {
+        found = prev;
+      } else if (c - (k - 1) <= kWalk && (k - 1) - c <= kWalk) {
+        const bool up = c > k - 1;
+        unsigned long long bound = pk;
+        for (int step = up ? c - (k - 1) : (k - 1) - c; step > 0; --step) {
+          unsigned long long best = up ? ~0ull : 0ull;
+          for (int t = s + tid; t < tn; t += kLabelThreads) {
+            const unsigned long long kt = key_of(q, t);
+            if (up ? (kt > bound && kt < best) : (kt < bound && kt > best)) best = kt;
+          }
+          bound = block_extreme(best, up);
+        }
+        found = (int)(0xffffffffu - (uint32_t)bound);
+      }
+    }
+    // otherwise a radix select of the k-th largest key among t in [s, tn)
     unsigned long long prefix = 0, mask = 0;
     int need = k;
-    int found = -1;
-    for (int shift = 56; shift >= 0; shift -= 8) {
+    for (int shift = 56; found < 0 && shift >= 0; shift -= 8) {
       for (int i = tid; i < 256; i += kLabelThreads) hist[i] = 0;
       __syncthreads();
       for (int t0 = s; t0 < tn; t0 += kLabelThreads) {  // warp-uniform loop
@@ -147,6 +204,7 @@ __global__ void __launch_bounds__(kLabelThreads)
         break;
       }
     }
+    prev = found;
     if (tid == 0) {
       int yy = -1;
       if (found >= 0) {

@@ -90,6 +90,24 @@ def test_teacher_labels_long_rows_uncached():
     assert (host(y)[0, 0, rows] == yr).all() and (host(tb)[0, 0, rows] == tbr).all()
 
 
+@pytest.mark.parametrize("S", [20000, 40000])   # rows beyond the register path: cached / global targets
+def test_teacher_labels_generic_kernel(S):
+    """Rows with more than 16384 candidates take the generic kernel (radix select,
+    and the previous row's cutoff as pivot within a CTA's 64 rows); whole CTA
+    chunks and scattered rows against the oracle, bit-exact."""
+    rng = np.random.default_rng(S)
+    s, w, k, n = 5, 100, 3000, 8
+    r = _targets(rng, 1, 2, S, "ties")
+    lg = np.log(np.array([0.93, 0.99], np.float32)).astype(np.float32)
+    tb, y = kvpop.teacher_labels(dev(r), s, w, k, n, dev(lg))
+    tb, y = host(tb), host(y)
+    rows = np.concatenate([np.arange(S - 192, S), np.arange(3136, 3200),
+                           np.random.default_rng(1).integers(w + s, S, 40)]).astype(np.int32)
+    for h in range(2):
+        tbr, yr = oracle.teacher_labels_rows(r[0, h], s, w, k, n, float(lg[h]), rows)
+        assert (y[0, h, rows] == yr).all() and (tb[0, h, rows] == tbr).all(), h
+
+
 def test_teacher_labels_full_size_follow_the_mask():
     """4B-like size (b1 H8 S16384, k 1520, w 512) without decay: the labels are the
     mask's decisions (property at any size, checked against the GPU mask, itself
