@@ -891,6 +891,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
           if (!(ok = wait_bar(&bars->q_full[u % NQS], (u / NQS) & 1, 42))) break;
           issue_sdp(u % NQS, 0);
           issue_sdp(u % NQS, 1);
+          // K and V are read by S^T and dP^T only: once the item's last query tile
+          // has both, the next item's K/V may load behind the remaining MMAs
+          if (x.NQ == 1) mma_commit(&bars->kv_empty);
           for (int i = 0; ok && i < x.NQ; ++i, ++u) {
             const int stg = u % NQS;
             const bool more = i + 1 < x.NQ;
@@ -905,11 +908,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
             if (!(ok = wait_bar(&bars->p_full[1], u & 1, 46))) break;
             issue_acc(stg, 1, false);
             mma_commit(&bars->q_empty[stg]);
-            if (more) issue_sdp(stg1, 1);
+            if (more) {
+              issue_sdp(stg1, 1);
+              if (i + 2 == x.NQ) mma_commit(&bars->kv_empty);
+            }
           }
           if (!ok) break;
           mma_commit(&bars->acc_full);
-          mma_commit(&bars->kv_empty);
           ++n;
         }
         mma_commit(&bars->drain);
