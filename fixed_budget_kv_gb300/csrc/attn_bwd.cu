@@ -745,10 +745,11 @@ __device__ __forceinline__ KvItem make_kv_item(const BwdParams& p, int it) {
 //   warps 4-11  elementwise: warpgroup h takes rows 64h .. 64h + 63 of each
 //               query tile, one key per thread (TMEM lane); then the epilogue:
 //               warpgroup 0 writes dv, warpgroup 1 dk
-// TMEM columns: dV at 0, dK at D; half h of a query tile: S^T at 256 + 128 h,
-// dP^T at 256 + 128 h + 64 (P^T and dS^T in bf16 over them).
-// MMA order per query tile u: dV, dK of half 0; S^T, dP^T of half 0 of tile
-// u + 1; dV, dK of half 1; S^T, dP^T of half 1 of tile u + 1.
+// TMEM columns: dV at 0, dK at D, S^T at 256 and dP^T at 384 (N = 128: the whole
+// query tile; N = 64 halves would read the K/V operand twice from shared memory).
+// Warpgroup h owns rows 64 h .. 64 h + 63 (columns 64 h ..) and packs P^T and dS^T
+// over the first 32 of them.  MMA order per query tile u: S^T, dP^T; dV, dK of
+// rows 0-63, then of rows 64-127, as each warpgroup finishes; then tile u + 1.
 template <int D, bool LONG>
 __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
   using L = KvLayout<D>;
@@ -839,7 +840,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
     } else if (warp == 1) {
       // ---------------------------------------------------------- MMA issuer
       if (lane == 0) {
-        constexpr uint32_t idesc_s = idesc_bf16(128, 64, 0);
+        constexpr uint32_t idesc_s = idesc_bf16(128, 128, 0);
         constexpr uint32_t idesc_acc = idesc_bf16(128, D, 1);
         auto wait_bar = [&](uint64_t* bar, uint32_t ph, int detail) -> bool {
           if (!mbar_wait(bar, ph, abort_flag)) {
@@ -850,36 +851,38 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
           return true;
         };
         // S^T_h = K Q_h^T and dP^T_h = V dO_h^T for half h of the tile in stage stg
-        auto issue_sdp = [&](int stg, int h) {
+        // S^T = K Q^T and dP^T = V dO^T over the whole 128-row query tile in stage stg
+        auto issue_sdp = [&](int stg) {
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
             const int dh = ks >> 2;
             const uint32_t w32 = (uint32_t)(ks & 3) * 32;
             const uint64_t a = smem_desc_sw128(k_addr + dh * kBlockBytes + w32, 16, 1024);
-            const uint64_t bd = smem_desc_sw128(q_stage(stg) + dh * kBlockBytes + h * kHalfBytes + w32, 16, 1024);
-            mma_ss(tbase + 256 + 128 * h, a, bd, idesc_s, ks > 0 ? 1u : 0u);
+            const uint64_t bd = smem_desc_sw128(q_stage(stg) + dh * kBlockBytes + w32, 16, 1024);
+            mma_ss(tbase + 256, a, bd, idesc_s, ks > 0 ? 1u : 0u);
           }
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
             const int dh = ks >> 2;
             const uint32_t w32 = (uint32_t)(ks & 3) * 32;
             const uint64_t a = smem_desc_sw128(v_addr + dh * kBlockBytes + w32, 16, 1024);
-            const uint64_t bd = smem_desc_sw128(do_stage(stg) + dh * kBlockBytes + h * kHalfBytes + w32, 16, 1024);
-            mma_ss(tbase + 256 + 128 * h + 64, a, bd, idesc_s, ks > 0 ? 1u : 0u);
+            const uint64_t bd = smem_desc_sw128(do_stage(stg) + dh * kBlockBytes + w32, 16, 1024);
+            mma_ss(tbase + 384, a, bd, idesc_s, ks > 0 ? 1u : 0u);
           }
-          mma_commit(&bars->s_full[h]);
+          mma_commit(&bars->s_full[0]);
         };
-        // dV += P^T_h dO_h and dK += dS^T_h Q_h
+        // dV += P^T dO and dK += dS^T Q over rows 64 h .. 64 h + 63, whose P^T and dS^T
+        // warpgroup h packed over the first 32 of its own 64 columns
         auto issue_acc = [&](int stg, int h, bool first) {
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
             const uint64_t bd = smem_desc_sw128(do_stage(stg) + h * kHalfBytes + ks * 2048, DH > 1 ? kBlockBytes : 16, 1024);
-            mma_ts(tbase, tbase + 256 + 128 * h + ks * 8, bd, idesc_acc, (first && ks == 0) ? 0u : 1u);
+            mma_ts(tbase, tbase + 256 + 64 * h + ks * 8, bd, idesc_acc, (first && ks == 0) ? 0u : 1u);
           }
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
             const uint64_t bd = smem_desc_sw128(q_stage(stg) + h * kHalfBytes + ks * 2048, DH > 1 ? kBlockBytes : 16, 1024);
-            mma_ts(tbase + D, tbase + 256 + 128 * h + 64 + ks * 8, bd, idesc_acc, (first && ks == 0) ? 0u : 1u);
+            mma_ts(tbase + D, tbase + 384 + 64 * h + ks * 8, bd, idesc_acc, (first && ks == 0) ? 0u : 1u);
           }
         };
         bool ok = true;
@@ -889,8 +892,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
           if (x.n == 0) continue;
           if (!(ok = wait_bar(&bars->kv_full, n & 1, 41))) break;
           if (!(ok = wait_bar(&bars->q_full[u % NQS], (u / NQS) & 1, 42))) break;
-          issue_sdp(u % NQS, 0);
-          issue_sdp(u % NQS, 1);
+          issue_sdp(u % NQS);
           // K and V are read by S^T and dP^T only: once the item's last query tile
           // has both, the next item's K/V may load behind the remaining MMAs
           if (x.NQ == 1) mma_commit(&bars->kv_empty);
@@ -901,15 +903,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
             if (!(ok = wait_bar(&bars->p_full[0], u & 1, 43))) break;
             if (i == 0 && !(ok = wait_bar(&bars->acc_empty, (n & 1) ^ 1, 44))) break;
             issue_acc(stg, 0, i == 0);
-            if (more) {
-              if (!(ok = wait_bar(&bars->q_full[stg1], ((u + 1) / NQS) & 1, 45))) break;
-              issue_sdp(stg1, 0);
-            }
             if (!(ok = wait_bar(&bars->p_full[1], u & 1, 46))) break;
             issue_acc(stg, 1, false);
             mma_commit(&bars->q_empty[stg]);
             if (more) {
-              issue_sdp(stg1, 1);
+              // the next tile's S^T and dP^T overwrite the columns these products read:
+              // the tensor core runs them in issue order
+              if (!(ok = wait_bar(&bars->q_full[stg1], ((u + 1) / NQS) & 1, 45))) break;
+              issue_sdp(stg1);
               if (i + 2 == x.NQ) mma_commit(&bars->kv_empty);
             }
           }
@@ -998,18 +999,18 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
       const int hi = LONG ? me.y : min(me.x + w, S);
       for (int i = 0; i < x.NQ; ++i, ++u) {
         const int stg = u % NQS;
-        if (!warp_wait(&bars->s_full[hh], u & 1, abort_flag)) {
+        if (!warp_wait(&bars->s_full[0], u & 1, abort_flag)) {
           if (lane == 0) fail(SITE_ATTN_SOFTMAX, 42);
           ok = false;
           break;
         }
         tc_fence_after();
         uint32_t sr[2][32], dr[2][32];
-        const uint32_t col = 256 + 128 * hh;
-        tmem_ld32(tl + col, sr[0]);
-        tmem_ld32(tl + col + 32, sr[1]);
-        tmem_ld32(tl + col + 64, dr[0]);
-        tmem_ld32(tl + col + 96, dr[1]);
+        const uint32_t scol = 256 + 64 * hh, dcol = 384 + 64 * hh;  // this warpgroup's 64 rows
+        tmem_ld32(tl + scol, sr[0]);
+        tmem_ld32(tl + scol + 32, sr[1]);
+        tmem_ld32(tl + dcol, dr[0]);
+        tmem_ld32(tl + dcol + 32, dr[1]);
         tmem_wait_ld_dep(sr[0]);
         tmem_wait_ld_dep(sr[1]);
         tmem_wait_ld_dep(dr[0]);
@@ -1050,8 +1051,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
               dk[(c + v2) >> 1] = pack_bf16x2(d0, d1);
             }
           }
-          tmem_st16(tl + col + 16 * ch, pk);
-          tmem_st16(tl + col + 64 + 16 * ch, dk);
+          tmem_st16(tl + scol + 16 * ch, pk);  // over this warpgroup's own columns
+          tmem_st16(tl + dcol + 16 * ch, dk);
         }
         tmem_wait_st();
         tc_fence_before();
