@@ -861,6 +861,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
             const uint64_t bd = smem_desc_sw128(q_stage(stg) + dh * kBlockBytes + w32, 16, 1024);
             mma_ss(tbase + 256, a, bd, idesc_s, ks > 0 ? 1u : 0u);
           }
+          mma_commit(&bars->s_full[0]);  // S^T: the elementwise warps start on P
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
             const int dh = ks >> 2;
@@ -869,7 +870,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
             const uint64_t bd = smem_desc_sw128(do_stage(stg) + dh * kBlockBytes + w32, 16, 1024);
             mma_ss(tbase + 384, a, bd, idesc_s, ks > 0 ? 1u : 0u);
           }
-          mma_commit(&bars->s_full[0]);
+          mma_commit(&bars->s_full[1]);  // dP^T
         };
         // dV += P^T dO and dK += dS^T Q over rows 64 h .. 64 h + 63, whose P^T and dS^T
         // warpgroup h packed over the first 32 of its own 64 columns
@@ -1005,16 +1006,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
           break;
         }
         tc_fence_after();
+        // P from S^T first (dP^T may still be in the tensor core), then dS
         uint32_t sr[2][32], dr[2][32];
         const uint32_t scol = 256 + 64 * hh, dcol = 384 + 64 * hh;  // this warpgroup's 64 rows
         tmem_ld32(tl + scol, sr[0]);
         tmem_ld32(tl + scol + 32, sr[1]);
-        tmem_ld32(tl + dcol, dr[0]);
-        tmem_ld32(tl + dcol + 32, dr[1]);
         tmem_wait_ld_dep(sr[0]);
         tmem_wait_ld_dep(sr[1]);
-        tmem_wait_ld_dep(dr[0]);
-        tmem_wait_ld_dep(dr[1]);
         // this half's rows: row 64 hh + c is at position pos_h + (c >> gshift);
         // the key sees the columns [clo, chi)
         const int pos_h = (x.qt0 + i) * P + ((64 * hh) >> gs);
@@ -1032,26 +1030,48 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
         const float4* rdl = rl2 + 32;
 #pragma unroll
         for (int ch = 0; ch < 2; ++ch) {
-          uint32_t pk[16], dk[16];
+          uint32_t pk[16];
 #pragma unroll
           for (int c = 0; c < 32; c += 4) {
             const float4 nl = rl2[(32 * ch + c) >> 2];  // -LSE2 of four rows (a broadcast read)
-            const float4 nd = rdl[(32 * ch + c) >> 2];  // -Delta of the same rows
 #pragma unroll
             for (int v2 = 0; v2 < 4; v2 += 2) {
               const uint64_t n2 = v2 == 0 ? pack2(nl.x, nl.y) : pack2(nl.z, nl.w);
-              const uint64_t d2 = v2 == 0 ? pack2(nd.x, nd.y) : pack2(nd.z, nd.w);
               float e0, e1;
               unpack2(fma2(pack2(__uint_as_float(sr[ch][c + v2]), __uint_as_float(sr[ch][c + v2 + 1])), s2, n2), e0, e1);
               const float p0 = ex2_approx(e0), p1 = ex2_approx(e1);
-              const uint64_t dd = add2(pack2(__uint_as_float(dr[ch][c + v2]), __uint_as_float(dr[ch][c + v2 + 1])), d2);
-              float d0, d1;
-              unpack2(fma2(pack2(p0, p1), dd, zero2), d0, d1);
+              sr[ch][c + v2] = __float_as_uint(p0);  // P in fp32 for dS
+              sr[ch][c + v2 + 1] = __float_as_uint(p1);
               pk[(c + v2) >> 1] = pack_bf16x2(p0, p1);
-              dk[(c + v2) >> 1] = pack_bf16x2(d0, d1);
             }
           }
           tmem_st16(tl + scol + 16 * ch, pk);  // over this warpgroup's own columns
+        }
+        if (!warp_wait(&bars->s_full[1], u & 1, abort_flag)) {
+          if (lane == 0) fail(SITE_ATTN_SOFTMAX, 43);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        tmem_ld32(tl + dcol, dr[0]);
+        tmem_ld32(tl + dcol + 32, dr[1]);
+        tmem_wait_ld_dep(dr[0]);
+        tmem_wait_ld_dep(dr[1]);
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {
+          uint32_t dk[16];
+#pragma unroll
+          for (int c = 0; c < 32; c += 4) {
+            const float4 nd = rdl[(32 * ch + c) >> 2];  // -Delta of four rows
+#pragma unroll
+            for (int v2 = 0; v2 < 4; v2 += 2) {
+              const uint64_t d2 = v2 == 0 ? pack2(nd.x, nd.y) : pack2(nd.z, nd.w);
+              const uint64_t dd = add2(pack2(__uint_as_float(dr[ch][c + v2]), __uint_as_float(dr[ch][c + v2 + 1])), d2);
+              float d0, d1;
+              unpack2(fma2(pack2(__uint_as_float(sr[ch][c + v2]), __uint_as_float(sr[ch][c + v2 + 1])), dd, zero2), d0, d1);
+              dk[(c + v2) >> 1] = pack_bf16x2(d0, d1);
+            }
+          }
           tmem_st16(tl + dcol + 16 * ch, dk);
         }
         tmem_wait_st();
