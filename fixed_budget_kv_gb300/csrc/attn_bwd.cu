@@ -24,7 +24,7 @@
 //              span): S = Q K^T and dP = dO V^T in TMEM, dS in bf16 written
 //              over S, dQ += dS K accumulated in TMEM over the key tiles.
 //   bwd_dkdv   key-major: the 128 keys of an item are the TMEM lanes and the
-//              query rows stream by in 64-row halves: S^T = K Q^T and
+//              query rows stream by in 128-row tiles: S^T = K Q^T and
 //              dP^T = V dO^T, P^T and dS^T in bf16 written over them,
 //              dV += P^T dO and dK += dS^T Q.  Launched twice: band items (128
 //              consecutive keys against rows t <= q < t + w) store dk and dv;
@@ -748,8 +748,9 @@ __device__ __forceinline__ KvItem make_kv_item(const BwdParams& p, int it) {
 // TMEM columns: dV at 0, dK at D, S^T at 256 and dP^T at 384 (N = 128: the whole
 // query tile; N = 64 halves would read the K/V operand twice from shared memory).
 // Warpgroup h owns rows 64 h .. 64 h + 63 (columns 64 h ..) and packs P^T and dS^T
-// over the first 32 of them.  MMA order per query tile u: S^T, dP^T; dV, dK of
-// rows 0-63, then of rows 64-127, as each warpgroup finishes; then tile u + 1.
+// over the first 32 of them.  MMA order per query tile u: S^T (its own commit: the
+// warpgroups compute P meanwhile), dP^T; dV, dK of rows 0-63, then of rows 64-127,
+// as each warpgroup finishes; then tile u + 1.
 template <int D, bool LONG>
 __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
   using L = KvLayout<D>;
@@ -850,8 +851,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
           tc_fence_after();
           return true;
         };
-        // S^T_h = K Q_h^T and dP^T_h = V dO_h^T for half h of the tile in stage stg
-        // S^T = K Q^T and dP^T = V dO^T over the whole 128-row query tile in stage stg
+        // S^T = K Q^T and dP^T = V dO^T over the whole 128-row query tile in stage stg,
+        // committed separately so that P can be computed while dP^T runs
         auto issue_sdp = [&](int stg) {
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
