@@ -36,7 +36,7 @@ LAUNCHES_DECODE_STEP = 2
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum, one ncu
 # capture of `bench.py --only <pass>` on a GB300) for the kernels as they stand;
 # decode: update + attention of one step
-TRAFFIC_BYTES = {"sparse_attn": 309.91e6, "dense_lse": 173.46e6, "future_target": 170.12e6, "decode": 558.19e6}
+TRAFFIC_BYTES = {"sparse_attn": 310.24e6, "dense_lse": 172.50e6, "future_target": 169.39e6, "decode": 558.19e6}
 
 
 def max_over_ranks(x: float, world: int, device) -> float:
