@@ -11,7 +11,9 @@ to 2^-9, about 1.1e-3 RMS for round-to-nearest) before the products whose
 fp32 sums give dv, dq and dk; each output is a random-sign sum of such terms,
 so its error is about that relative RMS of the sum's own scale, and the bound
 leaves a factor of about ten for the largest of many elements.  dO . O with
-the bf16 forward output stands in for sum_t P dP, an error of the same order."""
+the bf16 forward output stands in for sum_t P dP, an error of the same order.
+A gradient that vanishes exactly (a row with one retained key has P = 1 and
+dS = 0) leaves only that fp32 rounding, so 1e-5 is allowed on top."""
 import math
 
 import numpy as np
@@ -25,6 +27,7 @@ from gpu_util import dev, dev_bf16, host
 pytestmark = pytest.mark.gpu
 
 TOL_GRAD = 1e-2
+ATOL_GRAD = 1e-5
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -51,8 +54,8 @@ def check(got, ref, what):
     scale = float(np.abs(ref).max())
     err = float(np.abs(got - ref).max())
     assert np.isfinite(got).all(), f"{what}: non-finite values"
-    assert err <= TOL_GRAD * scale, f"{what}: max abs error {err:.3e} > {TOL_GRAD:.0e} * {scale:.3e}"
-    return err / scale
+    assert err <= TOL_GRAD * scale + ATOL_GRAD, f"{what}: max abs error {err:.3e} > {TOL_GRAD:.0e} * {scale:.3e}"
+    return err / max(scale, ATOL_GRAD)
 
 
 CASES = [
@@ -68,6 +71,10 @@ CASES = [
     (1, 1, 16, 128, 350, 3, 24, 40),      # G = 16: 8 positions per query tile
     (2, 3, 2, 128, 520, 5, 40, 70),       # G = 2, three KV heads, two sequences
     (1, 1, 4, 128, 2100, 600, 300, 400),  # more sinks than a key tile, blocks of sinks only
+    (1, 1, 2, 64, 1, 1, 1, 1),            # one token
+    (1, 2, 4, 64, 20, 2, 3, 4),           # shorter than one query tile
+    (1, 1, 4, 128, 300, 0, 400, 8),       # the window covers the sequence: band pairs only
+    (1, 1, 128, 64, 40, 2, 5, 6),         # G = 128: one position per query tile
 ]
 
 
