@@ -150,10 +150,11 @@ kvpop_status kvpop_attn_fwd(const void* q, const void* k, const void* v, int b, 
  *   dq         [b, S, Hq, D] fp32; dk, dv [b, S, H, D] fp32; all overwritten
  * workspace: kvpop_attn_bwd_workspace_size() bytes, 256-byte aligned (row
  * constants and per-block key lists; contents undefined between calls).
- * D 64 or 128, G dividing 128, tensors 16-byte aligned.  bf16 operands (P and
- * dS rounded to bf16 before their products), fp32 accumulation; dk and dv
- * take fp32 atomic additions, so their last bits vary from run to run.
- * Errors: INVALID_ARG, UNSUPPORTED, CUDA.
+ * D 64 or 128, G dividing 128, tensors 16-byte aligned, b and H <= 65535,
+ * S <= 2^24.  bf16 operands (P and dS rounded to bf16 before their products),
+ * fp32 accumulation; dk and dv take fp32 atomic additions, so their last bits
+ * vary from run to run.  Errors: INVALID_ARG (NULL pointer, bad shape or budget,
+ * workspace too small), UNSUPPORTED (D, G, alignment, sizes), CUDA.
  * ---------------------------------------------------------------------- */
 kvpop_status kvpop_attn_bwd_workspace_size(int b, int S, int Hq, int H, kvpop_budget budget, size_t* bytes);
 kvpop_status kvpop_attn_bwd(const void* q, const void* k, const void* v, const void* O, const void* dO,
