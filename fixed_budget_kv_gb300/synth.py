@@ -93,6 +93,19 @@ def normal(seed: int, stream: int, n: int, start: int = 0) -> np.ndarray:
     return _chunked(n, fill)
 
 
+def normal_at(seed: int, stream: int, idx: np.ndarray) -> np.ndarray:
+    """Normal draws number ``idx`` (any integer array) of a stream, fp32: the same
+    values as ``normal`` at those positions, without drawing the rest."""
+    idx = np.asarray(idx, dtype=np.uint64)
+    key = stream_key(seed, stream)
+    with np.errstate(over="ignore"):
+        z0 = _mix64(key + (np.uint64(2) * idx + np.uint64(1)) * _GOLDEN)
+        z1 = _mix64(key + (np.uint64(2) * idx + np.uint64(2)) * _GOLDEN)
+    u1 = ((z0 >> np.uint64(11)).astype(np.float64) + 1.0) * 2.0 ** -53
+    u2 = (z1 >> np.uint64(11)).astype(np.float64) * 2.0 ** -53
+    return (np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * np.pi * u2)).astype(np.float32)
+
+
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """Round-to-nearest-even fp32 -> bf16, returned as uint16 bit patterns."""
     b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)

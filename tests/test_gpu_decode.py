@@ -110,6 +110,7 @@ def test_decode_prefix_shorter_than_budget():
 
 def test_decode_full_workload_sampled():
     """The decode workload's shape (64 sequences, B = 2048, 8192-token prefix):
-    slot sets of every sequence, floats of sequences 0-3, for a few steps."""
+    slot sets and evicted positions of all 64 sequences at each of 64 steps (every
+    step evicts: the prefix is longer than the budget), floats of sequences 0-3."""
     wl = synth.DECODE
-    run_decode(wl, 6, check_seqs=range(wl.n), float_seqs=range(4), check_every=1)
+    run_decode(wl, 64, check_seqs=range(wl.n), float_seqs=range(4), check_every=1)
