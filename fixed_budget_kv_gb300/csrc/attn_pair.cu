@@ -34,6 +34,7 @@ constexpr int kQBytes = 128 * 128;    // one 64-dim half of a 128-row query tile
 constexpr int kKHalf = 64 * 128;      // 64 key rows x 64 dims
 constexpr int kVBytes = 128 * 128;    // 128 key rows x 64 dims
 constexpr float kRescaleLog2 = 8.0f;
+constexpr float kRescaleMax = 256.0f;  // 2^kRescaleLog2
 constexpr int kRegsIo = 64;
 constexpr int kRegsSoftmax = 216;
 constexpr int kRegsNeeded = (128 * kRegsIo + 256 * kRegsSoftmax + kThreads - 1) / kThreads;
@@ -435,7 +436,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int ch = 0; ch < 4; ++ch) tmem_ld32(tl + s_col + ch * 32, sr[ch]);
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) tmem_wait_ld_dep(sr[ch]);
-        float mt = neg_inf();
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
           const int2 sum = km[kKeys + ch];
@@ -446,53 +446,70 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               if (!(e.x <= q && q < e.y)) sr[ch][c] = 0xff800000u;
             }
           }
-          mt = fmaxf(mt, max32(sr[ch]));
         }
-        // lazy rescale of the running max
-        const float m_new = fmaxf(m_ref, mt);
-        const bool need = (m_new - m_ref) * sl2 > kRescaleLog2;  // true when m_ref == -inf and mt finite
-        float alpha = 1.0f;
-        if (need) {
-          alpha = ex2_approx((m_ref - m_new) * sl2);
-          l *= alpha;
-          m_ref = m_new;
-        }
-        if (__any_sync(0xffffffffu, need) && j > 0) {
-          // O of tile j-1 is complete: s_full for tile j was committed after it
+        // P = exp2(s * scale_log2 - m) as bf16, written over S; returns the row's sum
+        auto exps = [&](float nm) -> float {
+          const uint64_t n2 = pack2(nm, nm);
+          uint64_t lacc[4] = {0, 0, 0, 0};
 #pragma unroll
-          for (int cd = 0; cd < 4; ++cd) {
-            uint32_t r[32];
-            tmem_ld32(tl + o_col + cd * 32, r);
-            tmem_wait_ld_dep(r);
+          for (int ch = 0; ch < 4; ++ch) {
+            uint32_t pk[16];
 #pragma unroll
-            for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * alpha);
-            tmem_st32(tl + o_col + cd * 32, r);
+            for (int c = 0; c < 32; c += 2) {
+              const uint64_t xx =
+                  fma2(pack2(__uint_as_float(sr[ch][c]), __uint_as_float(sr[ch][c + 1])), s2, n2);
+              float e0, e1;
+              unpack2(xx, e0, e1);
+              const float p0 = ex2_approx(e0), p1 = ex2_approx(e1);
+              lacc[(c >> 1) & 3] = add2(lacc[(c >> 1) & 3], pack2(p0, p1));
+              pk[c >> 1] = pack_bf16x2(p0, p1);
+            }
+            tmem_st16(tl + s_col + ch * 16, pk);
           }
-          tmem_wait_st();
-        }
-        // P = exp2(s * scale_log2 - m) as bf16, written over S
-        const float nm = (m_ref == neg_inf()) ? 0.0f : -m_ref * sl2;
-        const uint64_t n2 = pack2(nm, nm);
-        uint64_t lacc = 0;
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            const uint64_t xx = fma2(pack2(__uint_as_float(sr[ch][c]), __uint_as_float(sr[ch][c + 1])), s2, n2);
-            float e0, e1;
-            unpack2(xx, e0, e1);
-            const float p0 = ex2_approx(e0), p1 = ex2_approx(e1);
-            lacc = add2(lacc, pack2(p0, p1));
-            pk[c >> 1] = pack_bf16x2(p0, p1);
-          }
-          tmem_st16(tl + s_col + ch * 16, pk);
-        }
-        {
           float l0, l1;
-          unpack2(lacc, l0, l1);
-          l += l0 + l1;
+          unpack2(add2(add2(lacc[0], lacc[1]), add2(lacc[2], lacc[3])), l0, l1);
+          return l0 + l1;
+        };
+        // The running reference m_ref moves only when a row's maximum exceeds it by
+        // more than 2^kRescaleLog2 in probability.  Once every row of the warp has a
+        // reference, the exponentials are taken against it straight away: if no
+        // row's sum exceeds 2^kRescaleLog2, no single term can, and the maximum is
+        // never formed.  Otherwise (and on an item's first tile) the exact path runs.
+        float ts = 0.0f;
+        bool fast = false;
+        if (j > 0 && __all_sync(0xffffffffu, m_ref != neg_inf())) {
+          ts = exps(-m_ref * sl2);
+          fast = __all_sync(0xffffffffu, ts <= kRescaleMax);
         }
+        if (!fast) {
+          tmem_wait_st();
+          float mt = neg_inf();
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) mt = fmaxf(mt, max32(sr[ch]));
+          const float m_new = fmaxf(m_ref, mt);
+          const bool need = (m_new - m_ref) * sl2 > kRescaleLog2;  // true when m_ref == -inf and mt finite
+          float alpha = 1.0f;
+          if (need) {
+            alpha = ex2_approx((m_ref - m_new) * sl2);
+            l *= alpha;
+            m_ref = m_new;
+          }
+          if (__any_sync(0xffffffffu, need) && j > 0) {
+            // O of tile j-1 is complete: s_full for tile j was committed after it
+#pragma unroll
+            for (int cd = 0; cd < 4; ++cd) {
+              uint32_t r[32];
+              tmem_ld32(tl + o_col + cd * 32, r);
+              tmem_wait_ld_dep(r);
+#pragma unroll
+              for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * alpha);
+              tmem_st32(tl + o_col + cd * 32, r);
+            }
+            tmem_wait_st();
+          }
+          ts = exps((m_ref == neg_inf()) ? 0.0f : -m_ref * sl2);
+        }
+        l += ts;
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();

@@ -305,6 +305,25 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       : "memory");
 }
 
+// 8 consecutive 32-bit TMEM columns of this thread's lane, and the matching store.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                 "=r"(r[7])
+               : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+               "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld_dep8(uint32_t (&r)[8]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7])
+               :
+               : "memory");
+}
+
 // Warp-uniform bounded wait: every lane waits (acquire), the warp agrees on the result.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
   bool ok = mbar_wait(bar, parity, abort_flag);
@@ -385,12 +404,16 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   return d;
 }
 
-// Maximum of 32 fp32 values held as raw bits.
+// Maximum of 32 fp32 values held as raw bits: a tree of three-input maxima
+// (four dependent steps instead of sixteen).
 __device__ __forceinline__ float max32(const uint32_t (&r)[32]) {
-  float m = __uint_as_float(r[0]);
+  float a[11];
 #pragma unroll
-  for (int c = 1; c < 31; c += 2) m = max3(m, __uint_as_float(r[c]), __uint_as_float(r[c + 1]));
-  return fmaxf(m, __uint_as_float(r[31]));
+  for (int i = 0; i < 10; ++i)
+    a[i] = max3(__uint_as_float(r[3 * i]), __uint_as_float(r[3 * i + 1]), __uint_as_float(r[3 * i + 2]));
+  a[10] = fmaxf(__uint_as_float(r[30]), __uint_as_float(r[31]));
+  const float b0 = max3(a[0], a[1], a[2]), b1 = max3(a[3], a[4], a[5]), b2 = max3(a[6], a[7], a[8]);
+  return max3(max3(b0, b1, b2), a[9], a[10]);
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {
