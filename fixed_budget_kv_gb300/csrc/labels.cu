@@ -32,6 +32,9 @@ constexpr int kLabelThreads = 512;
 constexpr int kLabelRowsPerCta = 64;
 constexpr int kCacheFloats = 32768;  // targets kept in shared memory when S fits (128 KB)
 constexpr int kWalk = 16;            // largest cutoff move followed key by key
+constexpr int kWindow = 512;         // keys kept around the pivot by the long-row kernel
+constexpr int kLongRowsPerCta = 64;   // rows per CTA of the long-row kernel
+constexpr int kBand = 2048;           // candidates kept in the long-row kernel's score band
 
 __device__ __forceinline__ float decayed_score(float r, int q, int t, int n, float lg) {
   const float m = (float)((q - t) / n);
@@ -48,29 +51,71 @@ __device__ __forceinline__ unsigned long long label_key(float sc, int t) {
   return ((unsigned long long)u << 32) | (0xffffffffu - (uint32_t)t);
 }
 
+// floor(d / n) for 0 <= d < 2^24 through the fp32 reciprocal, corrected by one step
+__device__ __forceinline__ int div_floor(int d, int n, float inv_n) {
+  int m = __float2int_rz(__fmul_rn((float)d, inv_n));
+  if (m * n > d) --m;
+  else if ((m + 1) * n <= d) ++m;
+  return m;
+}
+
+__device__ __forceinline__ float decayed_score_m(float r, int m, float lg) {
+  float sc = __fadd_rn(r, __fmul_rn((float)m, lg));
+  if (sc != sc) sc = __int_as_float(0xff800000);
+  return sc == 0.0f ? 0.0f : sc;  // -0 == +0
+}
+
+// Rows with more candidates than the register-resident kernel holds.
+//
+// Band: from row to row only two things change -- the candidate that joins
+// (the previous row's leaving token) and the candidates whose decay step
+// floor((q - t) / n) grows at this row (t = q mod n, one in n); every other
+// score is bit for bit what it was.  So the CTA keeps a band of scores
+// [lo, hi] around the cutoff: the number of candidates above hi, and the list
+// of those inside (index and target, in shared memory).  A row updates the
+// count and the list from the joining and the decaying candidates only
+// (scores only fall, so a listed candidate never rises above hi; one that
+// falls below lo stays listed and is skipped), then selects the cutoff among
+// the listed candidates -- the previous cutoff tried first, a radix select
+// over the list otherwise.  When the cutoff leaves the band, or the list
+// overflows, the row takes the full path below and the band is rebuilt
+// around the new cutoff in one more pass.
+//
+// Full path: one pass over all candidates against the previous row's cutoff as
+// pivot counts the keys above it and gathers, in shared memory, the keys whose
+// score lies within +-delta of the pivot's.  When the cutoff moved by d places,
+// the new one is the d-th nearest key above (or below) the pivot; if the window
+// holds at least d of them it is found there.  delta adapts so the window holds
+// a few dozen to a few hundred keys; a row whose window was too narrow, or
+// overflowed, falls back to a radix select.
+template <bool kFastDiv>
 __global__ void __launch_bounds__(kLabelThreads)
-    teacher_labels_kernel(const float* __restrict__ r_tgt, int H, int S, int s, int w, int k, int n,
+    teacher_labels_kernel(const float* __restrict__ r_tgt, int H, int S, int s, int w, int k, int n, float inv_n,
                           const float* __restrict__ log_gamma, int32_t* __restrict__ t_bnd,
                           int32_t* __restrict__ y, int cache, int* status) {
   extern __shared__ float rs[];  // the row of targets, when it fits
   __shared__ uint32_t hist[256];
   __shared__ unsigned long long s_prefix;
-  __shared__ int s_need, s_left, s_found;
+  __shared__ int s_need, s_left, s_found, s_wcount;
   __shared__ int red[kLabelThreads / 32];
-  __shared__ unsigned long long red64[kLabelThreads / 32];
+  __shared__ unsigned long long wbuf[kWindow];
+  __shared__ int band_t[kBand];
+  __shared__ float band_r[kBand];
+  __shared__ int s_bn;
   const int bh = blockIdx.y;
   const int h = bh % H;
   const float* r = r_tgt + (size_t)bh * S;
   const float lg = log_gamma[h];
-  const int q0 = blockIdx.x * kLabelRowsPerCta;
-  const int q1 = min(S, q0 + kLabelRowsPerCta);
+  const int q0 = blockIdx.x * kLongRowsPerCta;
+  const int q1 = min(S, q0 + kLongRowsPerCta);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int tmax = max(0, q1 - 1 - w);  // candidates of this CTA's rows are t < tmax
   if (cache)
     for (int t = tid; t < tmax; t += kLabelThreads) rs[t] = r[t];
   __syncthreads();
-  auto key_of = [&](int q, int t) -> unsigned long long {
-    return label_key(decayed_score(cache ? rs[t] : __ldg(r + t), q, t, n, lg), t);
+  auto score_of = [&](int q, int t) -> float {
+    const float rt = cache ? rs[t] : __ldg(r + t);
+    return kFastDiv ? decayed_score_m(rt, div_floor(q - t, n, inv_n), lg) : decayed_score(rt, q, t, n, lg);
   };
   auto block_sum = [&](int v) -> int {
     v = __reduce_add_sync(0xffffffffu, v);
@@ -82,28 +127,168 @@ __global__ void __launch_bounds__(kLabelThreads)
     __syncthreads();
     return tot;
   };
-  auto block_extreme = [&](unsigned long long v, bool up) -> unsigned long long {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const unsigned long long u = __shfl_xor_sync(0xffffffffu, v, o);
-      v = up ? (u < v ? u : v) : (u > v ? u : v);
+  float delta = 1.0f / 64.0f;  // half-width of the window, in score units
+  int prev = -1;               // the previous row's cutoff
+  // band state (uniform over the CTA)
+  bool band_ok = false;
+  float b_lo = 0.0f, b_hi = 0.0f, bdelta = 1.0f / 32.0f;
+  int ahi = 0;       // candidates scored above b_hi
+  int band_age = 0;  // rows served by the current band
+  auto cat = [&](float sc) -> int { return sc > b_hi ? 2 : (sc >= b_lo ? 1 : 0); };  // NaN -> 0
+  auto append = [&](int t, float rt) {
+    const int slot = atomicAdd(&s_bn, 1);
+    if (slot < kBand) {
+      band_t[slot] = t;
+      band_r[slot] = rt;
     }
-    if (lane == 0) red64[warp] = v;
-    __syncthreads();
-    unsigned long long m = red64[0];
-#pragma unroll
-    for (int i = 1; i < kLabelThreads / 32; ++i) {
-      const unsigned long long u = red64[i];
-      m = up ? (u < m ? u : m) : (u > m ? u : m);
-    }
-    __syncthreads();
-    return m;
   };
-  int prev = -1;  // the previous row's cutoff
+  auto band_score = [&](int q, int i) -> float {
+    const int t = band_t[i];
+    return decayed_score_m(band_r[i], kFastDiv ? div_floor(q - t, n, inv_n) : (q - t) / n, lg);
+  };
+  // the row's cutoff from the band, or -1 when it left the band (band_ok falls)
+  auto band_row = [&](int q, int tn) -> int {
+    // candidates whose decay step grows at this row: t = q (mod n), already candidates at q - 1
+    int dA = 0;
+    for (int t = s + (q - s) % n + n * tid; t < tn - 1; t += n * kLabelThreads) {
+      const float rt = cache ? rs[t] : __ldg(r + t);
+      const int mq = kFastDiv ? div_floor(q - t, n, inv_n) : (q - t) / n;
+      const int oc = cat(decayed_score_m(rt, mq - 1, lg)), nc = cat(decayed_score_m(rt, mq, lg));
+      if (oc == 2 && nc != 2) {
+        --dA;
+        if (nc == 1) append(t, rt);
+      }
+    }
+    if (tid == 0) {  // the candidate that joins: the previous row's leaving token
+      const int t = tn - 1;
+      const float rt = cache ? rs[t] : __ldg(r + t);
+      const int c = cat(decayed_score_m(rt, kFastDiv ? div_floor(q - t, n, inv_n) : (q - t) / n, lg));
+      if (c == 2) ++dA;
+      if (c == 1) append(t, rt);
+    }
+    ahi += block_sum(dA);  // its barriers also publish the list
+    const int bn = s_bn;
+    const int need = k - ahi;  // the cutoff is the need-th best listed candidate
+    if (bn > kBand || need < 1) return -1;
+    // listed candidates still in the band, and those above the previous cutoff
+    const float sp = prev >= 0 ? score_of(q, prev) : 0.0f;
+    const bool piv = prev >= 0 && sp >= b_lo;  // (then it is listed: it was the cutoff)
+    const unsigned long long pk = piv ? label_key(sp, prev) : 0ull;
+    int alive = 0, above = 0;
+    for (int i = tid; i < bn; i += kLabelThreads) {
+      const float sc = band_score(q, i);
+      if (sc >= b_lo) {
+        ++alive;
+        above += piv && label_key(sc, band_t[i]) > pk;
+      }
+    }
+    alive = block_sum(alive);
+    above = block_sum(above);
+    if (alive < need) return -1;
+    if (piv && above == need - 1) return prev;
+    // radix select of the need-th largest key among the listed candidates in the band
+    unsigned long long prefix = 0, mask = 0;
+    int nd = need;
+    for (int shift = 56; shift >= 0; shift -= 8) {
+      for (int i = tid; i < 256; i += kLabelThreads) hist[i] = 0;
+      __syncthreads();
+      for (int i0 = 0; i0 < bn; i0 += kLabelThreads) {  // warp-uniform loop
+        const int i = i0 + tid;
+        bool match = false;
+        unsigned long long key = 0;
+        if (i < bn) {
+          const float sc = band_score(q, i);
+          key = label_key(sc, band_t[i]);
+          match = sc >= b_lo && (key & mask) == prefix;
+        }
+        const uint32_t active = __ballot_sync(0xffffffffu, match);
+        if (match) {
+          const uint32_t bin = (uint32_t)(key >> shift) & 255u;
+          const uint32_t peers = __match_any_sync(active, bin);
+          if ((__ffs(peers) - 1) == lane) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
+        }
+      }
+      __syncthreads();
+      if (warp == 0) {
+        uint32_t cnt[8], tot = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          cnt[j] = hist[255 - 8 * lane - j];
+          tot += cnt[j];
+        }
+        uint32_t incl = tot;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += v;
+        }
+        const uint32_t excl = incl - tot;
+        if (excl < (uint32_t)nd && (uint32_t)nd <= incl) {
+          uint32_t run = excl;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (run + cnt[j] >= (uint32_t)nd) {
+              s_prefix = prefix | ((unsigned long long)(255 - 8 * lane - j) << shift);
+              s_need = nd - (int)run;
+              s_left = (int)cnt[j];
+              break;
+            }
+            run += cnt[j];
+          }
+        }
+      }
+      __syncthreads();
+      prefix = s_prefix;
+      mask |= 255ull << shift;
+      nd = s_need;
+      const int left = s_left;
+      __syncthreads();
+      if (left == 1 || shift == 0) break;
+    }
+    // the one listed candidate that carries the prefix (keys are distinct)
+    if (tid == 0) s_found = -1;
+    __syncthreads();
+    for (int i = tid; i < bn; i += kLabelThreads) {
+      const float sc = band_score(q, i);
+      if (sc >= b_lo && (label_key(sc, band_t[i]) & mask) == prefix) atomicMax(&s_found, band_t[i]);
+    }
+    __syncthreads();
+    const int res = s_found;
+    __syncthreads();
+    return res;
+  };
+  // a band of scores around the cutoff `cut` of row q, from one pass over T(q)
+  auto build_band = [&](int q, int tn, int cut) {
+    const float sc0 = score_of(q, cut);
+    band_ok = false;
+    // scores never rise only while the decay factor is at most 1 (log gamma <= 0)
+    if (!(lg <= 0.0f) || !(sc0 > __int_as_float(0xff800000) && sc0 < __int_as_float(0x7f800000))) return;
+    b_lo = sc0 - bdelta;
+    b_hi = sc0 + bdelta;
+    if (tid == 0) s_bn = 0;
+    __syncthreads();
+    int a = 0;
+    for (int t = s + tid; t < tn; t += kLabelThreads) {
+      const float rt = cache ? rs[t] : __ldg(r + t);
+      const int c = cat(decayed_score_m(rt, kFastDiv ? div_floor(q - t, n, inv_n) : (q - t) / n, lg));
+      a += c == 2;
+      if (c == 1) append(t, rt);
+    }
+    ahi = block_sum(a);
+    const int bn = s_bn;
+    if (bn > kBand) {
+      bdelta *= 0.5f;
+      return;
+    }
+    if (bn > kBand / 2) bdelta *= 0.75f;
+    band_ok = true;
+    band_age = 0;
+  };
   for (int q = q0; q < q1; ++q) {
     const int tn = q - w;
     const size_t out = (size_t)bh * S + q;
     if (tn < s || k == 0 || tn - s < k) {  // uniform over the CTA
+      band_ok = false;
       if (tid == 0) {
         t_bnd[out] = -1;
         y[out] = tn < s ? 0 : (k == 0 ? -1 : 1);
@@ -111,29 +296,99 @@ __global__ void __launch_bounds__(kLabelThreads)
       continue;
     }
     int found = -1;
-    if (prev >= 0) {
-      // the previous row's cutoff as pivot: still the cutoff when exactly k - 1
-      // candidates beat it; a move of a few places is followed key by key (each
-      // step one pass: the smallest key above the bound, or the largest below)
-      const unsigned long long pk = key_of(q, prev);
-      int c = 0;
-      for (int t = s + tid; t < tn; t += kLabelThreads) c += key_of(q, t) > pk;
-      c = block_sum(c);
-      if (c == k - 1) {
-        found = prev;
-      } else if (c - (k - 1) <= kWalk && (k - 1) - c <= kWalk) {
-        const bool up = c > k - 1;
-        unsigned long long bound = pk;
-        for (int step = up ? c - (k - 1) : (k - 1) - c; step > 0; --step) {
-          unsigned long long best = up ? ~0ull : 0ull;
-          for (int t = s + tid; t < tn; t += kLabelThreads) {
-            const unsigned long long kt = key_of(q, t);
-            if (up ? (kt > bound && kt < best) : (kt < bound && kt > best)) best = kt;
-          }
-          bound = block_extreme(best, up);
-        }
-        found = (int)(0xffffffffu - (uint32_t)bound);
+    if (band_ok) {
+      found = band_row(q, tn);
+      if (found >= 0) {
+        ++band_age;
+      } else {
+        band_ok = false;
+        if (band_age < 16) bdelta *= 2.0f;  // the cutoff left the band quickly: widen it
       }
+    }
+    const bool rebuild = found < 0;
+    const float sp = (found < 0 && prev >= 0) ? score_of(q, prev) : 0.0f;
+    // (a pivot scored -inf ties with NaN candidates, which the plain comparisons
+    // below do not see: such rows take the radix select)
+    if (found < 0 && prev >= 0 && sp != __int_as_float(0xff800000)) {
+      const unsigned long long pk = label_key(sp, prev);
+      const float lo = sp - delta, hi = sp + delta;
+      if (tid == 0) {
+        s_wcount = 0;
+        s_found = -1;
+      }
+      __syncthreads();
+      int c = 0;
+      // this thread's candidates t = s + tid + 512 i: q - t falls by 512 per step,
+      // so floor((q - t) / n) follows by a subtraction and one carry
+      int t = s + tid;
+      int m = 0, rem = 0;
+      if (t < tn) {
+        m = kFastDiv ? div_floor(q - t, n, inv_n) : (q - t) / n;
+        rem = q - t - m * n;
+      }
+      const int step_m = kLabelThreads / n, step_r = kLabelThreads % n;
+      // the decayed score exactly as defined (one rounding after the product and
+      // one after the sum); plain comparisons already treat -0 as +0 and put NaN
+      // below a finite pivot, as the key order does
+      auto visit = [&](int tt, float rt, int mm) {
+        const float sc = __fadd_rn(rt, __fmul_rn((float)mm, lg));
+        c += (sc > sp) || (sc == sp && tt < prev);
+        if (sc >= lo && sc <= hi && tt != prev) {
+          const int slot = atomicAdd(&s_wcount, 1);
+          if (slot < kWindow) wbuf[slot] = label_key(sc == 0.0f ? 0.0f : sc, tt);
+        }
+      };
+      auto advance = [&]() {
+        rem -= step_r;
+        m -= step_m;
+        if (rem < 0) {
+          rem += n;
+          --m;
+        }
+      };
+      // four candidates per round, their loads issued together
+      for (; t + 3 * kLabelThreads < tn; t += 4 * kLabelThreads) {
+        float rv[4];
+#pragma unroll
+        for (int u4 = 0; u4 < 4; ++u4) rv[u4] = cache ? rs[t + u4 * kLabelThreads] : __ldg(r + t + u4 * kLabelThreads);
+#pragma unroll
+        for (int u4 = 0; u4 < 4; ++u4) {
+          visit(t + u4 * kLabelThreads, rv[u4], m);
+          advance();
+        }
+      }
+      for (; t < tn; t += kLabelThreads) {
+        visit(t, cache ? rs[t] : __ldg(r + t), m);
+        advance();
+      }
+      c = block_sum(c);  // its barriers also publish the window
+      const int wc = s_wcount;
+      const int dm = c - (k - 1);  // places the cutoff moved: > 0 up, < 0 down
+      if (dm == 0) {
+        found = prev;
+      } else if (wc <= kWindow) {
+        const bool up = dm > 0;
+        const int want = up ? dm - 1 : -dm - 1;  // keys strictly between the pivot and the new cutoff
+        for (int i = tid; i < wc; i += kLabelThreads) {
+          const unsigned long long e = wbuf[i];
+          if (up ? e > pk : e < pk) {
+            int rank = 0;
+            for (int j = 0; j < wc && rank <= want; ++j) {
+              const unsigned long long f = wbuf[j];
+              rank += up ? (f > pk && f < e) : (f < pk && f > e);
+            }
+            if (rank == want) s_found = (int)(0xffffffffu - (uint32_t)e);
+          }
+        }
+        __syncthreads();
+        found = s_found;
+      }
+      // keep the window at a few dozen keys (uniform decisions)
+      if (wc > kWindow) delta *= 0.25f;
+      else if (found < 0) delta *= 4.0f;
+      else if (wc > kWindow / 4) delta *= 0.75f;
+      else if (wc < kWindow / 32) delta *= 1.5f;
+      __syncthreads();
     }
     // otherwise a radix select of the k-th largest key among t in [s, tn)
     unsigned long long prefix = 0, mask = 0;
@@ -145,7 +400,7 @@ __global__ void __launch_bounds__(kLabelThreads)
         const int t = t0 + tid;
         const bool valid = t < tn;
         unsigned long long key = 0;
-        if (valid) key = label_key(decayed_score(cache ? rs[t] : __ldg(r + t), q, t, n, lg), t);
+        if (valid) key = label_key(score_of(q, t), t);
         const bool match = valid && (key & mask) == prefix;
         const uint32_t active = __ballot_sync(0xffffffffu, match);
         if (match) {
@@ -157,11 +412,11 @@ __global__ void __launch_bounds__(kLabelThreads)
       __syncthreads();
       if (warp == 0) {
         // bins from the top: lane l owns bins 255 - 8l .. 248 - 8l
-        uint32_t c[8], tot = 0;
+        uint32_t cnt[8], tot = 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          c[i] = hist[255 - 8 * lane - i];
-          tot += c[i];
+          cnt[i] = hist[255 - 8 * lane - i];
+          tot += cnt[i];
         }
         uint32_t incl = tot;  // inclusive scan over lanes (higher bins first)
 #pragma unroll
@@ -174,13 +429,13 @@ __global__ void __launch_bounds__(kLabelThreads)
           uint32_t run = excl;
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            if (run + c[i] >= (uint32_t)need) {
+            if (run + cnt[i] >= (uint32_t)need) {
               s_prefix = prefix | ((unsigned long long)(255 - 8 * lane - i) << shift);
               s_need = need - (int)run;
-              s_left = (int)c[i];
+              s_left = (int)cnt[i];
               break;
             }
-            run += c[i];
+            run += cnt[i];
           }
         }
       }
@@ -195,7 +450,7 @@ __global__ void __launch_bounds__(kLabelThreads)
         if (tid == 0) s_found = -1;
         __syncthreads();
         for (int t = s + tid; t < tn; t += kLabelThreads) {
-          const unsigned long long key = label_key(decayed_score(cache ? rs[t] : __ldg(r + t), q, t, n, lg), t);
+          const unsigned long long key = label_key(score_of(q, t), t);
           if ((key & mask) == prefix) atomicMax(&s_found, t);
         }
         __syncthreads();
@@ -204,11 +459,12 @@ __global__ void __launch_bounds__(kLabelThreads)
         break;
       }
     }
+    if (rebuild && found >= 0) build_band(q, tn, found);
     prev = found;
     if (tid == 0) {
       int yy = -1;
       if (found >= 0) {
-        const float sb = decayed_score(cache ? rs[found] : __ldg(r + found), q, found, n, lg);
+        const float sb = score_of(q, found);
         const float sn = decayed_score(__ldg(r + tn), q, tn, n, lg);
         yy = sn > sb ? 1 : -1;  // t_new has the larger index: it loses ties
       } else {
@@ -218,20 +474,6 @@ __global__ void __launch_bounds__(kLabelThreads)
       y[out] = yy;
     }
   }
-}
-
-// floor(d / n) for 0 <= d < 2^24 through the fp32 reciprocal, corrected by one step
-__device__ __forceinline__ int div_floor(int d, int n, float inv_n) {
-  int m = __float2int_rz(__fmul_rn((float)d, inv_n));
-  if (m * n > d) --m;
-  else if ((m + 1) * n <= d) ++m;
-  return m;
-}
-
-__device__ __forceinline__ float decayed_score_m(float r, int m, float lg) {
-  float sc = __fadd_rn(r, __fmul_rn((float)m, lg));
-  if (sc != sc) sc = __int_as_float(0xff800000);
-  return sc == 0.0f ? 0.0f : sc;  // -0 == +0
 }
 
 // Same result as teacher_labels_kernel for rows with at most CPT * kLabelThreads
@@ -558,12 +800,13 @@ extern "C" kvpop_status kvpop_teacher_labels(const float* r_tgt, int b, int H, i
   }
   const int cache = S <= kCacheFloats ? 1 : 0;
   const int smem = cache ? S * 4 : 0;
-  kvpop_status st = cuda_check(
-      cudaFuncSetAttribute(teacher_labels_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kCacheFloats * 4),
-      "kvpop_teacher_labels: smem attribute");
+  auto kern = S < (1 << 24) ? teacher_labels_kernel<true> : teacher_labels_kernel<false>;
+  grid.x = (S + kLongRowsPerCta - 1) / kLongRowsPerCta;
+  kvpop_status st = cuda_check(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kCacheFloats * 4),
+                               "kvpop_teacher_labels: smem attribute");
   if (st != KVPOP_OK) return st;
-  teacher_labels_kernel<<<grid, kLabelThreads, smem, cs>>>(r_tgt, H, S, bud.s, bud.w, bud.k, n, log_gamma, t_bnd,
-                                                            y, cache, device_status_ptr());
+  kern<<<grid, kLabelThreads, smem, cs>>>(r_tgt, H, S, bud.s, bud.w, bud.k, n, inv_n, log_gamma, t_bnd, y, cache,
+                                          device_status_ptr());
   return cuda_check(cudaGetLastError(), "kvpop_teacher_labels: launch");
 }
 

@@ -90,19 +90,40 @@ def test_teacher_labels_long_rows_uncached():
     assert (host(y)[0, 0, rows] == yr).all() and (host(tb)[0, 0, rows] == tbr).all()
 
 
-@pytest.mark.parametrize("S", [20000, 40000])   # rows beyond the register path: cached / global targets
-def test_teacher_labels_generic_kernel(S):
-    """Rows with more than 16384 candidates take the generic kernel (radix select,
-    and the previous row's cutoff as pivot within a CTA's 64 rows); whole CTA
-    chunks and scattered rows against the oracle, bit-exact."""
+@pytest.mark.parametrize("S,kind,gammas", [(20000, "ties", [0.93, 0.99]),      # cached targets
+                                            (40000, "ties", [0.93, 0.99]),      # global targets
+                                            (24000, "special", [1.0, 0.95])])   # NaN/-inf/-0, no decay
+def test_teacher_labels_generic_kernel(S, kind, gammas):
+    """Rows with more than 16384 candidates take the long-row kernel (a band of
+    scores carried from row to row, the previous cutoff as pivot, radix select);
+    whole CTA chunks and scattered rows against the oracle, bit-exact."""
     rng = np.random.default_rng(S)
     s, w, k, n = 5, 100, 3000, 8
-    r = _targets(rng, 1, 2, S, "ties")
-    lg = np.log(np.array([0.93, 0.99], np.float32)).astype(np.float32)
+    r = _targets(rng, 1, 2, S, kind)
+    lg = np.log(np.array(gammas, np.float32)).astype(np.float32)
     tb, y = kvpop.teacher_labels(dev(r), s, w, k, n, dev(lg))
     tb, y = host(tb), host(y)
     rows = np.concatenate([np.arange(S - 192, S), np.arange(3136, 3200),
                            np.random.default_rng(1).integers(w + s, S, 40)]).astype(np.int32)
+    for h in range(2):
+        tbr, yr = oracle.teacher_labels_rows(r[0, h], s, w, k, n, float(lg[h]), rows)
+        assert (y[0, h, rows] == yr).all() and (tb[0, h, rows] == tbr).all(), h
+
+
+def test_teacher_labels_long_context_rows():
+    """The long-context shape (S = 131072, budget s16 w1024 k3056, n = 64): rows of up
+    to 130 000 candidates, where each CTA carries a band of scores around its cutoff
+    from row to row.  Whole CTA chunks (64 consecutive rows, so every row after the
+    first works from the band and the previous cutoff) and scattered rows against
+    the oracle, bit-exact, for a slow and a fast decay."""
+    rng = np.random.default_rng(131072)
+    S, s, w, k, n = 131072, 16, 1024, 3056, 64
+    r = _targets(rng, 1, 2, S, "normal")
+    lg = np.log(np.array([0.90, 0.99], np.float32)).astype(np.float32)
+    tb, y = kvpop.teacher_labels(dev(r), s, w, k, n, dev(lg))
+    tb, y = host(tb), host(y)
+    rows = np.concatenate([np.arange(S - 128, S), np.arange(65536, 65600), np.arange(w + s + k, w + s + k + 64),
+                           np.random.default_rng(2).integers(w + s, S, 48)]).astype(np.int32)
     for h in range(2):
         tbr, yr = oracle.teacher_labels_rows(r[0, h], s, w, k, n, float(lg[h]), rows)
         assert (y[0, h, rows] == yr).all() and (tb[0, h, rows] == tbr).all(), h
