@@ -9,15 +9,14 @@
 //   kvpop_boundary_loss    -- the pairwise logistic loss on (t_new, t_bnd) with the
 //                             same decay on the predicted scores, and its gradient.
 //
-// Labels: one CTA per (row chunk, batch x head) walks its rows; per row the k-th
-// best "other" token is found by a radix select over a 64-bit key (decayed
-// score in order-preserving form, then the inverted index so that the lower
-// index wins ties), 8 bits per pass with a shared-memory histogram fed by
-// warp-aggregated increments, stopping as soon as one candidate is left.  Up to
-// 16384 candidates per row the keys stay in registers across the passes and the
-// previous row's cutoff is tried first as a pivot: one counting pass tells how
-// far the cutoff moved, and a move of up to kWalk places is followed key by key
-// (block-wide minimum or maximum beyond the pivot) instead of a full select.  The
+// Labels: one CTA per (64-row chunk, batch x head) walks its rows; per row the
+// k-th best "other" token is found among the candidates by their 64-bit keys
+// (decayed score in order-preserving form, then the inverted index so that the
+// lower index wins ties).  The CTA carries a band of scores around the cutoff
+// from row to row and re-scores only the candidates whose score changed; full
+// rows count against the previous cutoff and, failing that, take a radix select
+// (8 bits per pass, a shared-memory histogram fed by warp-aggregated
+// increments, stopping as soon as one candidate is left) -- see the kernel.  The
 // decayed score is computed in fp32 with one rounding after the product and one
 // after the sum (no contraction), -0 read as +0 and NaN as -inf, so the integer
 // outputs are exactly those of that definition.
@@ -31,10 +30,8 @@ namespace {
 constexpr int kLabelThreads = 512;
 constexpr int kLabelRowsPerCta = 64;
 constexpr int kCacheFloats = 32768;  // targets kept in shared memory when S fits (128 KB)
-constexpr int kWalk = 16;            // largest cutoff move followed key by key
-constexpr int kWindow = 512;         // keys kept around the pivot by the long-row kernel
-constexpr int kLongRowsPerCta = 64;   // rows per CTA of the long-row kernel
-constexpr int kBand = 2048;           // candidates kept in the long-row kernel's score band
+constexpr int kWindow = 512;         // keys kept around the pivot on a full row
+constexpr int kBand = 2048;          // candidates kept in the score band
 
 __device__ __forceinline__ float decayed_score(float r, int q, int t, int n, float lg) {
   const float m = (float)((q - t) / n);
@@ -65,8 +62,6 @@ __device__ __forceinline__ float decayed_score_m(float r, int m, float lg) {
   return sc == 0.0f ? 0.0f : sc;  // -0 == +0
 }
 
-// Rows with more candidates than the register-resident kernel holds.
-//
 // Band: from row to row only two things change -- the candidate that joins
 // (the previous row's leaving token) and the candidates whose decay step
 // floor((q - t) / n) grows at this row (t = q mod n, one in n); every other
@@ -106,8 +101,8 @@ __global__ void __launch_bounds__(kLabelThreads)
   const int h = bh % H;
   const float* r = r_tgt + (size_t)bh * S;
   const float lg = log_gamma[h];
-  const int q0 = blockIdx.x * kLongRowsPerCta;
-  const int q1 = min(S, q0 + kLongRowsPerCta);
+  const int q0 = blockIdx.x * kLabelRowsPerCta;
+  const int q1 = min(S, q0 + kLabelRowsPerCta);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int tmax = max(0, q1 - 1 - w);  // candidates of this CTA's rows are t < tmax
   if (cache)
@@ -476,186 +471,6 @@ __global__ void __launch_bounds__(kLabelThreads)
   }
 }
 
-// Same result as teacher_labels_kernel for rows with at most CPT * kLabelThreads
-// candidates: each thread keeps its candidates' keys in registers for all the
-// radix passes, and a row first tries the previous row's cutoff as a pivot (one
-// counting pass: it is still the cutoff when exactly k - 1 candidates beat it).
-template <int CPT>
-__global__ void __launch_bounds__(kLabelThreads)
-    teacher_labels_regs(const float* __restrict__ r_tgt, int H, int S, int s, int w, int k, int n, float inv_n,
-                        const float* __restrict__ log_gamma, int32_t* __restrict__ t_bnd,
-                        int32_t* __restrict__ y, int* status) {
-  static_assert(CPT <= 32, "validity bits");
-  __shared__ uint32_t hist[256];
-  __shared__ unsigned long long s_prefix;
-  __shared__ int s_need, s_left, s_found;
-  __shared__ int red[kLabelThreads / 32];
-  const int bh = blockIdx.y;
-  const float* r = r_tgt + (size_t)bh * S;
-  const float lg = log_gamma[bh % H];
-  const int q0 = blockIdx.x * kLabelRowsPerCta;
-  const int q1 = min(S, q0 + kLabelRowsPerCta);
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // block-wide sum of one int per thread (every thread gets it)
-  auto block_sum = [&](int v) -> int {
-    v = __reduce_add_sync(0xffffffffu, v);
-    if (lane == 0) red[warp] = v;
-    __syncthreads();
-    int tot = 0;
-#pragma unroll
-    for (int i = 0; i < kLabelThreads / 32; ++i) tot += red[i];
-    __syncthreads();
-    return tot;
-  };
-  // block-wide minimum (up) or maximum of a 64-bit key
-  __shared__ unsigned long long red64[kLabelThreads / 32];
-  auto block_extreme = [&](unsigned long long v, bool up) -> unsigned long long {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const unsigned long long u = __shfl_xor_sync(0xffffffffu, v, o);
-      v = up ? (u < v ? u : v) : (u > v ? u : v);
-    }
-    if (lane == 0) red64[warp] = v;
-    __syncthreads();
-    unsigned long long r = red64[0];
-#pragma unroll
-    for (int i = 1; i < kLabelThreads / 32; ++i) {
-      const unsigned long long u = red64[i];
-      r = up ? (u < r ? u : r) : (u > r ? u : r);
-    }
-    __syncthreads();
-    return r;
-  };
-  int prev = -1;  // the previous row's cutoff
-  for (int q = q0; q < q1; ++q) {
-    const int tn = q - w;
-    const size_t out = (size_t)bh * S + q;
-    if (tn < s || k == 0 || tn - s < k) {  // uniform over the CTA
-      if (tid == 0) {
-        t_bnd[out] = -1;
-        y[out] = tn < s ? 0 : (k == 0 ? -1 : 1);
-      }
-      continue;
-    }
-    unsigned long long kc[CPT];
-    uint32_t valid = 0;
-#pragma unroll
-    for (int j = 0; j < CPT; ++j) {
-      const int t = s + tid + j * kLabelThreads;
-      kc[j] = 0;
-      if (t < tn) {
-        kc[j] = label_key(decayed_score_m(__ldg(r + t), div_floor(q - t, n, inv_n), lg), t);
-        valid |= 1u << j;
-      }
-    }
-    int found = -1;
-    if (prev >= 0) {  // uniform: prev is a candidate of this row too (prev < q - 1 - w < tn)
-      const unsigned long long pk =
-          label_key(decayed_score_m(__ldg(r + prev), div_floor(q - prev, n, inv_n), lg), prev);
-      int c = 0;
-#pragma unroll
-      for (int j = 0; j < CPT; ++j) c += ((valid >> j) & 1u) && kc[j] > pk;
-      c = block_sum(c);  // keys above the previous cutoff
-      if (c == k - 1) {
-        found = prev;
-      } else if (c - (k - 1) <= kWalk && (k - 1) - c <= kWalk) {
-        // the cutoff moved by a few places: step key by key from the pivot --
-        // up through the (c - k + 1) smallest keys above it, or down through
-        // the (k - 1 - c) largest keys below it
-        const bool up = c > k - 1;
-        unsigned long long bound = pk;
-        for (int step = up ? c - (k - 1) : (k - 1) - c; step > 0; --step) {
-          unsigned long long best = up ? ~0ull : 0ull;
-#pragma unroll
-          for (int j = 0; j < CPT; ++j) {
-            if (!((valid >> j) & 1u)) continue;
-            if (up ? (kc[j] > bound && kc[j] < best) : (kc[j] < bound && kc[j] > best)) best = kc[j];
-          }
-          bound = block_extreme(best, up);
-        }
-        found = (int)(0xffffffffu - (uint32_t)bound);
-      }
-    }
-    if (found < 0) {
-      unsigned long long prefix = 0, mask = 0;
-      int need = k;
-      for (int shift = 56; shift >= 0; shift -= 8) {
-        for (int i = tid; i < 256; i += kLabelThreads) hist[i] = 0;
-        __syncthreads();
-#pragma unroll
-        for (int j = 0; j < CPT; ++j) {
-          const bool match = ((valid >> j) & 1u) && (kc[j] & mask) == prefix;
-          const uint32_t active = __ballot_sync(0xffffffffu, match);
-          if (match) {
-            const uint32_t bin = (uint32_t)(kc[j] >> shift) & 255u;
-            const uint32_t peers = __match_any_sync(active, bin);
-            if ((__ffs(peers) - 1) == lane) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
-          }
-        }
-        __syncthreads();
-        if (warp == 0) {
-          uint32_t c[8], tot = 0;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            c[i] = hist[255 - 8 * lane - i];
-            tot += c[i];
-          }
-          uint32_t incl = tot;
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += v;
-          }
-          const uint32_t excl = incl - tot;
-          if (excl < (uint32_t)need && (uint32_t)need <= incl) {
-            uint32_t run = excl;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              if (run + c[i] >= (uint32_t)need) {
-                s_prefix = prefix | ((unsigned long long)(255 - 8 * lane - i) << shift);
-                s_need = need - (int)run;
-                s_left = (int)c[i];
-                break;
-              }
-              run += c[i];
-            }
-          }
-        }
-        __syncthreads();
-        prefix = s_prefix;
-        mask |= 255ull << shift;
-        need = s_need;
-        const int left = s_left;
-        __syncthreads();
-        if (left == 1 || shift == 0) {
-          if (tid == 0) s_found = -1;
-          __syncthreads();
-#pragma unroll
-          for (int j = 0; j < CPT; ++j)
-            if (((valid >> j) & 1u) && (kc[j] & mask) == prefix) atomicMax(&s_found, s + tid + j * kLabelThreads);
-          __syncthreads();
-          found = s_found;
-          __syncthreads();
-          break;
-        }
-      }
-    }
-    prev = found;
-    if (tid == 0) {
-      int yy = -1;
-      if (found >= 0) {
-        const float sb = decayed_score_m(__ldg(r + found), div_floor(q - found, n, inv_n), lg);
-        const float sn = decayed_score_m(__ldg(r + tn), div_floor(q - tn, n, inv_n), lg);
-        yy = sn > sb ? 1 : -1;  // t_new has the larger index: it loses ties
-      } else {
-        report_error(status, KVPOP_ERR_INTERNAL, SITE_INTERNAL_CHECK, 21);
-      }
-      t_bnd[out] = found;
-      y[out] = yy;
-    }
-  }
-}
-
 __global__ void target_normalize_kernel(const float* __restrict__ target, long long total, int S, int G, int w,
                                         float eps, float* __restrict__ r) {
   const float leps = eps > 0.0f ? logf(eps) : __int_as_float(0xff800000);
@@ -785,23 +600,10 @@ extern "C" kvpop_status kvpop_teacher_labels(const float* r_tgt, int b, int H, i
   }
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   dim3 grid((S + kLabelRowsPerCta - 1) / kLabelRowsPerCta, b * H);
-  // candidates of the last row: S - 1 - w - s
-  const long long maxc = (long long)S - 1 - bud.w - bud.s;
   const float inv_n = 1.0f / (float)n;
-  if (S < (1 << 24) && maxc <= 8LL * kLabelThreads) {
-    teacher_labels_regs<8><<<grid, kLabelThreads, 0, cs>>>(r_tgt, H, S, bud.s, bud.w, bud.k, n, inv_n, log_gamma,
-                                                           t_bnd, y, device_status_ptr());
-    return cuda_check(cudaGetLastError(), "kvpop_teacher_labels: launch");
-  }
-  if (S < (1 << 24) && maxc <= 32LL * kLabelThreads) {
-    teacher_labels_regs<32><<<grid, kLabelThreads, 0, cs>>>(r_tgt, H, S, bud.s, bud.w, bud.k, n, inv_n, log_gamma,
-                                                            t_bnd, y, device_status_ptr());
-    return cuda_check(cudaGetLastError(), "kvpop_teacher_labels: launch");
-  }
   const int cache = S <= kCacheFloats ? 1 : 0;
   const int smem = cache ? S * 4 : 0;
   auto kern = S < (1 << 24) ? teacher_labels_kernel<true> : teacher_labels_kernel<false>;
-  grid.x = (S + kLongRowsPerCta - 1) / kLongRowsPerCta;
   kvpop_status st = cuda_check(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kCacheFloats * 4),
                                "kvpop_teacher_labels: smem attribute");
   if (st != KVPOP_OK) return st;

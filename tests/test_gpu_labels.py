@@ -90,13 +90,13 @@ def test_teacher_labels_long_rows_uncached():
     assert (host(y)[0, 0, rows] == yr).all() and (host(tb)[0, 0, rows] == tbr).all()
 
 
-@pytest.mark.parametrize("S,kind,gammas", [(20000, "ties", [0.93, 0.99]),      # cached targets
-                                            (40000, "ties", [0.93, 0.99]),      # global targets
+@pytest.mark.parametrize("S,kind,gammas", [(20000, "ties", [0.93, 0.99]),      # targets cached in shared memory
+                                            (40000, "ties", [0.93, 0.99]),      # targets read from global memory
                                             (24000, "special", [1.0, 0.95])])   # NaN/-inf/-0, no decay
-def test_teacher_labels_generic_kernel(S, kind, gammas):
-    """Rows with more than 16384 candidates take the long-row kernel (a band of
-    scores carried from row to row, the previous cutoff as pivot, radix select);
-    whole CTA chunks and scattered rows against the oracle, bit-exact."""
+def test_teacher_labels_long_rows(S, kind, gammas):
+    """Rows of tens of thousands of candidates (a band of scores carried from row
+    to row, the previous cutoff as pivot, radix select when the cutoff leaves the
+    band); whole CTA chunks and scattered rows against the oracle, bit-exact."""
     rng = np.random.default_rng(S)
     s, w, k, n = 5, 100, 3000, 8
     r = _targets(rng, 1, 2, S, kind)
