@@ -38,7 +38,6 @@ namespace {
 constexpr int kThreads = 384;
 constexpr int kKeys = 128;
 constexpr int kRows = 512;  // query positions per long-pair block (a multiple of the list block)
-constexpr int kMetaStages = 4;
 constexpr int kBlockBytes = 128 * 128;  // 128 rows x 128 bytes (64 bf16)
 constexpr int kHalfBytes = 64 * 128;    // 64 rows of such a block
 constexpr int kRegsIo = 80;
@@ -176,30 +175,38 @@ __global__ void __launch_bounds__(kRows) bwd_keys(const int32_t* __restrict__ ev
 // ---------------------------------------------------------------------------
 // bwd_dq: query-major dQ
 // ---------------------------------------------------------------------------
-template <int NS>
+constexpr int kDqMetaStages = 2;  // key metadata is read by the elementwise warps only
+
+template <int NSK, int NSV>
 struct DqBars {
   uint64_t q_full, q_empty;
-  uint64_t k_full[NS], k_empty[NS], v_full[NS], v_empty[NS];
+  uint64_t k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV];
   uint64_t s_full[2], ds_full[2];
   uint64_t dp_empty;
   uint64_t o_full, o_empty;
-  uint64_t meta_full[kMetaStages], meta_empty[kMetaStages];
+  uint64_t meta_full[kDqMetaStages], meta_empty[kDqMetaStages];
   uint64_t drain;
 };
 
+// A K stage lives from its gather until dQ of its tile has run (after the next
+// tile's S and dP), a V stage only until dP: three K stages and two V stages.
+// The layout fills the opt-in maximum exactly, so it assumes (and the kernel
+// checks) a 1024-byte aligned dynamic shared-memory base.
 template <int D>
 struct DqLayout {
   static constexpr int DH = D / 64;
-  static constexpr int NS = D == 128 ? 2 : 4;
+  static constexpr int NSK = D == 128 ? 3 : 4;
+  static constexpr int NSV = D == 128 ? 2 : 4;
   static constexpr int q_off = 0;
   static constexpr int do_off = q_off + DH * kBlockBytes;
   static constexpr int k_off = do_off + DH * kBlockBytes;
-  static constexpr int v_off = k_off + NS * DH * kBlockBytes;
-  static constexpr int meta_off = v_off + NS * DH * kBlockBytes;
-  static constexpr int meta_bytes = kMetaStages * (kKeys + 4) * 8;
+  static constexpr int v_off = k_off + NSK * DH * kBlockBytes;
+  static constexpr int meta_off = v_off + NSV * DH * kBlockBytes;
+  static constexpr int meta_bytes = kDqMetaStages * (kKeys + 4) * 8;
   static constexpr int bar_off = meta_off + meta_bytes;
-  static constexpr int misc_off = bar_off + (int)sizeof(DqBars<NS>);
-  static constexpr int total = misc_off + 64 + 1024;
+  static constexpr int misc_off = bar_off + (int)sizeof(DqBars<NSK, NSV>);
+  static constexpr int total = misc_off + 64;
+  static_assert(total <= 232448, "shared memory");
 };
 
 // One query tile (P positions x G heads) of (batch b, KV head h) and its key
@@ -234,6 +241,15 @@ __device__ __forceinline__ DqItem make_dq_item(const BwdParams& p, int it) {
   return x;
 }
 
+// Position of key i of an item's gathered part (sinks, then the list), or -1
+// for padding and for a list entry outside [0, S) (the metadata warp reports those).
+__device__ __forceinline__ int dq_gather_pos(const DqItem& x, int i, int S) {
+  int pos = -1;
+  if (i < x.n_sink) pos = i;
+  else if (i < x.n_sl) pos = __ldg(&x.list[i - x.n_sink].x);
+  return pos >= 0 && pos < S ? pos : -1;
+}
+
 // Warp roles (512 threads):
 //   warp 0      key metadata of each K/V tile: (position, eviction row) per key
 //               and per 32-key chunk the latest position and earliest
@@ -256,10 +272,14 @@ template <int D>
 __global__ void __launch_bounds__(kDqThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdParams p) {
   using L = DqLayout<D>;
   constexpr int DH = L::DH;
-  constexpr int NS = L::NS;
+  constexpr int NSK = L::NSK, NSV = L::NSV;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-  DqBars<NS>* bars = reinterpret_cast<DqBars<NS>*>(smem + L::bar_off);
+  if (smem_u32(smem_raw) & 1023) {  // the 128-byte swizzled tiles need 1024-byte alignment
+    if (threadIdx.x == 0) report_error(p.status, KVPOP_ERR_INTERNAL, SITE_INTERNAL_CHECK, 12);
+    return;
+  }
+  uint8_t* smem = smem_raw;
+  DqBars<NSK, NSV>* bars = reinterpret_cast<DqBars<NSK, NSV>*>(smem + L::bar_off);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::misc_off + 4);
   int2* meta = reinterpret_cast<int2*>(smem + L::meta_off);
@@ -271,9 +291,11 @@ __global__ void __launch_bounds__(kDqThreads, 1) bwd_dq_kernel(const __grid_cons
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 2);  // Q (warp 2) and dO (warp 3)
     mbar_init(&bars->q_empty, 1);
-    for (int i = 0; i < NS; ++i) {
+    for (int i = 0; i < NSK; ++i) {
       mbar_init(&bars->k_full[i], 1);
       mbar_init(&bars->k_empty[i], 1);
+    }
+    for (int i = 0; i < NSV; ++i) {
       mbar_init(&bars->v_full[i], 1);
       mbar_init(&bars->v_empty[i], 1);
     }
@@ -284,9 +306,9 @@ __global__ void __launch_bounds__(kDqThreads, 1) bwd_dq_kernel(const __grid_cons
     mbar_init(&bars->dp_empty, 8);
     mbar_init(&bars->o_full, 1);
     mbar_init(&bars->o_empty, 8);
-    for (int i = 0; i < kMetaStages; ++i) {
+    for (int i = 0; i < kDqMetaStages; ++i) {
       mbar_init(&bars->meta_full[i], 1);
-      mbar_init(&bars->meta_empty[i], 14);  // 8 elementwise warps + 2 loader warps + 4 helpers
+      mbar_init(&bars->meta_empty[i], 8);  // the elementwise warps
     }
     mbar_init(&bars->drain, 1);
     *abort_flag = 0;
@@ -311,18 +333,24 @@ __global__ void __launch_bounds__(kDqThreads, 1) bwd_dq_kernel(const __grid_cons
   const uint32_t do_addr = sbase + L::do_off;
   const uint32_t k_addr = sbase + L::k_off;
   const uint32_t v_addr = sbase + L::v_off;
-  // gather4 op `o` of a gathered tile (o < kGatherOps): keys 4 (o % 32) .. + 3, dims 64 (o / 32) ..
-  auto issue_gather_ops = [&](int first, int count, const int2* km, int row_base, int off, int st,
-                              const CUtensorMap* rmap, uint64_t* bar) {
+  // gather4 op `o` of a gathered tile (o < kGatherOps): keys 4 (o % 32) .. + 3, dims 64 (o / 32) ..;
+  // the rows are read from the item's list before the stage is free, so the
+  // list loads overlap the wait
+  auto gather_rows = [&](int first, int count, const DqItem& x, int j, int row_base, int (&rows)[4]) {
+    if (lane < count) {
+      const int q4 = (first + lane) & 31;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int pos = dq_gather_pos(x, j * kKeys + 4 * q4 + u, S);
+        rows[u] = pos >= 0 ? row_base + pos * p.H : row_base;  // padding: any row, masked
+      }
+    }
+  };
+  auto issue_gather_ops = [&](int first, int count, const int (&rows)[4], int off, int st, const CUtensorMap* rmap,
+                              uint64_t* bar) {
     if (lane < count) {
       const int o = first + lane;
       const int q4 = o & 31, d2 = o >> 5;
-      int rows[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int pos = km[4 * q4 + u].x;
-        rows[u] = pos != 0x7fffffff ? row_base + pos * p.H : row_base;  // padding: any row, masked
-      }
       tma_gather4(smem + off + (st * DH + d2) * kBlockBytes + q4 * 512, rmap, bar, d2 * 64, rows[0], rows[1],
                   rows[2], rows[3]);
     }
@@ -337,6 +365,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) bwd_dq_kernel(const __grid_cons
     uint64_t* full = is_v ? bars->v_full : bars->k_full;
     uint64_t* empty = is_v ? bars->v_empty : bars->k_empty;
     const int off = is_v ? L::v_off : L::k_off;
+    const int ns = is_v ? NSV : NSK;
     const int first = part * kOpsPerIssuer;
     const int count = min(kOpsPerIssuer, (DH * kKeys / 4) - first);
     bool ok = true;
@@ -345,23 +374,18 @@ __global__ void __launch_bounds__(kDqThreads, 1) bwd_dq_kernel(const __grid_cons
       const DqItem x = make_dq_item(p, it);
       const int row_base = x.b * S * p.H + x.h;
       for (int j = 0; j < x.NT; ++j, ++t) {
-        const int st = t % NS;
-        const int ms = t % kMetaStages;
-        if (!warp_wait(&bars->meta_full[ms], (t / kMetaStages) & 1, abort_flag)) {
-          if (lane == 0) fail(SITE_ATTN_PRODUCER, 40);
-          ok = false;
-          break;
-        }
+        const int st = t % ns;
+        int rows[4];
+        if (j < x.NTg) gather_rows(first, count, x, j, row_base, rows);
         // every tile, gathered or not: a parity wait is only exact while the
         // waiter is at most one phase ahead of the barrier
-        if (!warp_wait(&empty[st], ((t / NS) & 1) ^ 1, abort_flag)) {
+        if (!warp_wait(&empty[st], ((t / ns) & 1) ^ 1, abort_flag)) {
           if (lane == 0) fail(SITE_ATTN_PRODUCER, 43);
           ok = false;
           break;
         }
-        if (j < x.NTg) issue_gather_ops(first, count, meta + ms * (kKeys + 4), row_base, off, st, rmap, &full[st]);
+        if (j < x.NTg) issue_gather_ops(first, count, rows, off, st, rmap, &full[st]);
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->meta_empty[ms]);
       }
     }
   } else if (warp < 4) {
@@ -391,9 +415,9 @@ __global__ void __launch_bounds__(kDqThreads, 1) bwd_dq_kernel(const __grid_cons
         int2 cur_e[4], nxt_e[4];
         load_tile(0, cur_e);
         for (int j = 0; j < x.NT; ++j, ++t) {
-          const int ms = t % kMetaStages;
+          const int ms = t % kDqMetaStages;
           if (j + 1 < x.NT) load_tile(j + 1, nxt_e);
-          if (!warp_wait(&bars->meta_empty[ms], ((t / kMetaStages) & 1) ^ 1, abort_flag)) {
+          if (!warp_wait(&bars->meta_empty[ms], ((t / kDqMetaStages) & 1) ^ 1, abort_flag)) {
             if (lane == 0) fail(SITE_ATTN_PRODUCER, 31);
             ok = false;
             break;
@@ -427,16 +451,19 @@ __global__ void __launch_bounds__(kDqThreads, 1) bwd_dq_kernel(const __grid_cons
       if (lane == 0 && it0 < p.nitems) {
         constexpr uint32_t idesc_s = idesc_bf16(128, 128, 0);
         constexpr uint32_t idesc_dq = idesc_bf16(128, D, 1);
-        auto issue_nt = [&](uint32_t a_base, uint32_t b_base, uint32_t dcol) {  // A B^T over D
+        // the issuing thread shares its SMSP with busy elementwise warps, so each
+        // MMA is issued with as few instructions as possible: descriptor low
+        // words stepped by constants
+        auto issue_nt = [&](uint32_t a_lo, uint32_t b_lo, uint32_t d) {  // A B^T over D
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
-            const int dh = ks >> 2;
-            const uint32_t w32 = (uint32_t)(ks & 3) * 32;
-            const uint64_t a = smem_desc_sw128(a_base + dh * kBlockBytes + w32, 16, 1024);
-            const uint64_t bd = smem_desc_sw128(b_base + dh * kBlockBytes + w32, 16, 1024);
-            mma_ss(tbase + dcol, a, bd, idesc_s, ks > 0 ? 1u : 0u);
+            const uint32_t off = (uint32_t)(((ks >> 2) * kBlockBytes + (ks & 3) * 32) >> 4);
+            mma_ss_lo(d, a_lo + off, b_lo + off, idesc_s, ks > 0 ? 1u : 0u);
           }
         };
+        const uint32_t q_lo = desc_lo(q_addr, 16), do_lo = desc_lo(do_addr, 16);
+        const uint32_t k_lo = desc_lo(k_addr, 16), v_lo = desc_lo(v_addr, 16);
+        const uint32_t kq_lo = desc_lo(k_addr, DH > 1 ? kBlockBytes : 16);  // K as the MN-major B of dQ
         auto wait_bar = [&](uint64_t* bar, uint32_t ph, int detail) -> bool {
           if (!mbar_wait(bar, ph, abort_flag)) {
             fail(SITE_ATTN_MMA, detail);
@@ -445,42 +472,44 @@ __global__ void __launch_bounds__(kDqThreads, 1) bwd_dq_kernel(const __grid_cons
           tc_fence_after();
           return true;
         };
-        // S_t and dP_t of global tile t (ring stage st, phase ph); item counter n
-        auto issue_sdp = [&](int t, int st, uint32_t ph, bool first_of_item, int n) -> bool {
+        // S_t and dP_t of global tile t; item counter n
+        auto issue_sdp = [&](int t, bool first_of_item, int n) -> bool {
+          const int kst = t % NSK, vst = t % NSV;
           if (first_of_item && !wait_bar(&bars->q_full, n & 1, 31)) return false;
-          if (!wait_bar(&bars->k_full[st], ph, 32)) return false;
-          issue_nt(q_addr, k_addr + st * DH * kBlockBytes, 128u * (uint32_t)(t & 1));
+          if (!wait_bar(&bars->k_full[kst], (t / NSK) & 1, 32)) return false;
+          issue_nt(q_lo, k_lo + (uint32_t)(kst * DH * kBlockBytes >> 4), tbase + 128u * (uint32_t)(t & 1));
           if (t > 0 && !wait_bar(&bars->dp_empty, (t - 1) & 1, 33)) return false;
-          if (!wait_bar(&bars->v_full[st], ph, 34)) return false;
-          issue_nt(do_addr, v_addr + st * DH * kBlockBytes, 256u);
+          if (!wait_bar(&bars->v_full[vst], (t / NSV) & 1, 34)) return false;
+          issue_nt(do_lo, v_lo + (uint32_t)(vst * DH * kBlockBytes >> 4), tbase + 256u);
           mma_commit(&bars->s_full[t & 1]);
-          mma_commit(&bars->v_empty[st]);
+          mma_commit(&bars->v_empty[vst]);
           return true;
         };
         DqItem x = make_dq_item(p, it0);
-        bool ok = issue_sdp(0, 0, 0, true, 0);
+        bool ok = issue_sdp(0, true, 0);
         if (ok && x.NT == 1) mma_commit(&bars->q_empty);
         int t = 0, n = 0;
         for (int it = it0; ok;) {
           for (int j = 0; ok && j < x.NT; ++j, ++t) {
-            const int st = t % NS;
+            const int st = t % NSK;
             const bool last = j + 1 == x.NT;
             const int it1 = last ? it + dit : it;
             if (it1 < p.nitems) {
               const int NT1 = last ? make_dq_item(p, it1).NT : x.NT;
               const int j1 = last ? 0 : j + 1;
-              if (!(ok = issue_sdp(t + 1, (t + 1) % NS, ((t + 1) / NS) & 1, j1 == 0, last ? n + 1 : n))) break;
+              if (!(ok = issue_sdp(t + 1, j1 == 0, last ? n + 1 : n))) break;
               if (j1 == NT1 - 1) mma_commit(&bars->q_empty);  // every S and dP of that item issued
             }
             if (!(ok = wait_bar(&bars->ds_full[t & 1], (t >> 1) & 1, 35))) break;
             if (j == 0 && !(ok = wait_bar(&bars->o_empty, (n & 1) ^ 1, 36))) break;
+            const uint32_t b0 = kq_lo + (uint32_t)(st * DH * kBlockBytes >> 4);
+            const uint32_t a0 = tbase + 128u * (uint32_t)(t & 1);
+            const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
             for (int ks = 0; ks < kKeys / 16; ++ks) {
-              const uint64_t bd = smem_desc_sw128(k_addr + st * DH * kBlockBytes + ks * 2048,
-                                                  DH > 1 ? kBlockBytes : 16, 1024);
               // dS of keys 16 ks .. 16 ks + 15: warpgroup ks / 4 packed them over its own S columns
-              const uint32_t a_col = 128u * (uint32_t)(t & 1) + 64u * (uint32_t)(ks >> 2) + 8u * (uint32_t)(ks & 3);
-              mma_ts(tbase + 384, tbase + a_col, bd, idesc_dq, (j > 0 || ks > 0) ? 1u : 0u);
+              mma_ts_lo(tbase + 384, a0 + (uint32_t)(64 * (ks >> 2) + 8 * (ks & 3)), b0 + (uint32_t)(ks * 2048 >> 4),
+                        idesc_dq, ks > 0 ? 1u : acc0);
             }
             mma_commit(&bars->k_empty[st]);
             if (last) mma_commit(&bars->o_full);
@@ -504,6 +533,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) bwd_dq_kernel(const __grid_cons
       uint64_t* empty = is_v ? bars->v_empty : bars->k_empty;
       const int off = is_v ? L::v_off : L::k_off;
       const int qoff = is_v ? L::do_off : L::q_off;
+      const int ns = is_v ? NSV : NSK;
       if (lane == 0) tma_prefetch_desc(qmap);
       bool ok = true;
       int t = 0, n = 0;
@@ -523,14 +553,10 @@ __global__ void __launch_bounds__(kDqThreads, 1) bwd_dq_kernel(const __grid_cons
         if (!ok) break;
         const int row_base = x.b * S * p.H + x.h;  // row of position t is row_base + t * H
         for (int j = 0; j < x.NT; ++j, ++t) {
-          const int st = t % NS;
-          const uint32_t ph = (t / NS) & 1;
-          const int ms = t % kMetaStages;
-          if (!warp_wait(&bars->meta_full[ms], (t / kMetaStages) & 1, abort_flag)) {
-            if (lane == 0) fail(SITE_ATTN_PRODUCER, 38);
-            ok = false;
-            break;
-          }
+          const int st = t % ns;
+          const uint32_t ph = (t / ns) & 1;
+          int rows[4];
+          if (j < x.NTg) gather_rows(0, min(kOpsPerIssuer, DH * kKeys / 4), x, j, row_base, rows);
           if (!warp_wait(&empty[st], ph ^ 1, abort_flag)) {
             if (lane == 0) fail(SITE_ATTN_PRODUCER, 39);
             ok = false;
@@ -540,15 +566,13 @@ __global__ void __launch_bounds__(kDqThreads, 1) bwd_dq_kernel(const __grid_cons
           __syncwarp();
           if (j < x.NTg) {
             // the first third of the tile's gather4 ops; warps 12-15 issue the rest
-            issue_gather_ops(0, min(kOpsPerIssuer, DH * kKeys / 4), meta + ms * (kKeys + 4), row_base, off, st,
-                             rmap, &full[st]);
+            issue_gather_ops(0, min(kOpsPerIssuer, DH * kKeys / 4), rows, off, st, rmap, &full[st]);
           } else if (lane == 0) {
             const int span_row = x.sp0 + (j - x.NTg) * kKeys;
             for (int d2 = 0; d2 < DH; ++d2)
               tma_load_4d(smem + off + (st * DH + d2) * kBlockBytes, tmap, &full[st], d2 * 64, x.h, span_row, x.b);
           }
           __syncwarp();
-          if (lane == 0) mbar_arrive(&bars->meta_empty[ms]);
         }
       }
     }
@@ -578,8 +602,8 @@ __global__ void __launch_bounds__(kDqThreads, 1) bwd_dq_kernel(const __grid_cons
           break;
         }
         tc_fence_after();
-        const int ms = t % kMetaStages;
-        if (!warp_wait(&bars->meta_full[ms], (t / kMetaStages) & 1, abort_flag)) {
+        const int ms = t % kDqMetaStages;
+        if (!warp_wait(&bars->meta_full[ms], (t / kDqMetaStages) & 1, abort_flag)) {
           if (lane == 0) fail(SITE_ATTN_SOFTMAX, 32);
           ok = false;
           break;

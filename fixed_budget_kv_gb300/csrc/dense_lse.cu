@@ -154,7 +154,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!ok) fail(SITE_ATTN_MMA, 21);
         tc_fence_after();
         constexpr uint32_t idesc = idesc_bf16(256, 128, 0);
-        const uint32_t q_addr = sbase + L::q_off, k_addr = sbase + L::k_off;
+        // descriptor low words stepped by constants: the issuing thread shares
+        // its SMSP with four busy softmax warps, so every MMA costs few instructions
+        const uint32_t q_lo = desc_lo(sbase + L::q_off, 16), k_lo = desc_lo(sbase + L::k_off, 16);
         for (int j = 0; ok && j < NT; ++j) {
           const int st = j % NS;
           if (!mbar_wait(&bars->k_full[st], (j / NS) & 1, abort_flag)) {
@@ -170,13 +172,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               break;
             }
             tc_fence_after();
+            const uint32_t a0 = q_lo + (uint32_t)(u * DH * kBlockBytes >> 4);
+            const uint32_t b0 = k_lo + (uint32_t)(st * DH * kHalfBytes >> 4);
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks) {
-              const int dh = ks >> 2;
-              const uint32_t w32 = (uint32_t)(ks & 3) * 32;
-              const uint64_t a = smem_desc_sw128(q_addr + (u * DH + dh) * kBlockBytes + w32, 16, 1024);
-              const uint64_t bd = smem_desc_sw128(k_addr + (st * DH + dh) * kHalfBytes + w32, 16, 1024);
-              mma_ss_pair(tbase + 128 * u, a, bd, idesc, ks > 0 ? 1u : 0u);
+              const uint32_t w = (uint32_t)((ks & 3) * 32 >> 4);
+              mma_ss_pair_lo(tbase + 128 * u, a0 + (uint32_t)((ks >> 2) * kBlockBytes >> 4) + w,
+                             b0 + (uint32_t)((ks >> 2) * kHalfBytes >> 4) + w, idesc, ks > 0 ? 1u : 0u);
             }
             mma_commit_pair(&bars->s_full[u]);
           }

@@ -189,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1) target_kernel(const __grid_consta
       if (!ok) fail(SITE_TARGET_MMA, 1);
       tc_fence_after();
       constexpr uint32_t idesc = idesc_bf16(128, 128, 0);
-      const uint32_t k_addr = sbase + L::k_off, q_addr = sbase + L::q_off;
+      const uint32_t k_lo = desc_lo(sbase + L::k_off, 16), q_lo = desc_lo(sbase + L::q_off, 16);
       int n_rt[kNR] = {0, 0, 0, 0};
       for (int jc = 0; ok && jc < NTc; ++jc) {
         const int c = c_lo + jc;
@@ -209,13 +209,14 @@ __global__ void __launch_bounds__(kThreads, 1) target_kernel(const __grid_consta
             break;
           }
           tc_fence_after();
+          // descriptor low words stepped by constants: the issuing thread shares
+          // its SMSP with four busy warps, so every MMA costs few instructions
+          const uint32_t a0 = k_lo + (uint32_t)(rt * DH * kBlockBytes >> 4);
+          const uint32_t b0 = q_lo + (uint32_t)(st * DH * kBlockBytes >> 4);
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
-            const int dh = ks >> 2;
-            const uint32_t w32 = (uint32_t)(ks & 3) * 32;
-            const uint64_t a = smem_desc_sw128(k_addr + (rt * DH + dh) * kBlockBytes + w32, 16, 1024);
-            const uint64_t bd = smem_desc_sw128(q_addr + (st * DH + dh) * kBlockBytes + w32, 16, 1024);
-            mma_ss(tbase + 128 * rt, a, bd, idesc, ks > 0 ? 1u : 0u);
+            const uint32_t off = (uint32_t)(((ks >> 2) * kBlockBytes + (ks & 3) * 32) >> 4);
+            mma_ss_lo(tbase + 128 * rt, a0 + off, b0 + off, idesc, ks > 0 ? 1u : 0u);
           }
           mma_commit(&bars->s_full[rt]);
         }
