@@ -877,39 +877,39 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
         };
         // S^T = K Q^T and dP^T = V dO^T over the whole 128-row query tile in stage stg,
         // committed separately so that P can be computed while dP^T runs
+        // descriptor low words stepped by constants: the issuing thread shares
+        // its SMSP with busy elementwise warps, so every MMA costs few instructions
         auto issue_sdp = [&](int stg) {
+          const uint32_t ka = desc_lo(k_addr, 16), qb = desc_lo(q_stage(stg), 16);
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
-            const int dh = ks >> 2;
-            const uint32_t w32 = (uint32_t)(ks & 3) * 32;
-            const uint64_t a = smem_desc_sw128(k_addr + dh * kBlockBytes + w32, 16, 1024);
-            const uint64_t bd = smem_desc_sw128(q_stage(stg) + dh * kBlockBytes + w32, 16, 1024);
-            mma_ss(tbase + 256, a, bd, idesc_s, ks > 0 ? 1u : 0u);
+            const uint32_t off = (uint32_t)(((ks >> 2) * kBlockBytes + (ks & 3) * 32) >> 4);
+            mma_ss_lo(tbase + 256, ka + off, qb + off, idesc_s, ks > 0 ? 1u : 0u);
           }
           mma_commit(&bars->s_full[0]);  // S^T: the elementwise warps start on P
+          const uint32_t va = desc_lo(v_addr, 16), db = desc_lo(do_stage(stg), 16);
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
-            const int dh = ks >> 2;
-            const uint32_t w32 = (uint32_t)(ks & 3) * 32;
-            const uint64_t a = smem_desc_sw128(v_addr + dh * kBlockBytes + w32, 16, 1024);
-            const uint64_t bd = smem_desc_sw128(do_stage(stg) + dh * kBlockBytes + w32, 16, 1024);
-            mma_ss(tbase + 384, a, bd, idesc_s, ks > 0 ? 1u : 0u);
+            const uint32_t off = (uint32_t)(((ks >> 2) * kBlockBytes + (ks & 3) * 32) >> 4);
+            mma_ss_lo(tbase + 384, va + off, db + off, idesc_s, ks > 0 ? 1u : 0u);
           }
           mma_commit(&bars->s_full[1]);  // dP^T
         };
         // dV += P^T dO and dK += dS^T Q over rows 64 h .. 64 h + 63, whose P^T and dS^T
         // warpgroup h packed over the first 32 of its own 64 columns
         auto issue_acc = [&](int stg, int h, bool first) {
+          constexpr uint32_t lbo = DH > 1 ? kBlockBytes : 16;
+          const uint32_t db = desc_lo(do_stage(stg) + h * kHalfBytes, lbo);
+          const uint32_t acc0 = first ? 0u : 1u;
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t bd = smem_desc_sw128(do_stage(stg) + h * kHalfBytes + ks * 2048, DH > 1 ? kBlockBytes : 16, 1024);
-            mma_ts(tbase, tbase + 256 + 64 * h + ks * 8, bd, idesc_acc, (first && ks == 0) ? 0u : 1u);
-          }
+          for (int ks = 0; ks < 4; ++ks)
+            mma_ts_lo(tbase, tbase + 256 + 64 * h + ks * 8, db + (uint32_t)(ks * 2048 >> 4), idesc_acc,
+                      ks > 0 ? 1u : acc0);
+          const uint32_t qb = desc_lo(q_stage(stg) + h * kHalfBytes, lbo);
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t bd = smem_desc_sw128(q_stage(stg) + h * kHalfBytes + ks * 2048, DH > 1 ? kBlockBytes : 16, 1024);
-            mma_ts(tbase + D, tbase + 384 + 64 * h + ks * 8, bd, idesc_acc, (first && ks == 0) ? 0u : 1u);
-          }
+          for (int ks = 0; ks < 4; ++ks)
+            mma_ts_lo(tbase + D, tbase + 384 + 64 * h + ks * 8, qb + (uint32_t)(ks * 2048 >> 4), idesc_acc,
+                      ks > 0 ? 1u : acc0);
         };
         bool ok = true;
         int u = 0, n = 0;
