@@ -486,6 +486,9 @@ __global__ void __launch_bounds__(kDqThreads, 1) bwd_dq_kernel(const __grid_cons
           return true;
         };
         DqItem x = make_dq_item(p, it0);
+        // the next item's tile count, worked out once per item (its index
+        // arithmetic stays off the per-tile path)
+        int NTn = it0 + dit < p.nitems ? make_dq_item(p, it0 + dit).NT : 0;
         bool ok = issue_sdp(0, true, 0);
         if (ok && x.NT == 1) mma_commit(&bars->q_empty);
         int t = 0, n = 0;
@@ -493,9 +496,8 @@ __global__ void __launch_bounds__(kDqThreads, 1) bwd_dq_kernel(const __grid_cons
           for (int j = 0; ok && j < x.NT; ++j, ++t) {
             const int st = t % NSK;
             const bool last = j + 1 == x.NT;
-            const int it1 = last ? it + dit : it;
-            if (it1 < p.nitems) {
-              const int NT1 = last ? make_dq_item(p, it1).NT : x.NT;
+            if (!last || NTn > 0) {
+              const int NT1 = last ? NTn : x.NT;
               const int j1 = last ? 0 : j + 1;
               if (!(ok = issue_sdp(t + 1, j1 == 0, last ? n + 1 : n))) break;
               if (j1 == NT1 - 1) mma_commit(&bars->q_empty);  // every S and dP of that item issued
@@ -519,6 +521,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) bwd_dq_kernel(const __grid_cons
           ++n;
           if (it >= p.nitems) break;
           x = make_dq_item(p, it);
+          NTn = it + dit < p.nitems ? make_dq_item(p, it + dit).NT : 0;
         }
         mma_commit(&bars->drain);
         mbar_wait(&bars->drain, 0, nullptr);
