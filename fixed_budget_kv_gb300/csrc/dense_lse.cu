@@ -2,32 +2,28 @@
 // the dense causal attention; section 2.3: its normaliser LSE_d), the
 // QK^T-only pass behind kvpop_attn_fwd(O = NULL, no mask).
 //
-// A pair of CTAs (cluster of 2 on one TPC, tcgen05 cta_group::2) owns four
-// 256-row query tiles of one (batch, KV head): tile u covers 2 x 128/G
-// consecutive positions, CTA r holding the second half's rows when r = 1.
-// Every K tile of 128 keys is split between the pair (64 keys per CTA), so
-// each SM fetches and reads from shared memory half of every K tile, and one
-// M = 256 MMA per query tile computes S for both SMs.  576 threads per CTA:
-// warp 0 TMA producer, warp 1 TMEM allocator and (leader only) the
-// single-thread MMA issuer, warps 2-17 four softmax warpgroups (one per query
-// tile, one thread per row = TMEM lane).  A query tile's 128 TMEM columns are
-// handed back to the issuer as soon as both CTAs have read them, so the tensor
-// core computes the next S of that tile while the warpgroups still sum
-// exponentials.  Per row, l = sum 2^(s*scale*log2e - ref) against a reference
-// that moves only when a chunk would overflow.
+// A CTA owns four 128-row query tiles of one (batch, KV head): tile u covers
+// 128/G consecutive positions (rows are (position, query head) pairs).  K
+// tiles of 128 keys stream through a ring; for each, one M = 128, N = 128 MMA
+// group per query tile writes S into that tile's 128 TMEM columns.  576
+// threads: warp 0 TMA producer, warp 1 TMEM allocator and single-thread MMA
+// issuer, warps 2-17 four softmax warpgroups (one per query tile, one thread
+// per row = TMEM lane).  A tile's columns go back to the issuer as soon as its
+// warps have read them, so the tensor core computes that tile's next S while
+// the warps still sum exponentials.  Per row, l = sum 2^(s*scale*log2e - ref)
+// against a reference that moves only when a chunk would overflow.
 #include "common.cuh"
 
 namespace kvpop {
 namespace {
 
-constexpr int kNQ = 4;  // query tiles per pair (128 rows of each in each CTA)
+constexpr int kNQ = 4;  // 128-row query tiles per CTA
 constexpr int kThreads = (2 + 4 * kNQ) * 32;
-constexpr int kKeys = 128;             // keys per K tile (64 in each CTA)
+constexpr int kKeys = 128;             // keys per K tile
 constexpr int kBlockBytes = 128 * 128;  // 128 rows x 128 bytes
-constexpr int kHalfBytes = 64 * 128;    // 64 key rows x 128 bytes
 
 struct LseParams {
-  CUtensorMap tq, tk;  // Q box 64 x G x P, K box 64 x 1 x 64 (half a K tile)
+  CUtensorMap tq, tk;  // Q box 64 x G x P, K box 64 x 1 x 128
   float* lse;
   int* status;
   int S, Hq, H, G, P, npb, nbh;
@@ -45,10 +41,10 @@ struct LBars {
 template <int D>
 struct LLayout {
   static constexpr int DH = D / 64;
-  static constexpr int NS = D == 128 ? 6 : 12;
+  static constexpr int NS = D == 128 ? 3 : 8;
   static constexpr int q_off = 0;
   static constexpr int k_off = q_off + kNQ * DH * kBlockBytes;
-  static constexpr int bar_off = k_off + NS * DH * kHalfBytes;
+  static constexpr int bar_off = k_off + NS * DH * kBlockBytes;
   static constexpr int misc_off = bar_off + (int)sizeof(LBars<NS>);
   static constexpr int total = misc_off + 64 + 1024;
   static_assert(total <= 232448, "shared memory");
@@ -57,7 +53,7 @@ struct LLayout {
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 
 template <int D>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     dense_lse_kernel(const __grid_constant__ LseParams p) {
   using L = LLayout<D>;
   constexpr int DH = L::DH;
@@ -70,20 +66,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t sbase = smem_u32(smem);
 
   const int warp = warp_id(), lane = lane_id();
-  const uint32_t rank = cluster_rank();
-  const bool leader = rank == 0;
   // heaviest query blocks first across all (batch, head) pairs
-  const int cid = (int)(blockIdx.x >> 1);
+  const int cid = (int)blockIdx.x;
   const int pblock = p.npb - 1 - cid / p.nbh;
   const int bh = cid % p.nbh;
   const int b = bh / p.H, h = bh % p.H;
   const int S = p.S, G = p.G, P = p.P;
-  const int qb0 = pblock * kNQ * 2 * P;
-  int nt[kNQ];  // K tiles each query tile needs (causal, up to the pair's last row)
+  const int qb0 = pblock * kNQ * P;
+  int nt[kNQ];  // K tiles each query tile needs (causal, up to the tile's last row)
 #pragma unroll
   for (int u = 0; u < kNQ; ++u) {
-    const int first = qb0 + u * 2 * P;
-    const int last = min(first + 2 * P, S) - 1;
+    const int first = qb0 + u * P;
+    const int last = min(first + P, S) - 1;
     nt[u] = last >= first ? last / kKeys + 1 : 0;
   }
   int NT = 0;
@@ -98,19 +92,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < kNQ; ++i) {
       mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->s_empty[i], 8);  // 4 warps in each CTA
+      mbar_init(&bars->s_empty[i], 4);  // the tile's four softmax warps
     }
     mbar_init(&bars->drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc_pair(tmem_slot, 512);
-    tmem_relinquish_pair();
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
   // the previous kernel of the stream may still be running (programmatic
@@ -124,36 +117,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   };
 
   if (warp == 0) {
-    // both CTAs load their own halves; completion counts on the leader's barriers
     if (lane == 0 && NT > 0) {
       tma_prefetch_desc(&p.tq);
       tma_prefetch_desc(&p.tk);
-      const uint32_t q_bar = cluster_addr(smem_u32(&bars->q_full), 0);
-      if (leader) mbar_arrive_expect_tx(&bars->q_full, 2 * kNQ * DH * kBlockBytes);
+      mbar_arrive_expect_tx(&bars->q_full, kNQ * DH * kBlockBytes);
       for (int u = 0; u < kNQ; ++u)
         for (int dh = 0; dh < DH; ++dh)
-          tma_load_4d_pair(smem + L::q_off + (u * DH + dh) * kBlockBytes, &p.tq, q_bar, dh * 64, h * G,
-                           qb0 + u * 2 * P + (int)rank * P, b);
+          tma_load_4d(smem + L::q_off + (u * DH + dh) * kBlockBytes, &p.tq, &bars->q_full, dh * 64, h * G,
+                      qb0 + u * P, b);
       for (int j = 0; j < NT; ++j) {
         const int st = j % NS;
         if (!mbar_wait(&bars->k_empty[st], ((j / NS) & 1) ^ 1, abort_flag)) {
           fail(SITE_ATTN_PRODUCER, 21);
           break;
         }
-        if (leader) mbar_arrive_expect_tx(&bars->k_full[st], 2 * DH * kHalfBytes);
-        const uint32_t k_bar = cluster_addr(smem_u32(&bars->k_full[st]), 0);
+        mbar_arrive_expect_tx(&bars->k_full[st], DH * kBlockBytes);
         for (int dh = 0; dh < DH; ++dh)
-          tma_load_4d_pair(smem + L::k_off + (st * DH + dh) * kHalfBytes, &p.tk, k_bar, dh * 64, h,
-                           j * kKeys + (int)rank * 64, b);
+          tma_load_4d(smem + L::k_off + (st * DH + dh) * kBlockBytes, &p.tk, &bars->k_full[st], dh * 64, h,
+                      j * kKeys, b);
       }
     }
   } else if (warp == 1) {
     if (lane == 0 && NT > 0) {
-      if (leader) {
+      {
         bool ok = mbar_wait(&bars->q_full, 0, abort_flag);
         if (!ok) fail(SITE_ATTN_MMA, 21);
         tc_fence_after();
-        constexpr uint32_t idesc = idesc_bf16(256, 128, 0);
+        constexpr uint32_t idesc = idesc_bf16(128, 128, 0);
         // descriptor low words stepped by constants: the issuing thread shares
         // its SMSP with four busy softmax warps, so every MMA costs few instructions
         const uint32_t q_lo = desc_lo(sbase + L::q_off, 16), k_lo = desc_lo(sbase + L::k_off, 16);
@@ -173,20 +163,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             const uint32_t a0 = q_lo + (uint32_t)(u * DH * kBlockBytes >> 4);
-            const uint32_t b0 = k_lo + (uint32_t)(st * DH * kHalfBytes >> 4);
+            const uint32_t b0 = k_lo + (uint32_t)(st * DH * kBlockBytes >> 4);
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks) {
-              const uint32_t w = (uint32_t)((ks & 3) * 32 >> 4);
-              mma_ss_pair_lo(tbase + 128 * u, a0 + (uint32_t)((ks >> 2) * kBlockBytes >> 4) + w,
-                             b0 + (uint32_t)((ks >> 2) * kHalfBytes >> 4) + w, idesc, ks > 0 ? 1u : 0u);
+              const uint32_t off = (uint32_t)(((ks >> 2) * kBlockBytes + (ks & 3) * 32) >> 4);
+              mma_ss_lo(tbase + 128 * u, a0 + off, b0 + off, idesc, ks > 0 ? 1u : 0u);
             }
-            mma_commit_pair(&bars->s_full[u]);
+            mma_commit(&bars->s_full[u]);
           }
-          mma_commit_pair(&bars->k_empty[st]);
+          mma_commit(&bars->k_empty[st]);
         }
-        mma_commit_pair(&bars->drain);
+        mma_commit(&bars->drain);
       }
-      // both CTAs: every pair MMA has finished with this CTA's memory
       mbar_wait(&bars->drain, 0, nullptr);
     }
   } else {
@@ -195,10 +183,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const int p_row = row / G, g = row - p_row * G;
-    const int q_first = qb0 + u * 2 * P + (int)rank * P;
+    const int q_first = qb0 + u * P;
     const int q = q_first + p_row;
     const uint32_t tl = tbase + ((uint32_t)(quarter * 32) << 16) + 128 * u;
-    const uint32_t empty_bar = cluster_addr(smem_u32(&bars->s_empty[u]), 0);
+
     const float sl2 = p.scale_log2;
     const uint64_t s2 = pack2(sl2, sl2);
     float m_ref = neg_inf(), l = 0.0f;
@@ -224,7 +212,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         } else {  // every column of this tile is in registers: hand TMEM back
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(empty_bar);
+          if (lane == 0) mbar_arrive(&bars->s_empty[u]);
         }
         if (diag) {
           const int t0 = j * kKeys + ch * 32;
@@ -252,13 +240,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           l > 0.0f ? (m_ref * sl2 + __log2f(l)) * 0.69314718055994531f : neg_inf();
   }
 
-  // neither CTA releases its tensor or shared memory while the pair still works
   tc_fence_before();
   __syncthreads();
-  cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc_pair(tbase, 512);
+    tmem_dealloc(tbase, 512);
   }
 }
 
@@ -270,7 +256,7 @@ kvpop_status launch_d(const LseParams& prm, cudaStream_t cs) {
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::total),
       "dense LSE: smem attribute");
   if (st != KVPOP_OK) return st;
-  return cuda_check(launch_pdl(kern, dim3(2 * prm.npb * prm.nbh), dim3(kThreads), L::total, cs, prm),
+  return cuda_check(launch_pdl(kern, dim3(prm.npb * prm.nbh), dim3(kThreads), L::total, cs, prm),
                     "dense LSE: launch");
 }
 
@@ -287,7 +273,7 @@ kvpop_status launch_dense_lse(const void* q, const void* k, int b, int S, int Hq
   uint32_t bq[4] = {64, (uint32_t)G, (uint32_t)P, 1};
   uint64_t dk[4] = {(uint64_t)D, (uint64_t)H, (uint64_t)S, (uint64_t)b};
   uint64_t sk[3] = {(uint64_t)D * 2, (uint64_t)H * D * 2, (uint64_t)S * H * D * 2};
-  uint32_t bk[4] = {64, 1, 64, 1};
+  uint32_t bk[4] = {64, 1, 128, 1};
   if (!make_tmap_4d(&prm.tq, q, dq, sq, bq) || !make_tmap_4d(&prm.tk, k, dk, sk, bk)) return KVPOP_ERR_CUDA;
   prm.lse = lse;
   prm.status = device_status_ptr();
@@ -296,10 +282,10 @@ kvpop_status launch_dense_lse(const void* q, const void* k, int b, int S, int Hq
   prm.H = H;
   prm.G = G;
   prm.P = P;
-  prm.npb = (S + kNQ * 2 * P - 1) / (kNQ * 2 * P);
+  prm.npb = (S + kNQ * P - 1) / (kNQ * P);
   prm.nbh = b * H;
   prm.scale_log2 = scale_log2;
-  if (2LL * prm.npb * prm.nbh > 0x7fffffffLL) {
+  if ((long long)prm.npb * prm.nbh > 0x7fffffffLL) {
     set_last_error("dense LSE: grid too large");
     return KVPOP_ERR_UNSUPPORTED;
   }
