@@ -267,6 +267,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           return true;
         };
         PItem x = make_pitem(p, it0);
+        int NTn = it0 + dit < p.nitems ? make_pitem(p, it0 + dit).NT : 0;  // next item's tiles, once per item
         bool ok = wait_bar(&bars->k_full[0], 0, 2);
         for (int u = 0; u < 2 && ok; ++u) {
           ok = wait_bar(&bars->q_full[u], 0, 1);
@@ -282,9 +283,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int st = t % kNS;
             const uint32_t ph = (t / kNS) & 1;
             const bool last = j + 1 == x.NT;
-            const int it1 = last ? it + dit : it;
-            const bool has_next = it1 < p.nitems;
-            const int NT1 = last ? (has_next ? make_pitem(p, it1).NT : 0) : x.NT;
+            const bool has_next = !last || it + dit < p.nitems;
+            const int NT1 = last ? NTn : x.NT;
             const int j1 = last ? 0 : j + 1;
             const int n1 = last ? n + 1 : n;
             const int st1 = (t + 1) % kNS;
@@ -316,6 +316,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           ++n;
           if (it >= p.nitems) break;
           x = make_pitem(p, it);
+          NTn = it + dit < p.nitems ? make_pitem(p, it + dit).NT : 0;
         }
         mma_commit_pair(&bars->drain);
       }
