@@ -56,7 +56,7 @@ struct PairParams {
 
 struct PBars {
   uint64_t q_full[2], q_empty[2];
-  uint64_t k_full[kNS], k_empty[kNS], v_full[kNS], v_empty[kNS];
+  uint64_t k_full[kNS], k_empty[kNS], v_full[kNS];  // a V stage is freed by a K-stage commit
   uint64_t s_full[2], p_full[2];
   uint64_t o_full[2], o_empty[2];
   uint64_t meta_full[kMetaStages], meta_empty[kMetaStages];
@@ -135,7 +135,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&bars->k_full[i], 1);
       mbar_init(&bars->v_full[i], 1);
       mbar_init(&bars->k_empty[i], 1);
-      mbar_init(&bars->v_empty[i], 1);
     }
     for (int i = 0; i < kMetaStages; ++i) {
       mbar_init(&bars->meta_full[i], 1);
@@ -299,7 +298,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 mma_ts_pair(tbase + 256 + 128 * u, tbase + 128 * u + ks * 8, bd, idesc_pv,
                             (j > 0 || ks > 0) ? 1u : 0u);
               }
-              if (u == 1) mma_commit_pair(&bars->v_empty[st]);
               if (last) mma_commit_pair(&bars->o_full[u]);
               if (has_next) {
                 if (j1 == 0 && !(ok = wait_bar(&bars->q_full[u], n1 & 1, 1))) break;
@@ -326,7 +324,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // ---------------------------------------------------------- loaders: warp 2 K, warp 3 V
       const bool is_v = warp == 3;
       uint64_t* full = is_v ? bars->v_full : bars->k_full;
-      uint64_t* empty = is_v ? bars->v_empty : bars->k_empty;
+      uint64_t* empty = bars->k_empty;
       const int tile_bytes = 2 * 2 * kKHalf;  // both CTAs: 2 x 8 KB per dim half (K) or 2 x 16 KB (V)
       if (lane == 0 && !is_v) tma_prefetch_desc(&p.tq);
       bool ok = true;
@@ -346,7 +344,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          if (!warp_wait(&empty[st], ph ^ 1, abort_flag)) {
+          bool free_ok = true;
+          if (!is_v) {
+            free_ok = warp_wait(&empty[st], ph ^ 1, abort_flag);
+          } else if (t >= kNS) {
+            // V stage of tile t - kNS: its PVs ran before tile t - kNS + 1's S, whose
+            // K-stage commit therefore frees it too
+            const int tn = t - kNS + 1;
+            free_ok = warp_wait(&bars->k_empty[tn % kNS], (tn / kNS) & 1, abort_flag);
+          }
+          if (!free_ok) {
             if (lane == 0) fail(SITE_ATTN_PRODUCER, 4);
             ok = false;
             break;
