@@ -444,14 +444,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int ch = 0; ch < 4; ++ch) tmem_ld32(tl + s_col + ch * 32, sr[ch]);
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) tmem_wait_ld_dep(sr[ch]);
+        if (G == 4) {
+          // the layers this kernel is tuned for: a warp's 32 rows hold 8 positions
+          // (4 heads each); lane l tests key 32 ch + l against each of them, one
+          // ballot per position, and keeps the word of its own position, whose bit c
+          // says whether key 32 ch + c is visible (two bit operations per element
+          // instead of a metadata load and two compares)
+          const int qw = q_first + quarter * 8;  // this warp's first position
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          const int2 sum = km[kKeys + ch];
-          if (!(q >= sum.x && q < sum.y)) {
+          for (int ch = 0; ch < 4; ++ch) {
+            const int2 sum = km[kKeys + ch];
+            if (__any_sync(0xffffffffu, !(q >= sum.x && q < sum.y))) {
+              const int2 e = km[ch * 32 + lane];
+              uint32_t mw = 0;
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              const int2 e = km[ch * 32 + c];
-              if (!(e.x <= q && q < e.y)) sr[ch][c] = 0xff800000u;
+              for (int i = 0; i < 8; ++i) {
+                const int qi = qw + i;
+                const uint32_t w = __ballot_sync(0xffffffffu, e.x <= qi && qi < e.y);
+                mw = (lane >> 2) == i ? w : mw;
+              }
+              if (mw != 0xffffffffu) {
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                  const uint32_t keep = (uint32_t)((int32_t)(mw << (31 - c)) >> 31);
+                  sr[ch][c] = (sr[ch][c] & keep) | (0xff800000u & ~keep);
+                }
+              }
+            }
+          }
+        } else {
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            const int2 sum = km[kKeys + ch];
+            if (!(q >= sum.x && q < sum.y)) {
+#pragma unroll
+              for (int c = 0; c < 32; ++c) {
+                const int2 e = km[ch * 32 + c];
+                if (!(e.x <= q && q < e.y)) sr[ch][c] = 0xff800000u;
+              }
             }
           }
         }
