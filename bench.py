@@ -39,9 +39,9 @@ LAUNCHES_DECODE_STEP = 2
 # kernels as they stand, per workload; None where no capture of the current
 # kernel exists.  decode: update + attention of one step.
 TRAFFIC_BYTES = {
-    "long-context-prefill": {"sparse_attn": 2.89e9, "dense_lse": 11.807e9, "future_target": 27.048e9},
-    "qwen3-4b-layer-prefill": {"sparse_attn": 309.77e6, "dense_lse": 172.47e6, "future_target": 169.48e6},
-    "qwen3-8b-layer-prefill": {"sparse_attn": 768.66e6, "dense_lse": 512.03e6, "future_target": 325.99e6},
+    "long-context-prefill": {"sparse_attn": 2.887e9, "dense_lse": 11.807e9, "future_target": 27.048e9},
+    "qwen3-4b-layer-prefill": {"sparse_attn": 309.92e6, "dense_lse": 172.47e6, "future_target": 169.48e6},
+    "qwen3-8b-layer-prefill": {"sparse_attn": 759.50e6, "dense_lse": 512.03e6, "future_target": 325.99e6},
     "fixed-budget-decode": {"decode": 558.19e6},
 }
 OTHER_WORKLOADS = ("qwen3-4b-layer-prefill", "qwen3-8b-layer-prefill")
