@@ -448,8 +448,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // the layers this kernel is tuned for: a warp's 32 rows hold 8 positions
           // (4 heads each); lane l tests key 32 ch + l against each of them, one
           // ballot per position, and keeps the word of its own position, whose bit c
-          // says whether key 32 ch + c is visible (two bit operations per element
-          // instead of a metadata load and two compares)
+          // says whether key 32 ch + c is visible (a bit test per element instead
+          // of a metadata load and two compares)
           const int qw = q_first + quarter * 8;  // this warp's first position
 #pragma unroll
           for (int ch = 0; ch < 4; ++ch) {
@@ -466,8 +466,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               if (mw != 0xffffffffu) {
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
-                  const uint32_t keep = (uint32_t)((int32_t)(mw << (31 - c)) >> 31);
-                  sr[ch][c] = (sr[ch][c] & keep) | (0xff800000u & ~keep);
+                  if (!(mw & (1u << c))) sr[ch][c] = 0xff800000u;
                 }
               }
             }
