@@ -57,6 +57,7 @@ static_assert(kRows % KVPOP_LIST_QBLOCK == 0 && kRows % 128 == 0, "block of rows
 
 struct BwdParams {
   CUtensorMap tq, tdo, tk, tv;  // 4-D tiles: q/dO box {64, G, P, 1}; k/v box {64, 1, 128, 1}
+  CUtensorMap tk64, tv64;       // k/v box {64, 1, 64, 1} (half a key tile)
   CUtensorMap tkr, tvr;         // K, V as [b*S*H rows, D] with one-row boxes (gather4)
   const int32_t* evict_at;
   const int2* lists;
@@ -70,7 +71,7 @@ struct BwdParams {
   int* status;
   int S, Spad, Hq, H, G, gshift, P, nb;
   int s, w, kk, nL;
-  int nqt, nblk, cap, ctiles;
+  int nqt, nqt2, nblk, cap, ctiles;  // nqt2: 256-row query tiles (CTA pairs)
   int nitems;
   float scale, scale_log2;
 };
@@ -219,15 +220,17 @@ struct DqItem {
   const int2* list;
 };
 
-__device__ __forceinline__ DqItem make_dq_item(const BwdParams& p, int it) {
+// pair: a 256-row query tile (2P positions) of the CTA-pair kernel
+__device__ __forceinline__ DqItem make_dq_item(const BwdParams& p, int it, bool pair = false) {
   DqItem x;
   const int nbh = p.H * p.nb;
   const int rank = it / nbh, rem = it - rank * nbh;
   x.h = rem % p.H;
   x.b = rem / p.H;
-  const int qt = p.nqt - 1 - rank;  // latest tiles first: they hold the full budget
-  x.q0 = qt * p.P;
-  x.q1 = min(x.q0 + p.P, p.S) - 1;
+  const int span = pair ? 2 * p.P : p.P;
+  const int qt = (pair ? p.nqt2 : p.nqt) - 1 - rank;  // latest tiles first: they hold the full budget
+  x.q0 = qt * span;
+  x.q1 = min(x.q0 + span, p.S) - 1;
   const int jl = x.q0 / KVPOP_LIST_QBLOCK;
   const int q0l = jl * KVPOP_LIST_QBLOCK;
   x.n_sink = min(p.s, x.q1 + 1);
@@ -696,6 +699,503 @@ __global__ void __launch_bounds__(kDqThreads, 1) bwd_dq_kernel(const __grid_cons
     tmem_dealloc(tbase, 512);
   }
 }
+
+// ---------------------------------------------------------------------------
+// bwd_dq_pair_kernel: query-major dQ on CTA pairs (D = 128)
+// ---------------------------------------------------------------------------
+// The dQ kernel above laid out for two SMs (tcgen05 cta_group::2), like the
+// sparse forward: an item is one 256-row query tile (2P positions), CTA r
+// holding rows 128 r .. 128 r + 127, and every M = 256 MMA, issued by the
+// leader, spans both SMs -- half the MMA instructions per row, which is what
+// bounds the single-CTA kernel (its one issuing thread).  K is the B operand of
+// S = Q K^T (N = keys, split by keys: CTA r supplies keys 64 r .. 64 r + 63)
+// and of dQ += dS K (N = dims, split by dims: CTA r supplies dims 64 r .. of
+// all 128 keys), so each CTA keeps two views of every K tile at offsets that
+// match across the pair: an S view [dh][64 keys] and a dQ view [128 keys] of
+// its 64 dims (the 8 KB both contain are fetched twice); V, the B operand of
+// dP = dO V^T (N = keys), only its S view.  Per tile each SM gathers 48 KB for
+// its 128 rows (64 KB in the single-CTA kernel).  Loads of both CTAs complete
+// on the leader's barriers, MMA commits arrive on both CTAs' barriers, and the
+// elementwise warps of both CTAs arrive on the leader's barriers.
+constexpr int kViewBytes = 64 * 128;  // 64 key rows x 128 bytes
+constexpr int kPairKOps = 64;         // gather4 ops per K tile and CTA: S view 32, dQ view 32
+constexpr int kPairVOps = 32;         // gather4 ops per V tile and CTA: S view
+constexpr int kPairKPer = (kPairKOps + 2) / 3;
+constexpr int kPairVPer = (kPairVOps + 2) / 3;
+
+struct DqPairLayout {
+  static constexpr int NSK = 3, NSV = 2;
+  static constexpr int k_stage = 4 * kViewBytes;  // S view (2 x 8 KB), then dQ view (16 KB)
+  static constexpr int v_stage = 2 * kViewBytes;  // S view
+  static constexpr int q_off = 0;
+  static constexpr int do_off = q_off + 2 * kBlockBytes;
+  static constexpr int k_off = do_off + 2 * kBlockBytes;
+  static constexpr int v_off = k_off + NSK * k_stage;
+  static constexpr int meta_off = v_off + NSV * v_stage;
+  static constexpr int meta_bytes = kDqMetaStages * (kKeys + 4) * 8;
+  static constexpr int bar_off = meta_off + meta_bytes;
+  static constexpr int misc_off = bar_off + (int)sizeof(DqBars<NSK, NSV>);
+  static constexpr int total = misc_off + 64 + 1024;
+  static_assert(total <= 232448, "shared memory");
+};
+
+// Roles as in the single-CTA kernel (warp 0 key metadata, warp 1 TMEM and --
+// leader only -- the MMA issuer, warps 2/3 Q and K / dO and V with warps 12-15
+// helping with the gathers, warps 4-11 elementwise on this CTA's 128 rows).
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDqThreads, 1)
+    bwd_dq_pair_kernel(const __grid_constant__ BwdParams p) {
+  constexpr int D = 128;
+  using L = DqPairLayout;
+  constexpr int NSK = L::NSK, NSV = L::NSV;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  DqBars<NSK, NSV>* bars = reinterpret_cast<DqBars<NSK, NSV>*>(smem + L::bar_off);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::misc_off);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::misc_off + 4);
+  int2* meta = reinterpret_cast<int2*>(smem + L::meta_off);
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = warp_id(), lane = lane_id();
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+  const int S = p.S, G = p.G, P = p.P;
+  const int it0 = (int)(blockIdx.x >> 1), dit = (int)(gridDim.x >> 1);
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 2);  // the leader's Q and dO loader warps, for both CTAs' bytes
+    mbar_init(&bars->q_empty, 1);
+    for (int i = 0; i < NSK; ++i) {
+      mbar_init(&bars->k_full[i], 1);
+      mbar_init(&bars->k_empty[i], 1);
+    }
+    for (int i = 0; i < NSV; ++i) {
+      mbar_init(&bars->v_full[i], 1);
+      mbar_init(&bars->v_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->s_full[i], 1);
+      mbar_init(&bars->ds_full[i], 16);  // 8 elementwise warps in each CTA
+    }
+    mbar_init(&bars->dp_empty, 16);
+    mbar_init(&bars->o_full, 1);
+    mbar_init(&bars->o_empty, 16);
+    for (int i = 0; i < kDqMetaStages; ++i) {
+      mbar_init(&bars->meta_full[i], 1);
+      mbar_init(&bars->meta_empty[i], 8);  // this CTA's elementwise warps
+    }
+    mbar_init(&bars->drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, 512);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  grid_dep_wait();
+  grid_dep_launch();
+
+  auto fail = [&](int site, int detail) {
+    report_error(p.status, KVPOP_ERR_TIMEOUT, site, detail);
+    *abort_flag = 1;
+  };
+  auto leader_bar = [&](uint64_t* bar) { return cluster_addr(smem_u32(bar), 0); };
+  const uint32_t q_addr = sbase + L::q_off;
+  const uint32_t do_addr = sbase + L::do_off;
+  const uint32_t k_addr = sbase + L::k_off;
+  const uint32_t v_addr = sbase + L::v_off;
+  const int r64 = 64 * (int)rank;
+  // gather4 op o of a gathered K (is_v false) or V tile: four key rows of 128
+  // bytes.  K: o < 32 the S view (dims half o / 16, keys r64 + 4 (o % 16) ..),
+  // o >= 32 the dQ view (this CTA's dims half, keys 4 (o - 32) ..).  V: the S view.
+  auto op_target = [&](bool is_v, int o, int& key0, int& xcoord, int& dst) {
+    if (is_v || o < 32) {
+      const int dh = o >> 4, g4 = o & 15;
+      key0 = r64 + 4 * g4;
+      xcoord = dh * 64;
+      dst = (is_v ? L::v_off : L::k_off) + dh * kViewBytes + g4 * 512;
+    } else {
+      const int g4 = o - 32;
+      key0 = 4 * g4;
+      xcoord = r64;
+      dst = L::k_off + 2 * kViewBytes + g4 * 512;
+    }
+  };
+  // rows of op o's four keys, read from the item's list before the stage is free
+  auto gather_rows = [&](bool is_v, int o, const DqItem& x, int j, int row_base, int (&rows)[4]) {
+    int key0, xc, dst;
+    op_target(is_v, o, key0, xc, dst);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int pos = dq_gather_pos(x, j * kKeys + key0 + u, S);
+      rows[u] = pos >= 0 ? row_base + pos * p.H : row_base;  // padding: any row, masked
+    }
+  };
+  auto issue_gather = [&](bool is_v, int o, int st, const int (&rows)[4], uint32_t bar) {
+    int key0, xc, dst;
+    op_target(is_v, o, key0, xc, dst);
+    tma_gather4_pair(smem + dst + st * (is_v ? L::v_stage : L::k_stage), is_v ? &p.tvr : &p.tkr, bar, xc, rows[0],
+                     rows[1], rows[2], rows[3]);
+  };
+
+  if (warp >= 12) {
+    setmaxnreg_dec<kDqRegsHelp>();
+    // ---------------------------------------------------------- gather helpers
+    const bool is_v = warp >= 14;
+    const int part = 1 + (warp & 1);  // issuer 0 is the loader warp itself
+    const int per = is_v ? kPairVPer : kPairKPer;
+    const int nops = is_v ? kPairVOps : kPairKOps;
+    uint64_t* full = is_v ? bars->v_full : bars->k_full;
+    uint64_t* empty = is_v ? bars->v_empty : bars->k_empty;
+    const int ns = is_v ? NSV : NSK;
+    const int first = part * per;
+    const int count = min(per, nops - first);
+    bool ok = true;
+    int t = 0;
+    for (int it = it0; ok && it < p.nitems; it += dit) {
+      const DqItem x = make_dq_item(p, it, true);
+      const int row_base = x.b * S * p.H + x.h;
+      for (int j = 0; j < x.NT; ++j, ++t) {
+        const int st = t % ns;
+        int rows[4];
+        if (j < x.NTg && lane < count) gather_rows(is_v, first + lane, x, j, row_base, rows);
+        // every tile, gathered or not: a parity wait is only exact while the
+        // waiter is at most one phase ahead of the barrier
+        if (!warp_wait(&empty[st], ((t / ns) & 1) ^ 1, abort_flag)) {
+          if (lane == 0) fail(SITE_ATTN_PRODUCER, 43);
+          ok = false;
+          break;
+        }
+        if (j < x.NTg && lane < count) issue_gather(is_v, first + lane, st, rows, leader_bar(&full[st]));
+        __syncwarp();
+      }
+    }
+  } else if (warp < 4) {
+    setmaxnreg_dec<kDqRegsIo>();
+    if (warp == 0) {
+      // ---------------------------------------------------------- key metadata (this CTA's masks)
+      bool ok = true;
+      int t = 0;
+      for (int it = it0; ok && it < p.nitems; it += dit) {
+        const DqItem x = make_dq_item(p, it, true);
+        const int32_t* ev = p.evict_at + (size_t)(x.b * p.H + x.h) * S;
+        auto load_tile = [&](int j, int2 (&e)[4]) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int r = lane + 32 * c;
+            e[c] = make_int2(0x7fffffff, 0);  // padding: never visible
+            if (j < x.NTg) {
+              const int i = j * kKeys + r;
+              if (i < x.n_sink) e[c] = make_int2(i, S);
+              else if (i < x.n_sl) e[c] = __ldg(x.list + (i - x.n_sink));
+            } else {
+              const int pos = x.sp0 + (j - x.NTg) * kKeys + r;
+              if (pos <= x.q1) e[c] = make_int2(pos, __ldg(ev + pos));
+            }
+          }
+        };
+        int2 cur_e[4], nxt_e[4];
+        load_tile(0, cur_e);
+        for (int j = 0; j < x.NT; ++j, ++t) {
+          const int ms = t % kDqMetaStages;
+          if (j + 1 < x.NT) load_tile(j + 1, nxt_e);
+          if (!warp_wait(&bars->meta_empty[ms], ((t / kDqMetaStages) & 1) ^ 1, abort_flag)) {
+            if (lane == 0) fail(SITE_ATTN_PRODUCER, 31);
+            ok = false;
+            break;
+          }
+          int2* m = meta + ms * (kKeys + 4);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int r = lane + 32 * c;
+            int2 e = cur_e[c];
+            if (e.x != 0x7fffffff && (e.x < 0 || e.x >= S)) {  // a corrupt list entry: never gathered
+              report_error(p.status, KVPOP_ERR_INTERNAL, SITE_INTERNAL_CHECK, 11);
+              e = make_int2(0x7fffffff, 0);
+            }
+            m[r] = e;
+            int lo = e.x, hi = e.y;  // rows in [lo, hi) see every key of the chunk
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+              lo = max(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+              hi = min(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+            }
+            if (lane == 0) m[kKeys + c] = make_int2(lo, hi);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->meta_full[ms]);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) cur_e[c] = nxt_e[c];
+        }
+      }
+    } else if (warp == 1) {
+      // ---------------------------------------------------------- MMA issuer (leader)
+      // TMEM of both CTAs: S of key tile t at 128 (t & 1), dP at 256, dQ at 384
+      if (lane == 0 && leader && it0 < p.nitems) {
+        constexpr uint32_t idesc_s = idesc_bf16(256, 128, 0);
+        constexpr uint32_t idesc_dq = idesc_bf16(256, D, 1);
+        // A B^T over D: A a 128-row block pair per CTA ([dh][128 rows]), B an S view
+        // ([dh][64 keys]); descriptor low words stepped by constants
+        auto issue_nt = [&](uint32_t a_lo, uint32_t b_lo, uint32_t d) {
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t w = (uint32_t)((ks & 3) * 32 >> 4);
+            mma_ss_pair_lo(d, a_lo + (uint32_t)((ks >> 2) * kBlockBytes >> 4) + w,
+                           b_lo + (uint32_t)((ks >> 2) * kViewBytes >> 4) + w, idesc_s, ks > 0 ? 1u : 0u);
+          }
+        };
+        const uint32_t q_lo = desc_lo(q_addr, 16), do_lo = desc_lo(do_addr, 16);
+        const uint32_t k_lo = desc_lo(k_addr, 16), v_lo = desc_lo(v_addr, 16);
+        const uint32_t kq_lo = desc_lo(k_addr + 2 * kViewBytes, kBlockBytes);  // the dQ views, MN-major
+        auto wait_bar = [&](uint64_t* bar, uint32_t ph, int detail) -> bool {
+          if (!mbar_wait(bar, ph, abort_flag)) {
+            fail(SITE_ATTN_MMA, detail);
+            return false;
+          }
+          tc_fence_after();
+          return true;
+        };
+        // S_t and dP_t of global tile t; item counter n
+        auto issue_sdp = [&](int t, bool first_of_item, int n) -> bool {
+          const int kst = t % NSK, vst = t % NSV;
+          if (first_of_item && !wait_bar(&bars->q_full, n & 1, 31)) return false;
+          if (!wait_bar(&bars->k_full[kst], (t / NSK) & 1, 32)) return false;
+          issue_nt(q_lo, k_lo + (uint32_t)(kst * L::k_stage >> 4), tbase + 128u * (uint32_t)(t & 1));
+          if (t > 0 && !wait_bar(&bars->dp_empty, (t - 1) & 1, 33)) return false;
+          if (!wait_bar(&bars->v_full[vst], (t / NSV) & 1, 34)) return false;
+          issue_nt(do_lo, v_lo + (uint32_t)(vst * L::v_stage >> 4), tbase + 256u);
+          mma_commit_pair(&bars->s_full[t & 1]);
+          mma_commit_pair(&bars->v_empty[vst]);
+          return true;
+        };
+        DqItem x = make_dq_item(p, it0, true);
+        int NTn = it0 + dit < p.nitems ? make_dq_item(p, it0 + dit, true).NT : 0;  // once per item
+        bool ok = issue_sdp(0, true, 0);
+        if (ok && x.NT == 1) mma_commit_pair(&bars->q_empty);
+        int t = 0, n = 0;
+        for (int it = it0; ok;) {
+          for (int j = 0; ok && j < x.NT; ++j, ++t) {
+            const int st = t % NSK;
+            const bool last = j + 1 == x.NT;
+            if (!last || NTn > 0) {
+              const int NT1 = last ? NTn : x.NT;
+              const int j1 = last ? 0 : j + 1;
+              if (!(ok = issue_sdp(t + 1, j1 == 0, last ? n + 1 : n))) break;
+              if (j1 == NT1 - 1) mma_commit_pair(&bars->q_empty);  // every S and dP of that item issued
+            }
+            if (!(ok = wait_bar(&bars->ds_full[t & 1], (t >> 1) & 1, 35))) break;
+            if (j == 0 && !(ok = wait_bar(&bars->o_empty, (n & 1) ^ 1, 36))) break;
+            const uint32_t b0 = kq_lo + (uint32_t)(st * L::k_stage >> 4);
+            const uint32_t a0 = tbase + 128u * (uint32_t)(t & 1);
+            const uint32_t acc0 = j > 0 ? 1u : 0u;
+#pragma unroll
+            for (int ks = 0; ks < kKeys / 16; ++ks) {
+              // dS of keys 16 ks .. 16 ks + 15: warpgroup ks / 4 packed them over its own S columns
+              mma_ts_pair_lo(tbase + 384, a0 + (uint32_t)(64 * (ks >> 2) + 8 * (ks & 3)),
+                             b0 + (uint32_t)(ks * 2048 >> 4), idesc_dq, ks > 0 ? 1u : acc0);
+            }
+            mma_commit_pair(&bars->k_empty[st]);
+            if (last) mma_commit_pair(&bars->o_full);
+          }
+          if (!ok) break;
+          it += dit;
+          ++n;
+          if (it >= p.nitems) break;
+          x = make_dq_item(p, it, true);
+          NTn = it + dit < p.nitems ? make_dq_item(p, it + dit, true).NT : 0;
+        }
+        mma_commit_pair(&bars->drain);
+      }
+      // both CTAs: every pair MMA is done with this CTA's memory before teardown
+      if (lane == 0 && it0 < p.nitems) mbar_wait(&bars->drain, 0, nullptr);
+    } else {
+      // ---------------------------------------------------------- loaders: warp 2 Q and K, warp 3 dO and V
+      const bool is_v = warp == 3;
+      const CUtensorMap* qmap = is_v ? &p.tdo : &p.tq;
+      uint64_t* full = is_v ? bars->v_full : bars->k_full;
+      uint64_t* empty = is_v ? bars->v_empty : bars->k_empty;
+      const int qoff = is_v ? L::do_off : L::q_off;
+      const int ns = is_v ? NSV : NSK;
+      const int per = is_v ? kPairVPer : kPairKPer;
+      // bytes per tile of both CTAs, counted on the leader's barrier
+      const uint32_t tile_bytes = 2u * (uint32_t)(is_v ? L::v_stage : L::k_stage);
+      if (lane == 0) tma_prefetch_desc(qmap);
+      bool ok = true;
+      int t = 0, n = 0;
+      for (int it = it0; ok && it < p.nitems; it += dit, ++n) {
+        const DqItem x = make_dq_item(p, it, true);
+        if (lane == 0) {
+          ok = mbar_wait(&bars->q_empty, (n & 1) ^ 1, abort_flag);
+          if (!ok) {
+            fail(SITE_ATTN_PRODUCER, 37);
+          } else {
+            if (leader) mbar_arrive_expect_tx(&bars->q_full, 2 * 2 * kBlockBytes);
+            const uint32_t qb = leader_bar(&bars->q_full);
+            for (int dh = 0; dh < 2; ++dh)
+              tma_load_4d_pair(smem + qoff + dh * kBlockBytes, qmap, qb, dh * 64, x.h * G, x.q0 + (int)rank * P, x.b);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        const int row_base = x.b * S * p.H + x.h;  // row of position t is row_base + t * H
+        for (int j = 0; j < x.NT; ++j, ++t) {
+          const int st = t % ns;
+          const uint32_t ph = (t / ns) & 1;
+          int rows[4];
+          if (j < x.NTg && lane < per) gather_rows(is_v, lane, x, j, row_base, rows);
+          if (!warp_wait(&empty[st], ph ^ 1, abort_flag)) {
+            if (lane == 0) fail(SITE_ATTN_PRODUCER, 39);
+            ok = false;
+            break;
+          }
+          if (lane == 0 && leader) mbar_arrive_expect_tx(&full[st], tile_bytes);
+          __syncwarp();
+          const uint32_t fb = leader_bar(&full[st]);
+          if (j < x.NTg) {
+            // the first third of the tile's gather4 ops; warps 12-15 issue the rest
+            if (lane < per) issue_gather(is_v, lane, st, rows, fb);
+          } else if (lane == 0) {
+            const int span_row = x.sp0 + (j - x.NTg) * kKeys;
+            if (!is_v) {
+              for (int dh = 0; dh < 2; ++dh)
+                tma_load_4d_pair(smem + L::k_off + st * L::k_stage + dh * kViewBytes, &p.tk64, fb, dh * 64, x.h,
+                                 span_row + r64, x.b);
+              tma_load_4d_pair(smem + L::k_off + st * L::k_stage + 2 * kViewBytes, &p.tk, fb, r64, x.h, span_row,
+                               x.b);
+            } else {
+              for (int dh = 0; dh < 2; ++dh)
+                tma_load_4d_pair(smem + L::v_off + st * L::v_stage + dh * kViewBytes, &p.tv64, fb, dh * 64, x.h,
+                                 span_row + r64, x.b);
+            }
+          }
+          __syncwarp();
+        }
+      }
+    }
+  } else {
+    setmaxnreg_inc<kDqRegsEw>();
+    // ------------------------------------------------------------ elementwise
+    const int wg = (warp - 4) >> 2;  // key half of each tile
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const int p_row = row >> p.gshift, g = row - (p_row << p.gshift);
+    const uint32_t tl = tbase + ((uint32_t)(quarter * 32) << 16);
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    int t = 0, n = 0;
+    for (int it = it0; ok && it < p.nitems; it += dit, ++n) {
+      const DqItem x = make_dq_item(p, it, true);
+      const int qc = x.q0 + (int)rank * P;  // this CTA's first position
+      const int q = qc + p_row;
+      const size_t ro = ((size_t)(x.b * p.H + x.h) * p.Spad + qc) * G + row;
+      const float nl2 = __ldg(p.nlse2 + ro);
+      const float nd = __ldg(p.ndelta + ro);
+      const uint64_t s2 = pack2(sl2, sl2), n2 = pack2(nl2, nl2), nd2 = pack2(nd, nd), zero2 = pack2(0.0f, 0.0f);
+      for (int j = 0; j < x.NT; ++j, ++t) {
+        const int sb = t & 1;
+        if (!warp_wait(&bars->s_full[sb], (t >> 1) & 1, abort_flag)) {
+          if (lane == 0) fail(SITE_ATTN_SOFTMAX, 31);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int ms = t % kDqMetaStages;
+        if (!warp_wait(&bars->meta_full[ms], (t / kDqMetaStages) & 1, abort_flag)) {
+          if (lane == 0) fail(SITE_ATTN_SOFTMAX, 32);
+          ok = false;
+          break;
+        }
+        const int2* km = meta + ms * (kKeys + 4);
+        uint32_t sr[2][32], dr[2][32];
+        tmem_ld32(tl + 128 * sb + 64 * wg, sr[0]);
+        tmem_ld32(tl + 128 * sb + 64 * wg + 32, sr[1]);
+        tmem_ld32(tl + 256 + 64 * wg, dr[0]);
+        tmem_ld32(tl + 256 + 64 * wg + 32, dr[1]);
+        tmem_wait_ld_dep(sr[0]);
+        tmem_wait_ld_dep(sr[1]);
+        tmem_wait_ld_dep(dr[0]);
+        tmem_wait_ld_dep(dr[1]);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(leader_bar(&bars->dp_empty));  // the next dP may overwrite its columns
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {
+          const int c32 = 2 * wg + ch;
+          const int2 sum = km[kKeys + c32];
+          if (!(q >= sum.x && q < sum.y)) {  // some key of the chunk is not visible from this row
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              const int2 e = km[c32 * 32 + c];
+              if (!(e.x <= q && q < e.y)) sr[ch][c] = 0xff800000u;
+            }
+          }
+          // P = exp2(s scale_log2 - LSE2), dS = P (dP - Delta), packed in pairs
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            float e0, e1;
+            unpack2(fma2(pack2(__uint_as_float(sr[ch][c]), __uint_as_float(sr[ch][c + 1])), s2, n2), e0, e1);
+            const uint64_t pp = pack2(ex2_approx(e0), ex2_approx(e1));
+            const uint64_t dd = add2(pack2(__uint_as_float(dr[ch][c]), __uint_as_float(dr[ch][c + 1])), nd2);
+            float d0, d1;
+            unpack2(fma2(pp, dd, zero2), d0, d1);
+            pk[c >> 1] = pack_bf16x2(d0, d1);
+          }
+          tmem_st16(tl + 128 * sb + 64 * wg + 16 * ch, pk);  // over this warpgroup's own S columns
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_cluster(leader_bar(&bars->ds_full[sb]));
+          mbar_arrive(&bars->meta_empty[ms]);
+        }
+      }
+      if (!ok) break;
+      // epilogue: this warpgroup's half of the dQ columns, scaled
+      if (!warp_wait(&bars->o_full, n & 1, abort_flag)) {
+        if (lane == 0) fail(SITE_ATTN_EPILOGUE, 31);
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      constexpr int HC = D / 2;  // columns per warpgroup
+      uint32_t acc[HC];
+#pragma unroll
+      for (int cc = 0; cc < HC / 32; ++cc) {
+        uint32_t r[32];
+        tmem_ld32(tl + 384 + HC * wg + 32 * cc, r);
+        tmem_wait_ld_dep(r);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) acc[32 * cc + c] = r[c];
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(leader_bar(&bars->o_empty));
+      if (q <= x.q1) {
+        float4* dst = reinterpret_cast<float4*>(p.dq + (((size_t)x.b * S + q) * p.Hq + x.h * G + g) * D + HC * wg);
+#pragma unroll
+        for (int u = 0; u < HC / 4; ++u)
+          dst[u] = make_float4(__uint_as_float(acc[4 * u]) * p.scale, __uint_as_float(acc[4 * u + 1]) * p.scale,
+                               __uint_as_float(acc[4 * u + 2]) * p.scale, __uint_as_float(acc[4 * u + 3]) * p.scale);
+      }
+    }
+  }
+
+  // neither CTA releases its tensor or shared memory while the pair still works
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc_pair(tbase, 512);
+  }
+}
+
 
 // ---------------------------------------------------------------------------
 // bwd_dkdv: key-major dK, dV
@@ -1186,8 +1686,17 @@ kvpop_status launch_bwd(BwdParams prm, const void* O, const void* dO, const floa
                              prm.w, prm.kk, prm.nL, prm.nblk, prm.cap, keys, nkeys),
                   "kvpop_attn_bwd: key lists");
   if (st != KVPOP_OK) return st;
-  // dQ
-  {
+  // dQ: CTA pairs for D = 128, single CTAs for D = 64
+  if (D == 128) {
+    auto kern = bwd_dq_pair_kernel;
+    if ((st = prepare(kern, DqPairLayout::total, "kvpop_attn_bwd: dq", kDqRegsNeeded)) != KVPOP_OK) return st;
+    BwdParams pq = prm;
+    pq.nitems = prm.nqt2 * nbh;
+    const int clusters = std::min(pq.nitems, num_sms() / 2);
+    st = cuda_check(launch_pdl(kern, dim3(2 * clusters), dim3(kDqThreads), DqPairLayout::total, cs, pq),
+                    "kvpop_attn_bwd: dq launch");
+    if (st != KVPOP_OK) return st;
+  } else {
     using L = DqLayout<D>;
     auto kern = bwd_dq_kernel<D>;
     if ((st = prepare(kern, L::total, "kvpop_attn_bwd: dq", kDqRegsNeeded)) != KVPOP_OK) return st;
@@ -1249,7 +1758,7 @@ kvpop_status bwd_sizes(int b, int S, int Hq, int H, kvpop_budget bud, BwdSizes* 
     return KVPOP_ERR_UNSUPPORTED;
   }
   z->P = 128 / z->G;
-  z->Spad = (S + 127) / 128 * 128;
+  z->Spad = (S + 255) / 256 * 256;  // whole 256-row query tiles of the CTA-pair dQ kernel for every G
   z->nblk = (S + kRows - 1) / kRows;
   z->cap = bud.s + bud.k + kRows;
   z->ctiles = (z->cap + kKeys - 1) / kKeys;
@@ -1322,8 +1831,10 @@ extern "C" kvpop_status kvpop_attn_bwd(const void* q, const void* k, const void*
     uint64_t dk4[4] = {(uint64_t)D, (uint64_t)H, (uint64_t)S, (uint64_t)b};
     uint64_t sk[3] = {(uint64_t)D * 2, (uint64_t)H * D * 2, (uint64_t)S * H * D * 2};
     uint32_t bk[4] = {64, 1, 128, 1};
+    uint32_t bk64[4] = {64, 1, 64, 1};
     if (!make_tmap_4d(&prm.tq, q, dq4, sq, bq) || !make_tmap_4d(&prm.tdo, dO, dq4, sq, bq) ||
         !make_tmap_4d(&prm.tk, k, dk4, sk, bk) || !make_tmap_4d(&prm.tv, v, dk4, sk, bk) ||
+        !make_tmap_4d(&prm.tk64, k, dk4, sk, bk64) || !make_tmap_4d(&prm.tv64, v, dk4, sk, bk64) ||
         !make_tmap_rows(&prm.tkr, k, (uint64_t)D, (uint64_t)b * S * H, 64) ||
         !make_tmap_rows(&prm.tvr, v, (uint64_t)D, (uint64_t)b * S * H, 64))
       return KVPOP_ERR_CUDA;
@@ -1356,6 +1867,7 @@ extern "C" kvpop_status kvpop_attn_bwd(const void* q, const void* k, const void*
   prm.kk = bud.k;
   prm.nL = (S + KVPOP_LIST_QBLOCK - 1) / KVPOP_LIST_QBLOCK;
   prm.nqt = (S + P - 1) / P;
+  prm.nqt2 = (S + 2 * P - 1) / (2 * P);
   prm.nblk = z.nblk;
   prm.cap = z.cap;
   prm.ctiles = z.ctiles;
