@@ -107,6 +107,12 @@ CASES = [
     (1, 2, 4, 64, 20, 2, 3, 4),           # shorter than one query tile
     (1, 1, 4, 128, 300, 0, 400, 8),       # the window covers the sequence: band pairs only
     (1, 1, 128, 64, 40, 2, 5, 6),         # G = 128: one position per query tile
+    # D = 128 runs the CTA-pair dQ kernel (256-row query tiles): its edge shapes
+    (1, 2, 1, 128, 400, 2, 30, 60),       # G = 1: 256 positions per pair of CTAs
+    (1, 1, 32, 128, 100, 2, 10, 12),      # G = 32: one position per warp
+    (1, 1, 128, 128, 40, 2, 5, 6),        # G = 128: one position per CTA
+    (1, 1, 2, 128, 1, 1, 1, 1),           # one token: the second CTA of the pair has no rows
+    (1, 2, 4, 128, 20, 2, 3, 4),          # shorter than one query tile
 ]
 
 
