@@ -82,27 +82,25 @@ __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); 
 // bwd_prep: -Delta and -LSE (log2 units) per row, in query-tile order
 // ---------------------------------------------------------------------------
 template <int D>
-__global__ void bwd_prep(const __nv_bfloat16* __restrict__ O, const __nv_bfloat16* __restrict__ dO,
-                         const float* __restrict__ lse, int b, int S, int Spad, int H, int G,
-                         float* __restrict__ nlse2, float* __restrict__ ndelta) {
+__global__ void __launch_bounds__(256) bwd_prep(const __nv_bfloat16* __restrict__ O,
+                                                const __nv_bfloat16* __restrict__ dO,
+                                                const float* __restrict__ lse, int b, int S, int Spad, int H,
+                                                int G, float* __restrict__ nlse2, float* __restrict__ ndelta) {
   grid_dep_wait();
   grid_dep_launch();
   constexpr int TPR = D / 8;  // threads per row, 8 elements each
   const int Hq = H * G;
-  const long long n = (long long)b * Spad * Hq * TPR;  // a multiple of 32 (Spad % 128 == 0)
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
-       i += (long long)gridDim.x * blockDim.x) {
-    const long long r = i / TPR;
-    const int part = (int)(i - r * TPR);
-    const int j = (int)(r % Hq);
-    const long long bq = r / Hq;
-    const int qp = (int)(bq % Spad);
-    const int bi = (int)(bq / Spad);
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  // rows of O and dO in memory order (batch, position, query head); only the
+  // lane that writes a row's results splits its index
+  const size_t n = (size_t)b * S * Hq * TPR;  // a multiple of TPR
+  const size_t n32 = (n + 31) & ~(size_t)31;   // whole warps take part in the row sums
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n32; i += stride) {
+    const bool in = i < n;
     float acc = 0.0f;
-    if (qp < S) {
-      const size_t off = (((size_t)bi * S + qp) * Hq + j) * D + part * 8;
-      const uint4 a = *reinterpret_cast<const uint4*>(O + off);
-      const uint4 c = *reinterpret_cast<const uint4*>(dO + off);
+    if (in) {
+      const uint4 a = *reinterpret_cast<const uint4*>(O + i * 8);
+      const uint4 c = *reinterpret_cast<const uint4*>(dO + i * 8);
       const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
       const __nv_bfloat162* c2 = reinterpret_cast<const __nv_bfloat162*>(&c);
 #pragma unroll
@@ -114,17 +112,36 @@ __global__ void bwd_prep(const __nv_bfloat16* __restrict__ O, const __nv_bfloat1
     }
 #pragma unroll
     for (int o = TPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (part == 0) {
+    if (in && (i & (TPR - 1)) == 0) {
+      const size_t r = i / TPR;
+      int j, qp, bi;
+      if (r < 0xffffffffull) {
+        const uint32_t r32 = (uint32_t)r, bq = r32 / (uint32_t)Hq;
+        j = (int)(r32 - bq * (uint32_t)Hq);
+        bi = (int)(bq / (uint32_t)S);
+        qp = (int)(bq - (uint32_t)bi * (uint32_t)S);
+      } else {
+        const size_t bq = r / Hq;
+        j = (int)(r - bq * Hq);
+        bi = (int)(bq / S);
+        qp = (int)(bq - (size_t)bi * S);
+      }
       const int h = j / G, g = j - h * G;
       const size_t o = (((size_t)bi * H + h) * Spad + qp) * G + g;
-      float nl2 = neg_inf();  // padded or empty rows: every probability is 0
-      if (qp < S) {
-        const float l = lse[((size_t)bi * Hq + j) * S + qp];
-        if (l != neg_inf()) nl2 = -l * 1.4426950408889634f;
-      }
-      nlse2[o] = nl2;
+      const float l = lse[((size_t)bi * Hq + j) * S + qp];
+      nlse2[o] = l != neg_inf() ? -l * 1.4426950408889634f : neg_inf();  // empty rows: every probability is 0
       ndelta[o] = -acc;
     }
+  }
+  // the padding rows [S, Spad) of every (batch, KV head): no probabilities
+  const int pad = Spad - S;
+  const size_t np = (size_t)b * H * pad * G;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < np; i += stride) {
+    const size_t bh = i / ((size_t)pad * G);
+    const int rem = (int)(i - bh * pad * G);
+    const size_t o = (bh * Spad + S) * G + rem;
+    nlse2[o] = neg_inf();
+    ndelta[o] = 0.0f;
   }
 }
 
@@ -1200,6 +1217,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDqThreads, 1)
 // ---------------------------------------------------------------------------
 // bwd_dkdv: key-major dK, dV
 // ---------------------------------------------------------------------------
+// Epilogue staging of one elementwise warp: 32 keys x 16 fp32 columns, rows
+// padded to 80 bytes (conflict-free row writes by the 32 key lanes).
+constexpr int kEpiRow = 80;
+constexpr int kEpiWarpBytes = 32 * kEpiRow;
+
 template <int NQS>
 struct KvBars {
   uint64_t kv_full, kv_empty;
@@ -1219,9 +1241,11 @@ struct KvLayout {
   static constexpr int stage_bytes = 2 * DH * kBlockBytes;         // Q then dO
   static constexpr int row_off = q_off + NQS * stage_bytes;        // stage i: 128 -LSE2 then 128 -Delta floats
   static constexpr int kmeta_off = row_off + NQS * 1024;
-  static constexpr int bar_off = kmeta_off + kKeys * 8;
+  static constexpr int epi_off = kmeta_off + kKeys * 8;          // per elementwise warp: kEpiWarpBytes
+  static constexpr int bar_off = epi_off + 8 * kEpiWarpBytes;
   static constexpr int misc_off = bar_off + (int)sizeof(KvBars<NQS>);
   static constexpr int total = misc_off + 64 + 1024;
+  static_assert(total <= 232448, "shared memory");
 };
 
 // Band item: keys [t0, t0 + 128) against rows t0 .. t0 + 126 + w.
@@ -1422,9 +1446,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
           if (!(ok = wait_bar(&bars->kv_full, n & 1, 41))) break;
           if (!(ok = wait_bar(&bars->q_full[u % NQS], (u / NQS) & 1, 42))) break;
           issue_sdp(u % NQS);
-          // K and V are read by S^T and dP^T only: once the item's last query tile
-          // has both, the next item's K/V may load behind the remaining MMAs
-          if (x.NQ == 1) mma_commit(&bars->kv_empty);
           for (int i = 0; ok && i < x.NQ; ++i, ++u) {
             const int stg = u % NQS;
             const bool more = i + 1 < x.NQ;
@@ -1433,6 +1454,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
             if (i == 0 && !(ok = wait_bar(&bars->acc_empty, (n & 1) ^ 1, 44))) break;
             issue_acc(stg, 0, i == 0);
             if (!(ok = wait_bar(&bars->p_full[1], u & 1, 46))) break;
+            // K and V are read by S^T and dP^T only, the key metadata by the
+            // elementwise warps before their first P: the next item may load once
+            // the last tile's S^T and dP^T are issued and every warp is past tile 0
+            if (x.NQ == 1) mma_commit(&bars->kv_empty);
             issue_acc(stg, 1, false);
             mma_commit(&bars->q_empty[stg]);
             if (more) {
@@ -1627,17 +1652,39 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->acc_empty);
-      const bool valid = me.x >= 0 && me.x < S;  // padding and rejected entries hold 0x7fffffff
-      if (valid) {
+      // rows of the warp's 32 keys go out 16 columns at a time through shared
+      // memory: each store (long: add) then covers 8 keys x 64 contiguous bytes
+      // instead of 32 keys x 16 bytes
+      {
         const float sc = hh == 1 ? p.scale : 1.0f;
         float* base = hh == 1 ? p.dk : p.dv;
-        float4* dst = reinterpret_cast<float4*>(base + (((size_t)x.b * S + me.x) * p.H + x.h) * D);
+        const bool valid = me.x >= 0 && me.x < S;  // padding and rejected entries hold 0x7fffffff
+        const long long roff = valid ? (((long long)x.b * S + me.x) * p.H + x.h) * D : -1;
+        const int kk = lane >> 2, c4 = lane & 3;
+        long long offs[4];
 #pragma unroll
-        for (int c4 = 0; c4 < D / 4; ++c4) {
-          const float4 val = make_float4(__uint_as_float(acc[4 * c4]) * sc, __uint_as_float(acc[4 * c4 + 1]) * sc,
-                                         __uint_as_float(acc[4 * c4 + 2]) * sc, __uint_as_float(acc[4 * c4 + 3]) * sc);
-          if (LONG) atomicAdd(dst + c4, val);
-          else dst[c4] = val;
+        for (int i = 0; i < 4; ++i) offs[i] = __shfl_sync(0xffffffffu, roff, 8 * i + kk);
+        uint8_t* stw = smem + L::epi_off + (warp - 4) * kEpiWarpBytes;
+#pragma unroll
+        for (int sl = 0; sl < D / 16; ++sl) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int c = 16 * sl + 4 * j;
+            *reinterpret_cast<float4*>(stw + lane * kEpiRow + 16 * j) =
+                make_float4(__uint_as_float(acc[c]) * sc, __uint_as_float(acc[c + 1]) * sc,
+                            __uint_as_float(acc[c + 2]) * sc, __uint_as_float(acc[c + 3]) * sc);
+          }
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float4 val = *reinterpret_cast<const float4*>(stw + (8 * i + kk) * kEpiRow + 16 * c4);
+            if (offs[i] >= 0) {
+              float* dst = base + offs[i] + 16 * sl + 4 * c4;
+              if (LONG) red_add_v4(dst, val);
+              else *reinterpret_cast<float4*>(dst) = val;
+            }
+          }
+          __syncwarp();
         }
       }
       ++n;
@@ -1674,8 +1721,8 @@ kvpop_status launch_bwd(BwdParams prm, const void* O, const void* dO, const floa
   const int nbh = b * H;
   kvpop_status st;
   {
-    const long long n = (long long)b * prm.Spad * prm.Hq * (D / 8);
-    const int blocks = (int)std::min<long long>((n + 255) / 256, 8LL * num_sms());
+    const long long n = (long long)b * S * prm.Hq * (D / 8);
+    const int blocks = (int)std::max<long long>(1, std::min<long long>((n + 255) / 256, 8LL * num_sms()));
     st = cuda_check(launch_pdl(bwd_prep<D>, dim3(blocks), dim3(256), 0, cs,
                                static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), lse, b,
                                S, prm.Spad, H, G, nlse2, ndelta),

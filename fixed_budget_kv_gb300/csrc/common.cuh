@@ -148,6 +148,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
 // async copies
 // ---------------------------------------------------------------------------
 
+// fire-and-forget add of four consecutive fp32 values to global memory
+__device__ __forceinline__ void red_add_v4(float* dst, float4 v) {
+  asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(v.x), "f"(v.y), "f"(v.z),
+               "f"(v.w)
+               : "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

@@ -113,6 +113,9 @@ CASES = [
     (1, 1, 128, 128, 40, 2, 5, 6),        # G = 128: one position per CTA
     (1, 1, 2, 128, 1, 1, 1, 1),           # one token: the second CTA of the pair has no rows
     (1, 2, 4, 128, 20, 2, 3, 4),          # shorter than one query tile
+    # long pairs: an odd key-chunk count and a last block inside one query tile (one-tile items)
+    (1, 2, 4, 128, 1040, 8, 64, 300),
+    (1, 1, 64, 128, 30, 2, 4, 6),         # G = 64: two positions per query tile
 ]
 
 
