@@ -59,6 +59,7 @@ struct BwdParams {
   CUtensorMap tq, tdo, tk, tv;  // 4-D tiles: q/dO box {64, G, P, 1}; k/v box {64, 1, 128, 1}
   CUtensorMap tk64, tv64;       // k/v box {64, 1, 64, 1} (half a key tile)
   CUtensorMap tkr, tvr;         // K, V as [b*S*H rows, D] with one-row boxes (gather4)
+  CUtensorMap tdqs;             // dq fp32 [b, S, Hq, D]: box {8, min(G, 32), 32 / min(G, 32), 1} (stores)
   const int32_t* evict_at;
   const int2* lists;
   const float* nlse2;   // [b, H, Spad, G]: -LSE * log2(e)
@@ -740,6 +741,9 @@ constexpr int kPairVOps = 32;         // gather4 ops per V tile and CTA: S view
 constexpr int kPairKPer = (kPairKOps + 2) / 3;
 constexpr int kPairVPer = (kPairVOps + 2) / 3;
 
+// dQ leaves by TMA: per elementwise warp two 1 KB slices of 32 rows x 8 fp32
+constexpr int kDqEpiWarpBytes = 2048;
+
 struct DqPairLayout {
   static constexpr int NSK = 3, NSV = 2;
   static constexpr int k_stage = 4 * kViewBytes;  // S view (2 x 8 KB), then dQ view (16 KB)
@@ -750,7 +754,8 @@ struct DqPairLayout {
   static constexpr int v_off = k_off + NSK * k_stage;
   static constexpr int meta_off = v_off + NSV * v_stage;
   static constexpr int meta_bytes = kDqMetaStages * (kKeys + 4) * 8;
-  static constexpr int bar_off = meta_off + meta_bytes;
+  static constexpr int epi_off = (meta_off + meta_bytes + 1023) / 1024 * 1024;  // TMA sources: 128 B aligned
+  static constexpr int bar_off = epi_off + 8 * kDqEpiWarpBytes;
   static constexpr int misc_off = bar_off + (int)sizeof(DqBars<NSK, NSV>);
   static constexpr int total = misc_off + 64 + 1024;
   static_assert(total <= 232448, "shared memory");
@@ -1098,7 +1103,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDqThreads, 1)
     const int wg = (warp - 4) >> 2;  // key half of each tile
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
-    const int p_row = row >> p.gshift, g = row - (p_row << p.gshift);
+    const int p_row = row >> p.gshift;
     const uint32_t tl = tbase + ((uint32_t)(quarter * 32) << 16);
     const float sl2 = p.scale_log2;
     bool ok = true;
@@ -1192,14 +1197,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDqThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(leader_bar(&bars->o_empty));
-      if (q <= x.q1) {
-        float4* dst = reinterpret_cast<float4*>(p.dq + (((size_t)x.b * S + q) * p.Hq + x.h * G + g) * D + HC * wg);
+      // the warp's 32 rows (32 / min(G, 32) positions x min(G, 32) heads, the order
+      // of a dq box) leave by TMA, 8 columns at a time through two 1 KB slices, so
+      // that the warp goes on while the stores drain; rows past S are clipped
+      const int row0 = quarter * 32;
+      const int ty = x.h * G + (row0 & (G - 1)), tz = qc + (row0 >> p.gshift);
+      if (tz < S) {
+        uint8_t* stw = smem + L::epi_off + (warp - 4) * kDqEpiWarpBytes;
 #pragma unroll
-        for (int u = 0; u < HC / 4; ++u)
-          dst[u] = make_float4(__uint_as_float(acc[4 * u]) * p.scale, __uint_as_float(acc[4 * u + 1]) * p.scale,
-                               __uint_as_float(acc[4 * u + 2]) * p.scale, __uint_as_float(acc[4 * u + 3]) * p.scale);
+        for (int sl = 0; sl < HC / 8; ++sl) {
+          uint8_t* buf = stw + (sl & 1) * 1024;
+          if (lane == 0) bulk_wait_read<1>();  // the slice stored two steps ago has been read
+          __syncwarp();
+          const int c = 8 * sl;
+          *reinterpret_cast<float4*>(buf + lane * 32) =
+              make_float4(__uint_as_float(acc[c]) * p.scale, __uint_as_float(acc[c + 1]) * p.scale,
+                          __uint_as_float(acc[c + 2]) * p.scale, __uint_as_float(acc[c + 3]) * p.scale);
+          *reinterpret_cast<float4*>(buf + lane * 32 + 16) =
+              make_float4(__uint_as_float(acc[c + 4]) * p.scale, __uint_as_float(acc[c + 5]) * p.scale,
+                          __uint_as_float(acc[c + 6]) * p.scale, __uint_as_float(acc[c + 7]) * p.scale);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_4d(&p.tdqs, buf, HC * wg + c, ty, tz, x.b);
+            bulk_commit();
+          }
+        }
       }
     }
+    if (lane == 0) bulk_wait_all();  // every dq store complete before the CTA retires
   }
 
   // neither CTA releases its tensor or shared memory while the pair still works
@@ -1885,6 +1911,10 @@ extern "C" kvpop_status kvpop_attn_bwd(const void* q, const void* k, const void*
         !make_tmap_rows(&prm.tkr, k, (uint64_t)D, (uint64_t)b * S * H, 64) ||
         !make_tmap_rows(&prm.tvr, v, (uint64_t)D, (uint64_t)b * S * H, 64))
       return KVPOP_ERR_CUDA;
+    const uint32_t gb = (uint32_t)std::min(G, 32);
+    uint64_t sq32[3] = {(uint64_t)D * 4, (uint64_t)Hq * D * 4, (uint64_t)S * Hq * D * 4};
+    uint32_t bdq[4] = {8, gb, 32 / gb, 1};
+    if (!make_tmap_4d_f32(&prm.tdqs, dq, dq4, sq32, bdq)) return KVPOP_ERR_CUDA;
   }
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   float* nlse2 = reinterpret_cast<float*>(ws);

@@ -155,6 +155,22 @@ __device__ __forceinline__ void red_add_v4(float* dst, float4 v) {
                : "memory");
 }
 
+// 4-D tiled TMA store from shared memory (bulk group of the issuing thread)
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, const void* src, int c0, int c1, int c2,
+                                             int c3) {
+  asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the issuing thread's bulk groups: all but the newest N have read their shared memory
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -624,6 +640,9 @@ namespace kvpop {
 // cuTensorMapEncodeTiled fetched through the runtime (no direct libcuda link).
 bool make_tmap_4d(CUtensorMap* map, const void* base, const uint64_t dims[4],
                   const uint64_t strides_bytes[3], const uint32_t box[4]);
+// 4-D fp32 map without swizzle (for tiled stores of fp32 results).
+bool make_tmap_4d_f32(CUtensorMap* map, const void* base, const uint64_t dims[4],
+                      const uint64_t strides_bytes[3], const uint32_t box[4]);
 // 2-D bf16 map with a one-row box of `box_cols` elements, 128-byte swizzle (for gather4).
 bool make_tmap_rows(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
                     uint32_t box_cols);
