@@ -1252,7 +1252,8 @@ template <int NQS>
 struct KvBars {
   uint64_t kv_full, kv_empty;
   uint64_t q_full[NQS], q_empty[NQS];
-  uint64_t s_full[2], p_full[2];
+  uint64_t s_full, s_free, d_full;  // S^T ready / held in registers by every warp; dP^T ready
+  uint64_t p_full[2];                 // warpgroup h packed P^T and dS^T of its rows
   uint64_t acc_full, acc_empty;
   uint64_t drain;
 };
@@ -1323,11 +1324,13 @@ __device__ __forceinline__ KvItem make_kv_item(const BwdParams& p, int it) {
 //               query tile, one key per thread (TMEM lane); then the epilogue:
 //               warpgroup 0 writes dv, warpgroup 1 dk
 // TMEM columns: dV at 0, dK at D, S^T at 256 and dP^T at 384 (N = 128: the whole
-// query tile; N = 64 halves would read the K/V operand twice from shared memory).
-// Warpgroup h owns rows 64 h .. 64 h + 63 (columns 64 h ..) and packs P^T and dS^T
-// over the first 32 of them.  MMA order per query tile u: S^T (its own commit: the
-// warpgroups compute P meanwhile), dP^T; dV, dK of rows 0-63, then of rows 64-127,
-// as each warpgroup finishes; then tile u + 1.
+// query tile; an N = 64 MMA costs an N = 128 one's cycles).  Warpgroup h owns rows
+// 64 h .. 64 h + 63 (columns 64 h ..): it loads its S^T columns into registers and
+// says so (the next S^T may then overwrite them), computes P, loads its dP^T columns,
+// computes dS and packs P^T and dS^T over those 64 dP^T columns.  MMA order per query
+// tile u: S^T of tile u + 1 (as soon as every warp holds S^T of tile u), dV, dK of
+// rows 0-63, then of rows 64-127, as each warpgroup finishes, then dP^T of tile
+// u + 1 -- so the S^T MMAs overlap the elementwise work instead of following it.
 template <int D, bool LONG>
 __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
   using L = KvLayout<D>;
@@ -1351,10 +1354,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
       mbar_init(&bars->q_full[i], 1);
       mbar_init(&bars->q_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->p_full[i], 4);
-    }
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->s_free, 8);  // every elementwise warp
+    mbar_init(&bars->d_full, 1);
+    for (int i = 0; i < 2; ++i) mbar_init(&bars->p_full[i], 4);
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->acc_empty, 8);
     mbar_init(&bars->drain, 1);
@@ -1428,40 +1431,43 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
           tc_fence_after();
           return true;
         };
-        // S^T = K Q^T and dP^T = V dO^T over the whole 128-row query tile in stage stg,
-        // committed separately so that P can be computed while dP^T runs
-        // descriptor low words stepped by constants: the issuing thread shares
-        // its SMSP with busy elementwise warps, so every MMA costs few instructions
-        auto issue_sdp = [&](int stg) {
+        // S^T = K Q^T into the S buffer once both warpgroups hold the previous S^T in
+        // registers; dP^T = V dO^T into the dP buffer once the previous tile's dV and
+        // dK products (whose A operands the warpgroups packed there) are issued.
+        // Descriptor low words stepped by constants: the issuing thread shares its
+        // SMSP with busy elementwise warps, so every MMA costs few instructions.
+        auto issue_s = [&](int stg) {
           const uint32_t ka = desc_lo(k_addr, 16), qb = desc_lo(q_stage(stg), 16);
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
             const uint32_t off = (uint32_t)(((ks >> 2) * kBlockBytes + (ks & 3) * 32) >> 4);
             mma_ss_lo(tbase + 256, ka + off, qb + off, idesc_s, ks > 0 ? 1u : 0u);
           }
-          mma_commit(&bars->s_full[0]);  // S^T: the elementwise warps start on P
+          mma_commit(&bars->s_full);
+        };
+        auto issue_dp = [&](int stg) {
           const uint32_t va = desc_lo(v_addr, 16), db = desc_lo(do_stage(stg), 16);
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
             const uint32_t off = (uint32_t)(((ks >> 2) * kBlockBytes + (ks & 3) * 32) >> 4);
             mma_ss_lo(tbase + 384, va + off, db + off, idesc_s, ks > 0 ? 1u : 0u);
           }
-          mma_commit(&bars->s_full[1]);  // dP^T
+          mma_commit(&bars->d_full);
         };
-        // dV += P^T dO and dK += dS^T Q over rows 64 h .. 64 h + 63, whose P^T and dS^T
-        // warpgroup h packed over the first 32 of its own 64 columns
+        // dV += P^T dO and dK += dS^T Q over rows 64 h .. 64 h + 63: warpgroup h packed
+        // P^T over the first 32 and dS^T over the last 32 of its 64 dP^T columns
         auto issue_acc = [&](int stg, int h, bool first) {
           constexpr uint32_t lbo = DH > 1 ? kBlockBytes : 16;
           const uint32_t db = desc_lo(do_stage(stg) + h * kHalfBytes, lbo);
           const uint32_t acc0 = first ? 0u : 1u;
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
-            mma_ts_lo(tbase, tbase + 256 + 64 * h + ks * 8, db + (uint32_t)(ks * 2048 >> 4), idesc_acc,
+            mma_ts_lo(tbase, tbase + 384 + 64 * h + ks * 8, db + (uint32_t)(ks * 2048 >> 4), idesc_acc,
                       ks > 0 ? 1u : acc0);
           const uint32_t qb = desc_lo(q_stage(stg) + h * kHalfBytes, lbo);
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
-            mma_ts_lo(tbase + D, tbase + 384 + 64 * h + ks * 8, qb + (uint32_t)(ks * 2048 >> 4), idesc_acc,
+            mma_ts_lo(tbase + D, tbase + 384 + 64 * h + 32 + ks * 8, qb + (uint32_t)(ks * 2048 >> 4), idesc_acc,
                       ks > 0 ? 1u : acc0);
         };
         bool ok = true;
@@ -1471,28 +1477,50 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
           if (x.n == 0) continue;
           if (!(ok = wait_bar(&bars->kv_full, n & 1, 41))) break;
           if (!(ok = wait_bar(&bars->q_full[u % NQS], (u / NQS) & 1, 42))) break;
-          issue_sdp(u % NQS);
+          // every warp holds the previous item's last S^T
+          if (u > 0 && !(ok = wait_bar(&bars->s_free, (u - 1) & 1, 48))) break;
+          issue_s(u % NQS);
+          issue_dp(u % NQS);
           for (int i = 0; ok && i < x.NQ; ++i, ++u) {
             const int stg = u % NQS;
             const bool more = i + 1 < x.NQ;
             const int stg1 = (u + 1) % NQS;
+            const uint32_t ph1 = ((u + 1) / NQS) & 1;
+            // the next S^T while the warpgroups compute this tile's P and dS, if its
+            // query tile has landed; otherwise after this tile's dV and dK products
+            bool s_next = !more;
+            if (more) {
+              if (!(ok = wait_bar(&bars->s_free, u & 1, 47))) break;
+              if (mbar_try_wait(&bars->q_full[stg1], ph1)) {
+                tc_fence_after();
+                issue_s(stg1);
+                s_next = true;
+              }
+            }
             if (!(ok = wait_bar(&bars->p_full[0], u & 1, 43))) break;
             if (i == 0 && !(ok = wait_bar(&bars->acc_empty, (n & 1) ^ 1, 44))) break;
             issue_acc(stg, 0, i == 0);
+            if (!s_next && mbar_try_wait(&bars->q_full[stg1], ph1)) {
+              tc_fence_after();
+              issue_s(stg1);
+              s_next = true;
+            }
             if (!(ok = wait_bar(&bars->p_full[1], u & 1, 46))) break;
-            // K and V are read by S^T and dP^T only, the key metadata by the
-            // elementwise warps before their first P: the next item may load once
-            // the last tile's S^T and dP^T are issued and every warp is past tile 0
-            if (x.NQ == 1) mma_commit(&bars->kv_empty);
             issue_acc(stg, 1, false);
             mma_commit(&bars->q_empty[stg]);
             if (more) {
-              // the next tile's S^T and dP^T overwrite the columns these products read:
-              // the tensor core runs them in issue order
-              if (!(ok = wait_bar(&bars->q_full[stg1], ((u + 1) / NQS) & 1, 45))) break;
-              issue_sdp(stg1);
-              if (i + 2 == x.NQ) mma_commit(&bars->kv_empty);
+              if (!s_next) {
+                if (!(ok = wait_bar(&bars->q_full[stg1], ph1, 45))) break;
+                issue_s(stg1);
+              }
+              // the next dP^T overwrites the columns these products read: the tensor
+              // core runs them in issue order
+              issue_dp(stg1);
             }
+            // K and V are read by S^T and dP^T only, the key metadata by the
+            // elementwise warps before their first P: the next item may load once
+            // the last tile's S^T and dP^T are issued and every warp is past tile 0
+            if (i + 2 == x.NQ || x.NQ == 1) mma_commit(&bars->kv_empty);
           }
           if (!ok) break;
           mma_commit(&bars->acc_full);
@@ -1579,19 +1607,22 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
       const int hi = LONG ? me.y : min(me.x + w, S);
       for (int i = 0; i < x.NQ; ++i, ++u) {
         const int stg = u % NQS;
-        if (!warp_wait(&bars->s_full[0], u & 1, abort_flag)) {
+        if (!warp_wait(&bars->s_full, u & 1, abort_flag)) {
           if (lane == 0) fail(SITE_ATTN_SOFTMAX, 42);
           ok = false;
           break;
         }
         tc_fence_after();
-        // P from S^T first (dP^T may still be in the tensor core), then dS
+        // S^T into registers, then the S buffer goes back for the next tile's S^T
         uint32_t sr[2][32], dr[2][32];
         const uint32_t scol = 256 + 64 * hh, dcol = 384 + 64 * hh;  // this warpgroup's 64 rows
         tmem_ld32(tl + scol, sr[0]);
         tmem_ld32(tl + scol + 32, sr[1]);
         tmem_wait_ld_dep(sr[0]);
         tmem_wait_ld_dep(sr[1]);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->s_free);
         // this half's rows: row 64 hh + c is at position pos_h + (c >> gshift);
         // the key sees the columns [clo, chi)
         const int pos_h = (x.qt0 + i) * P + ((64 * hh) >> gs);
@@ -1609,7 +1640,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
         const float4* rdl = rl2 + 32;
 #pragma unroll
         for (int ch = 0; ch < 2; ++ch) {
-          uint32_t pk[16];
 #pragma unroll
           for (int c = 0; c < 32; c += 4) {
             const float4 nl = rl2[(32 * ch + c) >> 2];  // -LSE2 of four rows (a broadcast read)
@@ -1618,15 +1648,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
               const uint64_t n2 = v2 == 0 ? pack2(nl.x, nl.y) : pack2(nl.z, nl.w);
               float e0, e1;
               unpack2(fma2(pack2(__uint_as_float(sr[ch][c + v2]), __uint_as_float(sr[ch][c + v2 + 1])), s2, n2), e0, e1);
-              const float p0 = ex2_approx(e0), p1 = ex2_approx(e1);
-              sr[ch][c + v2] = __float_as_uint(p0);  // P in fp32 for dS
-              sr[ch][c + v2 + 1] = __float_as_uint(p1);
-              pk[(c + v2) >> 1] = pack_bf16x2(p0, p1);
+              sr[ch][c + v2] = __float_as_uint(ex2_approx(e0));  // P in fp32
+              sr[ch][c + v2 + 1] = __float_as_uint(ex2_approx(e1));
             }
           }
-          tmem_st16(tl + scol + 16 * ch, pk);  // over this warpgroup's own columns
         }
-        if (!warp_wait(&bars->s_full[1], u & 1, abort_flag)) {
+        if (!warp_wait(&bars->d_full, u & 1, abort_flag)) {
           if (lane == 0) fail(SITE_ATTN_SOFTMAX, 43);
           ok = false;
           break;
@@ -1636,9 +1663,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
         tmem_ld32(tl + dcol + 32, dr[1]);
         tmem_wait_ld_dep(dr[0]);
         tmem_wait_ld_dep(dr[1]);
+        // P^T over the first 32 of the warpgroup's dP^T columns, dS^T over the last 32
 #pragma unroll
         for (int ch = 0; ch < 2; ++ch) {
-          uint32_t dk[16];
+          uint32_t pk[16], dk[16];
 #pragma unroll
           for (int c = 0; c < 32; c += 4) {
             const float4 nd = rdl[(32 * ch + c) >> 2];  // -Delta of four rows
@@ -1646,12 +1674,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
             for (int v2 = 0; v2 < 4; v2 += 2) {
               const uint64_t d2 = v2 == 0 ? pack2(nd.x, nd.y) : pack2(nd.z, nd.w);
               const uint64_t dd = add2(pack2(__uint_as_float(dr[ch][c + v2]), __uint_as_float(dr[ch][c + v2 + 1])), d2);
+              const float p0 = __uint_as_float(sr[ch][c + v2]), p1 = __uint_as_float(sr[ch][c + v2 + 1]);
               float d0, d1;
-              unpack2(fma2(pack2(__uint_as_float(sr[ch][c + v2]), __uint_as_float(sr[ch][c + v2 + 1])), dd, zero2), d0, d1);
+              unpack2(fma2(pack2(p0, p1), dd, zero2), d0, d1);
+              pk[(c + v2) >> 1] = pack_bf16x2(p0, p1);
               dk[(c + v2) >> 1] = pack_bf16x2(d0, d1);
             }
           }
-          tmem_st16(tl + dcol + 16 * ch, dk);
+          tmem_st16(tl + dcol + 16 * ch, pk);
+          tmem_st16(tl + dcol + 32 + 16 * ch, dk);
         }
         tmem_wait_st();
         tc_fence_before();
