@@ -1251,7 +1251,7 @@ constexpr int kEpiWarpBytes = 32 * kEpiRow;
 template <int NQS>
 struct KvBars {
   uint64_t kv_full, kv_empty;
-  uint64_t q_full[NQS], q_empty[NQS];
+  uint64_t q_full[NQS], o_full[NQS], q_empty[NQS];  // stage: Q (+ -LSE2) landed, dO (+ -Delta) landed
   uint64_t s_full, s_free, d_full;  // S^T ready / held in registers by every warp; dP^T ready
   uint64_t p_full[2];                 // warpgroup h packed P^T and dS^T of its rows
   uint64_t acc_full, acc_empty;
@@ -1352,6 +1352,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
     mbar_init(&bars->kv_empty, 1);
     for (int i = 0; i < NQS; ++i) {
       mbar_init(&bars->q_full[i], 1);
+      mbar_init(&bars->o_full[i], 1);
       mbar_init(&bars->q_empty[i], 1);
     }
     mbar_init(&bars->s_full, 1);
@@ -1405,16 +1406,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
               break;
             }
             const int qt = x.qt0 + i;
-            uint64_t* bar = &bars->q_full[stg];
-            mbar_arrive_expect_tx(bar, 2 * DH * kBlockBytes + 1024);
+            // Q (for the next S^T) lands on its own barrier, ahead of dO
+            uint64_t* qb = &bars->q_full[stg];
+            uint64_t* ob = &bars->o_full[stg];
             uint8_t* qs = smem + L::q_off + stg * L::stage_bytes;
-            for (int dh = 0; dh < DH; ++dh) {
-              tma_load_4d(qs + dh * kBlockBytes, &p.tq, bar, dh * 64, x.h * G, qt * P, x.b);
-              tma_load_4d(qs + (DH + dh) * kBlockBytes, &p.tdo, bar, dh * 64, x.h * G, qt * P, x.b);
-            }
             uint8_t* rs = smem + L::row_off + stg * 1024;
-            bulk_load(rs, p.nlse2 + rbase + (size_t)qt * 128, 512, bar);
-            bulk_load(rs + 512, p.ndelta + rbase + (size_t)qt * 128, 512, bar);
+            mbar_arrive_expect_tx(qb, DH * kBlockBytes + 512);
+            for (int dh = 0; dh < DH; ++dh)
+              tma_load_4d(qs + dh * kBlockBytes, &p.tq, qb, dh * 64, x.h * G, qt * P, x.b);
+            bulk_load(rs, p.nlse2 + rbase + (size_t)qt * 128, 512, qb);
+            mbar_arrive_expect_tx(ob, DH * kBlockBytes + 512);
+            for (int dh = 0; dh < DH; ++dh)
+              tma_load_4d(qs + (DH + dh) * kBlockBytes, &p.tdo, ob, dh * 64, x.h * G, qt * P, x.b);
+            bulk_load(rs + 512, p.ndelta + rbase + (size_t)qt * 128, 512, ob);
           }
         }
       }
@@ -1480,6 +1484,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
           // every warp holds the previous item's last S^T
           if (u > 0 && !(ok = wait_bar(&bars->s_free, (u - 1) & 1, 48))) break;
           issue_s(u % NQS);
+          if (!(ok = wait_bar(&bars->o_full[u % NQS], (u / NQS) & 1, 49))) break;
           issue_dp(u % NQS);
           for (int i = 0; ok && i < x.NQ; ++i, ++u) {
             const int stg = u % NQS;
@@ -1515,6 +1520,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
               }
               // the next dP^T overwrites the columns these products read: the tensor
               // core runs them in issue order
+              if (!(ok = wait_bar(&bars->o_full[stg1], ph1, 50))) break;
               issue_dp(stg1);
             }
             // K and V are read by S^T and dP^T only, the key metadata by the
