@@ -738,8 +738,8 @@ __global__ void __launch_bounds__(kDqThreads, 1) bwd_dq_kernel(const __grid_cons
 constexpr int kViewBytes = 64 * 128;  // 64 key rows x 128 bytes
 constexpr int kPairKOps = 64;         // gather4 ops per K tile and CTA: S view 32, dQ view 32
 constexpr int kPairVOps = 32;         // gather4 ops per V tile and CTA: S view
-constexpr int kPairKPer = (kPairKOps + 2) / 3;
-constexpr int kPairVPer = (kPairVOps + 2) / 3;
+constexpr int kPairKPer = (kPairKOps + 2) / 3;  // the K loader, warps 12 and 14
+constexpr int kPairVPer = (kPairVOps + 1) / 2;  // the V loader and warp 15
 
 // dQ leaves by TMA: per elementwise warp two 1 KB slices of 32 rows x 8 fp32
 constexpr int kDqEpiWarpBytes = 2048;
@@ -866,8 +866,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDqThreads, 1)
   if (warp >= 12) {
     setmaxnreg_dec<kDqRegsHelp>();
     // ---------------------------------------------------------- gather helpers
-    const bool is_v = warp >= 14;
-    const int part = 1 + (warp & 1);  // issuer 0 is the loader warp itself
+    // warps 12 and 14 (K) and 15 (V); warp 13 shares its SMSP with the MMA issuer
+    // and stays idle, so that issuing gathers does not slow the issue of MMAs
+    if (warp != 13) {
+    const bool is_v = warp == 15;
+    const int part = warp == 14 ? 2 : 1;  // part 0 is the loader warp itself
     const int per = is_v ? kPairVPer : kPairKPer;
     const int nops = is_v ? kPairVOps : kPairKOps;
     uint64_t* full = is_v ? bars->v_full : bars->k_full;
@@ -894,6 +897,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDqThreads, 1)
         if (j < x.NTg && lane < count) issue_gather(is_v, first + lane, st, rows, leader_bar(&full[st]));
         __syncwarp();
       }
+    }
     }
   } else if (warp < 4) {
     setmaxnreg_dec<kDqRegsIo>();
