@@ -50,6 +50,9 @@ CASES = [
     (1, 1, 4, 128, 600, 8, 16, 2000),     # budget covers the sequence
     (1, 1, 16, 128, 350, 3, 24, 40),      # G = 16: 8 positions per query tile
     (2, 3, 2, 128, 520, 5, 40, 70),       # G = 2, three KV heads, two sequences
+    (1, 2, 4, 128, 3000, 16, 256, 700),   # full lists (gathered tiles) and window spans over many blocks
+    (1, 1, 64, 128, 50, 2, 8, 10),        # G = 64
+    (1, 1, 128, 64, 40, 2, 5, 6),         # G = 128, D = 64: one position per query tile
 ]
 
 

@@ -116,6 +116,9 @@ CASES = [
     # long pairs: an odd key-chunk count and a last block inside one query tile (one-tile items)
     (1, 2, 4, 128, 1040, 8, 64, 300),
     (1, 1, 64, 128, 30, 2, 4, 6),         # G = 64: two positions per query tile
+    (2, 2, 4, 64, 1100, 8, 64, 300),      # D = 64: two sequences, several long-pair blocks
+    (1, 1, 1, 128, 1300, 4, 100, 300),    # G = 1 across several 512-row blocks
+    (1, 2, 8, 128, 1500, 0, 200, 500),    # s = 0, G = 8, several blocks
 ]
 
 
